@@ -1,0 +1,210 @@
+/*
+ * dpp.h -- C ABI of the displaced-patch-parallel layer library for GB300 (sm_103a).
+ *
+ * One denoising-step layer pass of DistriFusion-style displaced patch
+ * parallelism, with the P "ranks" emulated on one GPU: the feature map is cut
+ * into P row patches; each patch computes on its fresh activations spliced into
+ * stale full-size buffers left by the previous step, and a refresh kernel writes
+ * the fresh activations back as a compressed residual.
+ *   - "DistriFusion" project summary, How It Works: synchronous first step,
+ *     then asynchronous reuse of the previous step's activations.
+ *   - "OTIL for SDXL on 4x L40S", What is implemented where (Periodic layer-
+ *     context refresh; GroupNorm sync without the rest) and "Read this before
+ *     interpreting the numbers", item 3: the stale state is the conv halo rows,
+ *     the cross-slice attention K/V and the two GroupNorm scalars per group.
+ *   - "A way to reduce bandwidth requirement for xDiT" (raylight issue): send
+ *     only the compressed residual, the real change.
+ *   - "Benchmarking DistVAE", Glossary: halo rows, row bands (patchify).
+ *
+ * Conventions for every call
+ *   - Every pointer is caller-owned DEVICE memory unless stated otherwise; the
+ *     library allocates nothing, frees nothing and keeps no global state.
+ *   - Layout: NHWC == [B, L = H*W, C], row-major, contiguous.  Head h owns
+ *     channels [h*head_dim, (h+1)*head_dim).  Row patch p owns image rows
+ *     [p*H/P, (p+1)*H/P), i.e. the contiguous tokens [p*L/P, (p+1)*L/P).
+ *   - dtype: DPP_F32 (fp32 storage, fp32 SIMT arithmetic) or DPP_BF16 (bf16
+ *     storage, tcgen05 tensor cores with fp32 accumulation).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls only enqueue work; they return before it finishes.
+ *   - Return value: DPP_OK or an error code.  Argument errors are found on the
+ *     host before anything is launched.  Pointers must be 16-byte aligned
+ *     (128-bit accesses and TMA need it) unless stated otherwise.
+ *   - Device-side give-ups: every wait inside a kernel is bounded; a kernel
+ *     that gives up stores DPP_ERR_TIMEOUT into the device status word (if the
+ *     word is already 0) and returns early, leaving its output incomplete.
+ *     The environment variable DPP_DEBUG_WAIT_LIMIT (read at each call)
+ *     overrides the wait bound; 0 makes every such wait give up at once.
+ */
+#ifndef DPP_H_
+#define DPP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define DPP_OK 0
+#define DPP_ERR_NULL 1        /* a required pointer is NULL */
+#define DPP_ERR_SHAPE 2       /* a size is out of range or not a supported multiple */
+#define DPP_ERR_ALIGN 3       /* a pointer is not aligned as required */
+#define DPP_ERR_DTYPE 4       /* dtype is neither DPP_F32 nor DPP_BF16 */
+#define DPP_ERR_CUDA 5        /* a CUDA runtime/driver call failed */
+#define DPP_ERR_TIMEOUT 6     /* device status: a bounded wait gave up */
+#define DPP_ERR_BOUNDS 7      /* device status: an index check failed (debug builds) */
+#define DPP_ERR_UNSUPPORTED 8 /* the combination is not implemented */
+#define DPP_ERR_ARG 9         /* an enum/flag argument is invalid */
+
+#define DPP_F32 0
+#define DPP_BF16 1
+
+#define DPP_SYNC 0  /* warm-up / periodic refresh step: stale := fresh before use */
+#define DPP_STALE 1 /* steady step: use the stale state as given */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* dpp_status_string(int status);
+
+/* Library ABI version (major*100 + minor). */
+int dpp_version(void);
+
+/*
+ * refresh_residual -- compressed-residual refresh of a flat stale buffer, in place.
+ * ("A way to reduce bandwidth requirement for xDiT": send the compressed
+ * residual; the quantiser is block int8 with one fp32 scale per 128 elements.)
+ *
+ * For each block of 128 consecutive elements [128*j, min(128*j+128, n)):
+ *   d_i = f32(fresh_i) - f32(stale_i);  a = max |d_i|;  s = a / 127 (IEEE);
+ *   q_i = s == 0 ? 0 : clamp(rint(d_i / s), -127, 127)   (ties to even);
+ *   stale_i = store(fmaf(q_i, s, f32(stale_i)))  with store = bf16 RNE or fp32;
+ *   codes[i] = q_i;  scales[j] = s.
+ * fresh, stale: [n] elements of `dtype`.  codes: [n] int8.  scales: [ceil(n/128)]
+ * fp32 (4-byte alignment suffices).  n == 0 is a no-op.  Values must be finite.
+ * The codes/scales pair is the message a rank would send; stale holds what every
+ * receiver reconstructs.  Bit-exact across runs and against an IEEE CPU evaluation.
+ */
+int refresh_residual(const void* fresh, void* stale, int8_t* codes, float* scales,
+                     int64_t n, int dtype, void* stream);
+
+/*
+ * halo_conv3x3 -- 3x3 "same" convolution of each row band with stale halo rows.
+ * ("Benchmarking DistVAE", Glossary: halo; "OTIL for SDXL on 4x L40S", item 3.)
+ *
+ * out[b,r,c,o] = sum_{i,j in {-1,0,1}} sum_k w[o,i+1,j+1,k] * yhat[b,r+i,c+j,k]
+ * where, for r in band p = [r0, r1): yhat = y_fresh inside [r0, r1), y_stale
+ * for rows r0-1 and r1, and 0 outside the image (rows < 0, >= H; cols < 0, >= W).
+ * y_fresh, y_stale: [B,H,W,Cin]; w: [Cout,3,3,Cin]; out: [B,H,W,Cout]; all `dtype`.
+ * With y_stale == y_fresh the result is the unbanded convolution.
+ * Requires H % P == 0.  DPP_BF16 also requires Cin % 64 == 0, Cout % 128 == 0,
+ * W % 128 == 0 or 128 % W == 0, and (H/P)*W % 128 == 0.
+ * dev_status: device int (may be NULL) that receives a give-up code.
+ */
+int halo_conv3x3(const void* y_fresh, const void* y_stale, const void* w, void* out,
+                 int B, int H, int W, int Cin, int Cout, int P, int dtype,
+                 int* dev_status, void* stream);
+
+/*
+ * stale_kv_attention -- per-patch attention of fresh queries over spliced K/V.
+ * ("OTIL for SDXL on 4x L40S", item 3 and Periodic layer-context refresh: the
+ * cross-slice attention K/V are stale; Self-tests: own slice fresh, never a blend.)
+ *
+ * For token t in patch p (tokens [p*L/P, (p+1)*L/P)) and head h:
+ *   o[t,h] = sum_s softmax_s(q[t,h] . Khat_p[s,h] / sqrt(head_dim)) Vhat_p[s,h]
+ * Khat_p[s] = k_fresh[s] for s in patch p, else k_stale[s]; same for Vhat.  All L
+ * keys, no mask.  q, k_*, v_*, o: [B, L, heads*head_dim] of `dtype`.
+ * Requires head_dim == 64, L % P == 0 and (L/P) % 8 == 0.
+ * dev_status: device int (may be NULL) that receives a give-up code.
+ */
+int stale_kv_attention(const void* q, const void* k_fresh, const void* v_fresh,
+                       const void* k_stale, const void* v_stale, void* o,
+                       int B, int L, int heads, int head_dim, int P, int dtype,
+                       int* dev_status, void* stream);
+
+/* ---------------------------------------------------------------- layer step */
+
+typedef struct dpp_layer_params {
+  int B, H, W, C;  /* feature map [B,H,W,C] */
+  int P;           /* row patches (virtual ranks); H % P == 0 */
+  int G;           /* GroupNorm groups; C % G == 0 */
+  int heads;       /* attention heads; C == heads * head_dim */
+  int head_dim;    /* must be 64 */
+  int dtype;       /* DPP_F32 or DPP_BF16 */
+  int refresh;     /* DPP_STALE only: 1 = refresh the state, 0 = leave it (no_sync) */
+  float eps;       /* GroupNorm epsilon */
+} dpp_layer_params;
+
+typedef struct dpp_layer_weights {
+  const float* gamma; /* [C] fp32 GroupNorm scale */
+  const float* beta;  /* [C] fp32 GroupNorm shift */
+  const void* w_conv; /* [C,3,3,C] `dtype` conv weight (no bias) */
+  const void* w_qkv;  /* [3C,C] `dtype`: rows [0,C) = Wq, [C,2C) = Wk, [2C,3C) = Wv */
+  const void* w_o;    /* [C,C] `dtype` output projection */
+} dpp_layer_weights;
+
+typedef struct dpp_layer_state {
+  float* gn_stats; /* [B,P,G,2] fp32: (sum x, sum x^2) of each patch, previous step */
+  void* y_stale;   /* [B,H,W,C] `dtype`: previous conv input; only the 2(P-1) halo
+                      rows per batch (rows r-1, r at each boundary r) are read/written */
+  void* k_stale;   /* [B,L,C] `dtype` previous keys */
+  void* v_stale;   /* [B,L,C] `dtype` previous values */
+  int8_t* codes;   /* [dpp_message_elems] int8 residual codes (message order: K, V,
+                      then for each batch the P-1 halo ranges of 2*W*C elements) */
+  float* scales;   /* [dpp_message_blocks] fp32 block scales, same order */
+} dpp_layer_state;
+
+/* Byte offsets of the pieces of the caller-allocated workspace (all 256-aligned). */
+typedef struct dpp_workspace_layout {
+  size_t status;     /* int device status word (zeroed by each patch_layer_step) */
+  size_t gn_partial; /* fp32 per-chunk GroupNorm partial sums */
+  size_t gn_fresh;   /* [B,P,G,2] fp32 fresh sums of this step */
+  size_t y;          /* [B,H,W,C] GroupNorm output (conv input) */
+  size_t h;          /* [B,H,W,C] conv output */
+  size_t q, k, v;    /* [B,L,C] fresh projections */
+  size_t o;          /* [B,L,C] attention output */
+  size_t total;      /* bytes to allocate */
+} dpp_workspace_layout;
+
+/* Fills *out for these params; returns a status (argument checks as below). */
+int dpp_workspace_query(const dpp_layer_params* prm, dpp_workspace_layout* out);
+/* Workspace bytes for these params, or 0 if the params are invalid. */
+size_t dpp_workspace_size(const dpp_layer_params* prm);
+/* Number of int8 codes / fp32 scales in one refresh message of this layer. */
+int64_t dpp_message_elems(const dpp_layer_params* prm);
+int64_t dpp_message_blocks(const dpp_layer_params* prm);
+
+/*
+ * patch_layer_step -- one layer pass of all P virtual ranks, then the state update.
+ *   a1  fresh GroupNorm sums of every patch;
+ *   a2  GroupNorm of patch p with its fresh sums + the other patches' stale sums;
+ *   a3  halo conv3x3 (halo rows from state->y_stale);
+ *   a4  Q, K, V = h . Wq^T, h . Wk^T, h . Wv^T;
+ *   a5  stale-KV attention (own rows of K/V fresh, others from the state);
+ *   a6  out = O . Wo^T;
+ *   a7/a8 state update (after all patches have read the old state):
+ *     DPP_SYNC: stale := fresh is used in a1-a6, then the state is written
+ *       exactly (GN sums, halo rows of y, K, V); codes/scales are not touched.
+ *     DPP_STALE, refresh = 1: refresh_residual of K, V and the halo rows of y
+ *       (message in codes/scales), GN sums copied exactly.
+ *     DPP_STALE, refresh = 0 (no_sync): the state is left untouched.
+ * x, out: [B,H,W,C] `dtype`.  workspace: dpp_workspace_size() bytes, 256-aligned.
+ * Requirements: those of halo_conv3x3 (Cin = Cout = C) and stale_kv_attention
+ * (L = H*W), C % G == 0, C == heads*64, and for DPP_BF16 C % 128 == 0.
+ * The device status word is zeroed at the start of each call.
+ */
+int patch_layer_step(const dpp_layer_params* prm, const dpp_layer_weights* wts,
+                     const dpp_layer_state* st, const void* x, void* out, int mode,
+                     void* workspace, void* stream);
+
+/* Synchronizes `stream` and returns the workspace's device status word
+ * (DPP_OK, DPP_ERR_TIMEOUT, ...), or DPP_ERR_CUDA if the copy fails. */
+int dpp_read_device_status(const void* workspace, void* stream);
+
+/* Number of kernels one patch_layer_step launches for these params and mode. */
+int dpp_layer_kernel_count(const dpp_layer_params* prm, int mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DPP_H_ */
