@@ -1,0 +1,350 @@
+"""Benchmark of the displaced-patch layer step on GB300.
+
+A step is one patch_layer_step (DPP_STALE with refresh) of the SDXL-1024
+mid-level workload: bf16, B=2 (CFG halves), 64x64 map, C=640, P=4 row patches,
+GroupNorm 32 groups, 10 heads x 64, conv3x3 640->640 -- GroupNorm with spliced
+statistics, halo conv, QKV projection, stale-KV attention, output projection and
+the compressed-residual refresh of K, V and the conv halo rows.
+
+Timed region: W warm-up steps, then exactly K steps with a barrier and a device
+synchronize on both sides; the L2 is flushed (a 256 MiB write, outside the step
+events) before every timed step.  Each step's stage boundaries carry CUDA events
+recorded on the launch stream inside the library, which gives the per-kernel
+times used for the roofline lines.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (test infrastructure) on the host cores on
+a bounded sample of the same workload.  Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "patch-layer steps/s; attention TFLOP/s & refresh GB/s as % of GB300 roofline"
+WORKLOAD = "sdxl1024_mid_b2_64x64_c640_p4_bf16"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return dict(hbm=m["hbm_gbs"], bf16=m["bf16_tflops"], bf16_sus=m["bf16_tflops_sustained"],
+                    src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    lrank = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, lrank
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _layer_setup(dev):
+    import torch
+
+    import stale_activations_gb300 as dpp
+    import synth
+    cfg = synth.SDXL1024_MID
+    wts = synth.layer_weights(cfg, seed=0)
+    x, x_prev = synth.layer_inputs(cfg, seed=0)
+    prm = dpp.make_params(cfg.B, cfg.H, cfg.W, cfg.C, cfg.P, cfg.G, cfg.heads, dpp.BF16,
+                          refresh=True, eps=cfg.eps)
+    state, ws = dpp.alloc_layer(prm, device=dev)
+    wd = {k: v.to(dev) for k, v in wts.items()}
+    xd, xpd = x.to(dev), x_prev.to(dev)
+    out = torch.empty_like(xd)
+    # the stale state of this step is what the synchronous step over x_prev leaves
+    dpp.patch_layer_step(prm, wd, state, xpd, out, dpp.SYNC, ws)
+    return cfg, prm, wd, state, ws, x, xd, out
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as tdist
+
+    import stale_activations_gb300 as dpp
+
+    ws_n, rank, lrank = _dist()
+    torch.cuda.set_device(lrank)
+    dev = torch.device("cuda", lrank)
+    if ws_n > 1:
+        tdist.init_process_group("nccl", device_id=dev)
+    dpp.load()
+    peaks = _peaks()
+    cfg, prm, wd, state, wsb, x_host, xd, out = _layer_setup(dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    nst = dpp.NUM_STAGE_EVENTS
+
+    def step(evs=None):
+        dpp.patch_layer_step(prm, wd, state, xd, out, dpp.STALE, wsb, stage_events=evs)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if dpp.read_device_status(wsb) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    K = args.steps
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(K)]
+
+    def barrier():
+        if ws_n > 1:
+            tdist.barrier()
+        torch.cuda.synchronize()
+
+    with ClockSampler(lrank) as clocks:
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(K):
+            flush.fill_(1)
+            step(events[i])
+        barrier()
+        wall = time.perf_counter() - t0
+    st = dpp.read_device_status(wsb)
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the timed region")
+    stage_ms = [[events[i][s].elapsed_time(events[i][s + 1]) for s in range(nst - 1)]
+                for i in range(K)]
+    step_ms = [events[i][0].elapsed_time(events[i][nst - 1]) for i in range(K)]
+    tot_ms = sum(step_ms)
+    if ws_n > 1:
+        t = torch.tensor([tot_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        tot_ms = t.item()
+    ms_per_step = tot_ms / K
+    value = ws_n * K / (tot_ms / 1e3)
+
+    # per-stage averages and the roofline of the dominant kernel (attention)
+    avg = {name: sum(r[i] for r in stage_ms) / K for i, name in enumerate(dpp.STAGES)}
+    B, L, C, P = cfg.B, cfg.L, cfg.C, cfg.P
+    attn_flop = 4.0 * B * cfg.heads * L * L * cfg.head_dim
+    conv_flop = 2.0 * B * L * C * 9 * C
+    qkv_flop = 2.0 * B * L * C * 3 * C
+    o_flop = 2.0 * B * L * C * C
+    act = B * L * C
+    gn_bytes = 3 * act * 2             # read x (stats), read x + write y (apply)
+    halo_elems = B * (P - 1) * 2 * cfg.W * C
+    refresh_elems = 2 * act + halo_elems
+    refresh_bytes = 7.03125 * refresh_elems
+    attn_tfs = attn_flop / (avg["attention"] * 1e-3) / 1e12
+    kernels = {
+        "groupnorm": {"ms": avg["groupnorm"], "GB/s": gn_bytes / (avg["groupnorm"] * 1e-3) / 1e9},
+        "halo_conv": {"ms": avg["halo_conv"], "TFLOP/s": conv_flop / (avg["halo_conv"] * 1e-3) / 1e12},
+        "qkv_proj": {"ms": avg["qkv_proj"], "TFLOP/s": qkv_flop / (avg["qkv_proj"] * 1e-3) / 1e12},
+        "attention": {"ms": avg["attention"], "TFLOP/s": attn_tfs},
+        "out_proj": {"ms": avg["out_proj"], "TFLOP/s": o_flop / (avg["out_proj"] * 1e-3) / 1e12},
+        "state_update": {"ms": avg["state_update"],
+                         "GB/s": refresh_bytes / (avg["state_update"] * 1e-3) / 1e9},
+    }
+    for k, v in kernels.items():
+        if "GB/s" in v:
+            v["frac_hbm"] = v["GB/s"] / peaks["hbm"]
+        else:
+            v["frac_bf16_sustained"] = v["TFLOP/s"] / peaks["bf16_sus"]
+    roofline = {"kernel": "stale_kv_attention (tc_attn_kernel)", "bound": "tensor",
+                "achieved": attn_tfs, "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
+                "frac": attn_tfs / peaks["bf16_sus"], "traffic": None,
+                "peak_kind": f"bf16 dense sustained, {peaks['src']}",
+                "algorithmic": f"4*B*heads*L^2*d = {attn_flop:.4g} FLOP per launch"}
+
+    # end to end through the public API with host buffers (pinned), copies timed
+    x_pin = x_host.pin_memory()
+    out_pin = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e2e_ms = 0.0
+    for i in range(K):
+        flush.fill_(1)
+        e0.record(stream)
+        xd.copy_(x_pin, non_blocking=True)
+        step()
+        out_pin.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    barrier()
+    if ws_n > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        e2e_ms = t.item()
+    e2e = {"value": ws_n * K / (e2e_ms / 1e3), "unit": "steps/s",
+           "h2d_bytes_per_step": x_pin.numel() * x_pin.element_size(),
+           "d2h_bytes_per_step": out_pin.numel() * out_pin.element_size()}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": ws_n, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": cfg.H, "W": cfg.W, "C": C, "P": P,
+                   "G": cfg.G, "heads": cfg.heads, "head_dim": cfg.head_dim,
+                   "mode": "DPP_STALE+refresh", "parallelism": f"replicas x{ws_n}",
+                   "l2": "flushed (256 MiB write) before every timed step"},
+        "roofline": roofline, "kernels": kernels, "e2e": e2e,
+        "gpu_launches": dpp.layer_kernel_count(prm, dpp.STALE) * K,
+        "wall_s_timed_region": wall,
+    }
+    line["clocks"] = clocks.summary()
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
+    if ws_n > 1:
+        tdist.barrier()
+        tdist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+# ------------------------------------------------------------------ CPU oracle (reference arm)
+def _oracle_case():
+    import numpy as np
+
+    import oracle
+    import synth
+    cfg = synth.SDXL1024_MID
+    wts = synth.layer_weights(cfg, seed=0)
+    x, x_prev = synth.layer_inputs(cfg, seed=0)
+    wn = {k: v.double().numpy() for k, v in wts.items()}
+    st0 = oracle.empty_state(cfg.B, cfg.H, cfg.W, cfg.C, cfg.P, cfg.G)
+    _, state, _, _ = oracle.patch_layer_step(x_prev.double().numpy(), st0, wn, cfg.P, cfg.G,
+                                             cfg.heads, cfg.eps, "bf16", oracle.SYNC)
+    return cfg, wn, np.asarray(x.double().numpy()), state
+
+
+def _oracle_step(case):
+    import oracle
+    cfg, wn, x, state = case
+    return oracle.patch_layer_step(x, state, wn, cfg.P, cfg.G, cfg.heads, cfg.eps, "bf16",
+                                   oracle.STALE, refresh=True)
+
+
+def cpu_baseline(budget_s: float):
+    """The oracle, as it is, on this host: whole STALE layer steps of the same
+    workload, as many as fit in the budget (at least one)."""
+    case = _oracle_case()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(case)
+        n += 1
+        el = time.perf_counter() - t0
+        if el > budget_s or n >= 3:
+            break
+    return {"value": n / el, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} full oracle layer step(s) of {WORKLOAD} (numpy fp64 with its BLAS "
+                      f"threads + C refresh), {el:.1f} s"}
+
+
+def run_reference(args):
+    ws_n, rank, _ = _dist()
+    if rank != 0:
+        return
+    case = _oracle_case()
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        _oracle_step(case)
+    K = args.steps
+    t0 = time.perf_counter()
+    for _ in range(K):
+        _oracle_step(case)
+    el = time.perf_counter() - t0
+    v = K / el
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": ws_n,
+            "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * el / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": 2, "H": 64, "W": 64, "C": 640, "P": 4,
+                       "G": 32, "heads": 10, "head_dim": 64, "mode": "DPP_STALE+refresh"},
+            "cpu_baseline": {"value": v, "unit": "steps/s", "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": f"{K} full oracle layer steps (one warm-up), {el:.1f} s"},
+            "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-budget-s", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -196,6 +196,16 @@ int patch_layer_step(const dpp_layer_params* prm, const dpp_layer_weights* wts,
                      const dpp_layer_state* st, const void* x, void* out, int mode,
                      void* workspace, void* stream);
 
+/* Same as patch_layer_step, and records stage_events[i] (cudaEvent_t, created by the
+ * caller) on `stream` at each stage boundary: [0] start, [1] after GroupNorm (a1+a2),
+ * [2] after the halo conv, [3] after the QKV projection, [4] after the attention,
+ * [5] after the output projection, [6] after the state update.  stage_events may be
+ * NULL (then no event is recorded). */
+#define DPP_NUM_STAGE_EVENTS 7
+int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights* wts,
+                           const dpp_layer_state* st, const void* x, void* out, int mode,
+                           void* workspace, void* stream, void* const* stage_events);
+
 /* Synchronizes `stream` and returns the workspace's device status word
  * (DPP_OK, DPP_ERR_TIMEOUT, ...), or DPP_ERR_CUDA if the copy fails. */
 int dpp_read_device_status(const void* workspace, void* stream);

@@ -128,7 +128,7 @@ def gn_apply_spliced(x: np.ndarray, fresh: np.ndarray, stale: np.ndarray, gamma,
 
 # ---------------------------------------------------------------- halo conv
 def halo_conv3x3(y_fresh: np.ndarray, y_stale: np.ndarray, w: np.ndarray, P: int,
-                 dtype: str) -> np.ndarray:
+                 dtype: str, rows=None) -> np.ndarray:
     """3x3 "same" convolution of each row band, its halo rows taken from the stale map.
 
     "Benchmarking DistVAE", Glossary (halo: the neighbouring rows a sharded
@@ -138,27 +138,35 @@ def halo_conv3x3(y_fresh: np.ndarray, y_stale: np.ndarray, w: np.ndarray, P: int
       h[b,r,c,o] = sum_{i,j in -1..1} sum_k w[o, i+1, j+1, k] * yhat[b, r+i, c+j, k]
     yhat = fresh y inside the band, stale y for rows r0-1 and r1, zero outside
     the image (rows and columns).  w is [Cout, 3, 3, Cin].
+
+    ``rows``: optional sorted output rows to evaluate (each output row depends
+    only on its own three source rows); the result is then [B, len(rows), W, Cout].
     """
     B, H, W, Cin = y_fresh.shape
     Cout = w.shape[0]
     yf = np.asarray(y_fresh, dtype=np.float64)
     ys = np.asarray(y_stale, dtype=np.float64)
     w = np.asarray(w, dtype=np.float64)
-    h = np.empty((B, H, W, Cout))
+    sel = np.arange(H) if rows is None else np.asarray(rows)
+    h = np.empty((B, len(sel), W, Cout))
     for p in range(P):
         r0, r1 = patch_rows(H, P, p)
         Hp = r1 - r0
+        mine = np.nonzero((sel >= r0) & (sel < r1))[0]
+        if mine.size == 0:
+            continue
         yhat = np.zeros((B, Hp + 2, W + 2, Cin))
         yhat[:, 1:Hp + 1, 1:W + 1] = yf[:, r0:r1]
         if r0 > 0:
             yhat[:, 0, 1:W + 1] = ys[:, r0 - 1]
         if r1 < H:
             yhat[:, Hp + 1, 1:W + 1] = ys[:, r1]
-        acc = np.zeros((B, Hp, W, Cout))
+        loc = sel[mine] - r0                      # output rows within the band
+        acc = np.zeros((B, len(loc), W, Cout))
         for i in range(3):
             for j in range(3):
-                acc += yhat[:, i:i + Hp, j:j + W, :] @ w[:, i, j, :].T
-        h[:, r0:r1] = acc
+                acc += yhat[:, loc + i, j:j + W, :] @ w[:, i, j, :].T
+        h[:, mine] = acc
     return to_storage(h, dtype)
 
 

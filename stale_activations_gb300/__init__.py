@@ -1,0 +1,263 @@
+"""Displaced-patch-parallel layer step on GB300: thin Python binding of libdpp.so.
+
+The library (``csrc/``, declared in ``include/dpp.h``) does every step of the
+path in its own CUDA kernels; this module only marshals torch tensors (device
+memory and streams) into the C ABI's plain pointers and sizes, and raises
+``DppError`` on a non-zero status.  There is no fallback: if the library has not
+been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "DppError", "load", "F32", "BF16", "SYNC", "STALE", "LayerParams", "LayerWeights",
+    "LayerState", "WorkspaceLayout", "refresh_residual", "halo_conv3x3", "stale_kv_attention",
+    "patch_layer_step", "workspace_layout", "workspace_size", "message_sizes",
+    "read_device_status", "layer_kernel_count", "status_string", "dtype_code",
+]
+
+F32, BF16 = 0, 1
+SYNC, STALE = 0, 1
+_c_int, _c_void = ctypes.c_int, ctypes.c_void_p
+
+
+class DppError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: status {code} ({status_string(code)})")
+
+
+class LayerParams(ctypes.Structure):
+    _fields_ = [("B", _c_int), ("H", _c_int), ("W", _c_int), ("C", _c_int), ("P", _c_int),
+                ("G", _c_int), ("heads", _c_int), ("head_dim", _c_int), ("dtype", _c_int),
+                ("refresh", _c_int), ("eps", ctypes.c_float)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [("gamma", _c_void), ("beta", _c_void), ("w_conv", _c_void), ("w_qkv", _c_void),
+                ("w_o", _c_void)]
+
+
+class LayerState(ctypes.Structure):
+    _fields_ = [("gn_stats", _c_void), ("y_stale", _c_void), ("k_stale", _c_void),
+                ("v_stale", _c_void), ("codes", _c_void), ("scales", _c_void)]
+
+
+class WorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("status", "gn_partial", "gn_fresh", "y", "h", "q", "k", "v", "o", "total")]
+
+
+_lib = None
+EXPORTS = ("dpp_status_string", "dpp_version", "refresh_residual", "halo_conv3x3",
+           "stale_kv_attention", "dpp_workspace_query", "dpp_workspace_size", "dpp_message_elems",
+           "dpp_message_blocks", "patch_layer_step", "patch_layer_step_timed",
+           "dpp_read_device_status", "dpp_layer_kernel_count")
+
+
+def load(build_if_missing: bool = False):
+    """Load libdpp.so (optionally building it first).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise DppError(-1, f"CUDA library not built ({path}); run __graft_entry__.build()")
+        _build.build_library()
+    lib = ctypes.CDLL(path)
+    P, I64 = ctypes.POINTER, ctypes.c_int64
+    lib.dpp_status_string.restype = ctypes.c_char_p
+    lib.dpp_status_string.argtypes = [_c_int]
+    lib.dpp_version.restype = _c_int
+    lib.refresh_residual.restype = _c_int
+    lib.refresh_residual.argtypes = [_c_void, _c_void, _c_void, _c_void, I64, _c_int, _c_void]
+    lib.halo_conv3x3.restype = _c_int
+    lib.halo_conv3x3.argtypes = [_c_void] * 4 + [_c_int] * 7 + [_c_void, _c_void]
+    lib.stale_kv_attention.restype = _c_int
+    lib.stale_kv_attention.argtypes = [_c_void] * 6 + [_c_int] * 6 + [_c_void, _c_void]
+    lib.dpp_workspace_query.restype = _c_int
+    lib.dpp_workspace_query.argtypes = [P(LayerParams), P(WorkspaceLayout)]
+    lib.dpp_workspace_size.restype = ctypes.c_size_t
+    lib.dpp_workspace_size.argtypes = [P(LayerParams)]
+    lib.dpp_message_elems.restype = I64
+    lib.dpp_message_elems.argtypes = [P(LayerParams)]
+    lib.dpp_message_blocks.restype = I64
+    lib.dpp_message_blocks.argtypes = [P(LayerParams)]
+    lib.patch_layer_step.restype = _c_int
+    lib.patch_layer_step.argtypes = [P(LayerParams), P(LayerWeights), P(LayerState), _c_void,
+                                     _c_void, _c_int, _c_void, _c_void]
+    lib.patch_layer_step_timed.restype = _c_int
+    lib.patch_layer_step_timed.argtypes = [P(LayerParams), P(LayerWeights), P(LayerState), _c_void,
+                                           _c_void, _c_int, _c_void, _c_void, _c_void]
+    lib.dpp_read_device_status.restype = _c_int
+    lib.dpp_read_device_status.argtypes = [_c_void, _c_void]
+    lib.dpp_layer_kernel_count.restype = _c_int
+    lib.dpp_layer_kernel_count.argtypes = [P(LayerParams), _c_int]
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    if _lib is None:
+        return "library not loaded"
+    return _lib.dpp_status_string(code).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise DppError(rc, where)
+
+
+def dtype_code(t) -> int:
+    dt = t.dtype if isinstance(t, torch.Tensor) else t
+    if dt == torch.bfloat16:
+        return BF16
+    if dt == torch.float32:
+        return F32
+    raise DppError(4, f"unsupported dtype {dt}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise DppError(1, "tensor is not on a CUDA device")
+    if not t.is_contiguous():
+        raise DppError(2, "tensor is not contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def refresh_residual(fresh, stale, codes, scales, stream=None):
+    """Refresh ``stale`` in place from ``fresh``; writes int8 ``codes`` and fp32 ``scales``."""
+    lib = load()
+    _check(lib.refresh_residual(_ptr(fresh), _ptr(stale), _ptr(codes), _ptr(scales),
+                                fresh.numel(), dtype_code(fresh), _stream(stream)),
+           "refresh_residual")
+
+
+def halo_conv3x3(y_fresh, y_stale, w, out, P: int, dev_status=None, stream=None):
+    lib = load()
+    B, H, W, Cin = y_fresh.shape
+    Cout = w.shape[0]
+    _check(lib.halo_conv3x3(_ptr(y_fresh), _ptr(y_stale), _ptr(w), _ptr(out), B, H, W, Cin, Cout,
+                            P, dtype_code(y_fresh), _ptr(dev_status), _stream(stream)),
+           "halo_conv3x3")
+
+
+def stale_kv_attention(q, k_fresh, v_fresh, k_stale, v_stale, o, heads: int, P: int,
+                       dev_status=None, stream=None):
+    lib = load()
+    B, L, C = q.shape
+    _check(lib.stale_kv_attention(_ptr(q), _ptr(k_fresh), _ptr(v_fresh), _ptr(k_stale),
+                                  _ptr(v_stale), _ptr(o), B, L, heads, C // heads, P,
+                                  dtype_code(q), _ptr(dev_status), _stream(stream)),
+           "stale_kv_attention")
+
+
+def make_params(B, H, W, C, P, G, heads, dtype, refresh=True, eps=1e-5, head_dim=64):
+    return LayerParams(B, H, W, C, P, G, heads, head_dim, dtype, 1 if refresh else 0, eps)
+
+
+def workspace_layout(prm: LayerParams) -> WorkspaceLayout:
+    lo = WorkspaceLayout()
+    _check(load().dpp_workspace_query(ctypes.byref(prm), ctypes.byref(lo)), "dpp_workspace_query")
+    return lo
+
+
+def workspace_size(prm: LayerParams) -> int:
+    return workspace_layout(prm).total
+
+
+def message_sizes(prm: LayerParams):
+    lib = load()
+    return lib.dpp_message_elems(ctypes.byref(prm)), lib.dpp_message_blocks(ctypes.byref(prm))
+
+
+def layer_kernel_count(prm: LayerParams, mode: int) -> int:
+    return load().dpp_layer_kernel_count(ctypes.byref(prm), mode)
+
+
+NUM_STAGE_EVENTS = 7
+STAGES = ("groupnorm", "halo_conv", "qkv_proj", "attention", "out_proj", "state_update")
+
+
+def patch_layer_step(prm: LayerParams, weights: dict, state: dict, x, out, mode: int, workspace,
+                     stream=None, stage_events=None):
+    """One layer pass of all P virtual ranks plus the state update.
+
+    weights: gamma, beta (fp32 [C]), w_conv [C,3,3,C], w_qkv [3C,C], w_o [C,C].
+    state:   gn_stats [B,P,G,2] fp32, y_stale [B,H,W,C], k_stale/v_stale [B,L,C],
+             codes int8 [message elems], scales fp32 [message blocks].
+    workspace: uint8 device tensor of workspace_size(prm) bytes.
+    """
+    lib = load()
+    w = LayerWeights(_ptr(weights["gamma"]), _ptr(weights["beta"]), _ptr(weights["w_conv"]),
+                     _ptr(weights["w_qkv"]), _ptr(weights["w_o"]))
+    s = LayerState(_ptr(state["gn_stats"]), _ptr(state["y_stale"]), _ptr(state["k_stale"]),
+                   _ptr(state["v_stale"]), _ptr(state.get("codes")), _ptr(state.get("scales")))
+    if stage_events is None:
+        _check(lib.patch_layer_step(ctypes.byref(prm), ctypes.byref(w), ctypes.byref(s), _ptr(x),
+                                    _ptr(out), mode, _ptr(workspace), _stream(stream)),
+               "patch_layer_step")
+        return
+    if len(stage_events) != NUM_STAGE_EVENTS:
+        raise DppError(9, "stage_events needs 7 torch.cuda.Event objects")
+    evs = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[e.cuda_event for e in stage_events])
+    _check(lib.patch_layer_step_timed(ctypes.byref(prm), ctypes.byref(w), ctypes.byref(s),
+                                      _ptr(x), _ptr(out), mode, _ptr(workspace), _stream(stream),
+                                      evs),
+           "patch_layer_step_timed")
+
+
+def read_device_status(workspace, stream=None) -> int:
+    return load().dpp_read_device_status(_ptr(workspace), _stream(stream))
+
+
+# ------------------------------------------------------------------ helpers for callers
+def alloc_layer(prm: LayerParams, device="cuda"):
+    """Allocates (with torch) the state, message and workspace of one layer."""
+    dt = torch.bfloat16 if prm.dtype == BF16 else torch.float32
+    B, H, W, C, P, G = prm.B, prm.H, prm.W, prm.C, prm.P, prm.G
+    n_codes, n_scales = message_sizes(prm)
+    state = dict(
+        gn_stats=torch.zeros(B, P, G, 2, dtype=torch.float32, device=device),
+        y_stale=torch.zeros(B, H, W, C, dtype=dt, device=device),
+        k_stale=torch.zeros(B, H * W, C, dtype=dt, device=device),
+        v_stale=torch.zeros(B, H * W, C, dtype=dt, device=device),
+        codes=torch.zeros(n_codes, dtype=torch.int8, device=device),
+        scales=torch.zeros(n_scales, dtype=torch.float32, device=device),
+    )
+    ws = torch.zeros(workspace_size(prm), dtype=torch.uint8, device=device)
+    return state, ws
+
+
+def workspace_views(prm: LayerParams, ws):
+    """Typed views of the workspace pieces (for inspection and tests)."""
+    lo = workspace_layout(prm)
+    dt = torch.bfloat16 if prm.dtype == BF16 else torch.float32
+    es = 2 if prm.dtype == BF16 else 4
+    B, H, W, C, P, G = prm.B, prm.H, prm.W, prm.C, prm.P, prm.G
+    n = B * H * W * C
+
+    def view(off, count, dtype, shape):
+        return ws[off:off + count * (torch.finfo(dtype).bits // 8)].view(dtype).view(*shape)
+
+    out = dict(gn_fresh=view(lo.gn_fresh, B * P * G * 2, torch.float32, (B, P, G, 2)),
+               y=view(lo.y, n, dt, (B, H, W, C)), h=view(lo.h, n, dt, (B, H, W, C)))
+    for name in ("q", "k", "v", "o"):
+        out[name] = view(getattr(lo, name), n, dt, (B, H * W, C))
+    assert es in (2, 4)
+    return out

@@ -1,0 +1,380 @@
+// C ABI of the displaced-patch layer library: argument checks, workspace layout
+// and the composition of one layer step ("DistriFusion", How It Works: the
+// first step synchronous, later steps on the previous step's activations;
+// "OTIL for SDXL on 4x L40S", Periodic layer-context refresh: counter 0 puts
+// GroupNorm, the patched conv and the patched attention on their synchronous
+// branch).  Every step of the path runs in this library's kernels.
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "groupnorm.cuh"
+#include "refresh.cuh"
+#include "simt.cuh"
+#include "tc.cuh"
+
+namespace dpp_host {
+
+long long wait_limit_from_env() {
+  const char* s = getenv("DPP_DEBUG_WAIT_LIMIT");
+  if (!s || !*s) return dpp::kDefaultWaitLimit;
+  long long v = atoll(s);
+  return v < 0 ? dpp::kDefaultWaitLimit : v;
+}
+
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return dpp::kNumSMs;
+  std::lock_guard<std::mutex> g(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = dpp::kNumSMs;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace dpp_host
+
+namespace {
+
+using dpp_host::aligned16;
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+size_t esize(int dtype) { return dtype == DPP_BF16 ? 2 : 4; }
+long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+int check_dtype(int dtype) {
+  return (dtype == DPP_F32 || dtype == DPP_BF16) ? DPP_OK : DPP_ERR_DTYPE;
+}
+
+int check_conv(int B, int H, int W, int Cin, int Cout, int P, int dtype) {
+  if (B <= 0 || H <= 0 || W <= 0 || Cin <= 0 || Cout <= 0 || P <= 0) return DPP_ERR_SHAPE;
+  if (H % P) return DPP_ERR_SHAPE;
+  if ((long long)B * H * W * (long long)(Cin > Cout ? Cin : Cout) >= (1ll << 40)) return DPP_ERR_SHAPE;
+  if (dtype == DPP_BF16 && !dpp::tc_conv_supported(B, H, W, Cin, Cout, P)) return DPP_ERR_SHAPE;
+  return DPP_OK;
+}
+
+int check_attn(int B, int L, int heads, int head_dim, int P, int dtype) {
+  if (B <= 0 || L <= 0 || heads <= 0 || P <= 0) return DPP_ERR_SHAPE;
+  if (head_dim != 64) return DPP_ERR_SHAPE;
+  if (L % P || (L / P) % 8) return DPP_ERR_SHAPE;
+  if ((long long)B * L * heads * 64 >= (1ll << 40)) return DPP_ERR_SHAPE;
+  (void)dtype;
+  return DPP_OK;
+}
+
+int check_layer(const dpp_layer_params* p) {
+  if (!p) return DPP_ERR_NULL;
+  int rc = check_dtype(p->dtype);
+  if (rc) return rc;
+  if (p->B <= 0 || p->H <= 0 || p->W <= 0 || p->C <= 0 || p->P <= 0 || p->G <= 0 ||
+      p->heads <= 0)
+    return DPP_ERR_SHAPE;
+  if (p->C % p->G || p->C != p->heads * p->head_dim) return DPP_ERR_SHAPE;
+  const int vec = p->dtype == DPP_BF16 ? 8 : 4;
+  if (p->C % vec || p->C / vec > 256) return DPP_ERR_SHAPE;
+  if (p->refresh != 0 && p->refresh != 1) return DPP_ERR_ARG;
+  if (!(p->eps >= 0.f)) return DPP_ERR_ARG;
+  rc = check_conv(p->B, p->H, p->W, p->C, p->C, p->P, p->dtype);
+  if (rc) return rc;
+  rc = check_attn(p->B, p->H * p->W, p->heads, p->head_dim, p->P, p->dtype);
+  if (rc) return rc;
+  if (p->dtype == DPP_BF16 && !dpp::tc_linear_supported((long long)p->B * p->H * p->W, p->C))
+    return DPP_ERR_SHAPE;
+  return DPP_OK;
+}
+
+int layout(const dpp_layer_params* p, dpp_workspace_layout* o) {
+  int rc = check_layer(p);
+  if (rc) return rc;
+  const dpp::GnDims g = dpp::make_gn_dims(p->B, p->H, p->W, p->C, p->P, p->G);
+  const size_t act = (size_t)p->B * p->H * p->W * p->C * esize(p->dtype);
+  size_t off = 0;
+  o->status = off; off = align256(off + 256);
+  o->gn_partial = off; off = align256(off + dpp::gn_partial_bytes(g));
+  o->gn_fresh = off; off = align256(off + (size_t)p->B * p->P * p->G * 2 * sizeof(float));
+  o->y = off; off = align256(off + act);
+  o->h = off; off = align256(off + act);
+  o->q = off; off = align256(off + act);
+  o->k = off; off = align256(off + act);
+  o->v = off; off = align256(off + act);
+  o->o = off; off = align256(off + act);
+  o->total = off;
+  return DPP_OK;
+}
+
+int run_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,
+             int Cin, int Cout, int P, int dtype, int* st, cudaStream_t s) {
+  if (dtype == DPP_BF16)
+    return dpp::launch_tc_conv(yf, ys, w, out, B, H, W, Cin, Cout, P, st,
+                               dpp_host::wait_limit_from_env(), s);
+  return dpp::launch_simt_conv(yf, ys, w, out, B, H, W, Cin, Cout, P, dtype, s);
+}
+
+int run_linear(const void* a, const void* w, void* o0, void* o1, void* o2, long long M, int N,
+               int K, int dtype, int* st, cudaStream_t s) {
+  if (dtype == DPP_BF16)
+    return dpp::launch_tc_linear(a, w, o0, o1, o2, M, N, K, st, dpp_host::wait_limit_from_env(),
+                                 s);
+  dpp::SimtOut o{};
+  o.ptr[0] = o0; o.ptr[1] = o1; o.ptr[2] = o2;
+  o.ncols = o1 ? N / 3 : N;
+  return dpp::launch_simt_linear(a, w, o, M, N, K, dtype, s);
+}
+
+int run_attention(const void* q, const void* kf, const void* vf, const void* ks, const void* vs,
+                  void* o, int B, int L, int heads, int P, int dtype, int* st, cudaStream_t s) {
+  if (dtype == DPP_BF16)
+    return dpp::launch_tc_attention(q, kf, vf, ks, vs, o, B, L, heads, P, st,
+                                    dpp_host::wait_limit_from_env(), s);
+  return dpp::launch_simt_attention(q, kf, vf, ks, vs, o, B, L, heads, P, dtype, s);
+}
+
+int refresh_segments(dpp::RefreshSeg* segs, int nseg, int dtype, cudaStream_t s) {
+  for (int i0 = 0; i0 < nseg; i0 += dpp::kMaxRefreshSegs) {
+    dpp::RefreshTable tab{};
+    tab.nseg = nseg - i0 < dpp::kMaxRefreshSegs ? nseg - i0 : dpp::kMaxRefreshSegs;
+    tab.blk_start[0] = 0;
+    for (int j = 0; j < tab.nseg; ++j) {
+      tab.seg[j] = segs[i0 + j];
+      tab.blk_start[j + 1] = tab.blk_start[j] + cdiv(tab.seg[j].n, 128);
+    }
+    int rc = dpp::launch_refresh(tab, dtype, s);
+    if (rc) return rc;
+  }
+  return DPP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dpp_status_string(int status) {
+  switch (status) {
+    case DPP_OK: return "ok";
+    case DPP_ERR_NULL: return "null pointer";
+    case DPP_ERR_SHAPE: return "unsupported or invalid shape";
+    case DPP_ERR_ALIGN: return "misaligned pointer";
+    case DPP_ERR_DTYPE: return "invalid dtype";
+    case DPP_ERR_CUDA: return "CUDA error";
+    case DPP_ERR_TIMEOUT: return "device wait gave up (timeout)";
+    case DPP_ERR_BOUNDS: return "device index check failed";
+    case DPP_ERR_UNSUPPORTED: return "unsupported combination";
+    case DPP_ERR_ARG: return "invalid argument";
+    default: return "unknown status";
+  }
+}
+
+int dpp_version(void) { return 100; }
+
+int refresh_residual(const void* fresh, void* stale, int8_t* codes, float* scales, int64_t n,
+                     int dtype, void* stream) {
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  if (n < 0) return DPP_ERR_SHAPE;
+  if (n == 0) return DPP_OK;
+  if (!fresh || !stale || !codes || !scales) return DPP_ERR_NULL;
+  if (!aligned16(fresh) || !aligned16(stale) || !aligned16(codes) ||
+      (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return DPP_ERR_ALIGN;
+  dpp::RefreshSeg sg{fresh, stale, codes, scales, (long long)n, 1, 0};
+  return refresh_segments(&sg, 1, dtype, static_cast<cudaStream_t>(stream));
+}
+
+int halo_conv3x3(const void* y_fresh, const void* y_stale, const void* w, void* out, int B, int H,
+                 int W, int Cin, int Cout, int P, int dtype, int* dev_status, void* stream) {
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  if (!y_fresh || !y_stale || !w || !out) return DPP_ERR_NULL;
+  rc = check_conv(B, H, W, Cin, Cout, P, dtype);
+  if (rc) return rc;
+  if (!aligned16(y_fresh) || !aligned16(y_stale) || !aligned16(w) || !aligned16(out))
+    return DPP_ERR_ALIGN;
+  return run_conv(y_fresh, y_stale, w, out, B, H, W, Cin, Cout, P, dtype, dev_status,
+                  static_cast<cudaStream_t>(stream));
+}
+
+int stale_kv_attention(const void* q, const void* k_fresh, const void* v_fresh,
+                       const void* k_stale, const void* v_stale, void* o, int B, int L, int heads,
+                       int head_dim, int P, int dtype, int* dev_status, void* stream) {
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  if (!q || !k_fresh || !v_fresh || !k_stale || !v_stale || !o) return DPP_ERR_NULL;
+  rc = check_attn(B, L, heads, head_dim, P, dtype);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k_fresh) || !aligned16(v_fresh) || !aligned16(k_stale) ||
+      !aligned16(v_stale) || !aligned16(o))
+    return DPP_ERR_ALIGN;
+  return run_attention(q, k_fresh, v_fresh, k_stale, v_stale, o, B, L, heads, P, dtype,
+                       dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int dpp_workspace_query(const dpp_layer_params* prm, dpp_workspace_layout* out) {
+  if (!out) return DPP_ERR_NULL;
+  return layout(prm, out);
+}
+
+size_t dpp_workspace_size(const dpp_layer_params* prm) {
+  dpp_workspace_layout l;
+  return layout(prm, &l) == DPP_OK ? l.total : 0;
+}
+
+int64_t dpp_message_elems(const dpp_layer_params* p) {
+  if (check_layer(p)) return -1;
+  const long long blc = (long long)p->B * p->H * p->W * p->C;
+  return 2 * blc + (long long)p->B * (p->P - 1) * 2 * p->W * p->C;
+}
+
+int64_t dpp_message_blocks(const dpp_layer_params* p) {
+  if (check_layer(p)) return -1;
+  const long long blc = (long long)p->B * p->H * p->W * p->C;
+  return 2 * cdiv(blc, 128) + (long long)p->B * (p->P - 1) * cdiv(2ll * p->W * p->C, 128);
+}
+
+int dpp_layer_kernel_count(const dpp_layer_params* p, int mode) {
+  if (check_layer(p)) return -1;
+  int n = 2 /* gn */ + 1 /* conv */ + 1 /* qkv */ + 1 /* attention */ + 1 /* out proj */;
+  if (mode == DPP_STALE && p->refresh) {
+    const long long nseg = 2 + (long long)p->B * (p->P - 1);
+    n += (int)cdiv(nseg, dpp::kMaxRefreshSegs);
+  }
+  return n;
+}
+
+int patch_layer_step(const dpp_layer_params* prm, const dpp_layer_weights* wts,
+                     const dpp_layer_state* st, const void* x, void* out, int mode,
+                     void* workspace, void* stream) {
+  return patch_layer_step_timed(prm, wts, st, x, out, mode, workspace, stream, nullptr);
+}
+
+int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights* wts,
+                           const dpp_layer_state* st, const void* x, void* out, int mode,
+                           void* workspace, void* stream, void* const* stage_events) {
+  if (!prm || !wts || !st || !x || !out || !workspace) return DPP_ERR_NULL;
+  if (mode != DPP_SYNC && mode != DPP_STALE) return DPP_ERR_ARG;
+  dpp_workspace_layout lo;
+  int rc = layout(prm, &lo);
+  if (rc) return rc;
+  const dpp_layer_params& p = *prm;
+  if (!wts->gamma || !wts->beta || !wts->w_conv || !wts->w_qkv || !wts->w_o) return DPP_ERR_NULL;
+  if (!st->gn_stats || !st->y_stale || !st->k_stale || !st->v_stale) return DPP_ERR_NULL;
+  const bool refresh = mode == DPP_STALE && p.refresh;
+  if (refresh && (!st->codes || !st->scales)) return DPP_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return DPP_ERR_ALIGN;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(wts->w_conv) || !aligned16(wts->w_qkv) ||
+      !aligned16(wts->w_o) || !aligned16(st->y_stale) || !aligned16(st->k_stale) ||
+      !aligned16(st->v_stale) || (refresh && !aligned16(st->codes)) ||
+      (reinterpret_cast<uintptr_t>(wts->gamma) & 3u) ||
+      (reinterpret_cast<uintptr_t>(wts->beta) & 3u) ||
+      (reinterpret_cast<uintptr_t>(st->gn_stats) & 3u) ||
+      (refresh && (reinterpret_cast<uintptr_t>(st->scales) & 3u)))
+    return DPP_ERR_ALIGN;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + lo.status);
+  float* gn_partial = reinterpret_cast<float*>(ws + lo.gn_partial);
+  float* gn_fresh = reinterpret_cast<float*>(ws + lo.gn_fresh);
+  void* y = ws + lo.y;
+  void* h = ws + lo.h;
+  void* q = ws + lo.q;
+  void* k = ws + lo.k;
+  void* v = ws + lo.v;
+  void* o = ws + lo.o;
+  const bool sync = mode == DPP_SYNC;
+  const int L = p.H * p.W;
+  const long long M = (long long)p.B * L;
+
+  auto mark = [&](int i) -> int {
+    if (!stage_events || !stage_events[i]) return DPP_OK;
+    return cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s) == cudaSuccess
+               ? DPP_OK
+               : DPP_ERR_CUDA;
+  };
+  if ((rc = mark(0))) return rc;
+  // a1 + a2: fresh sums of every patch, spliced GroupNorm
+  const dpp::GnDims g = dpp::make_gn_dims(p.B, p.H, p.W, p.C, p.P, p.G);
+  rc = dpp::launch_gn(x, y, gn_partial, sync ? nullptr : st->gn_stats, gn_fresh, wts->gamma,
+                      wts->beta, g, p.eps, sync ? 1 : 0, p.dtype, status, s);
+  if (rc || (rc = mark(1))) return rc;
+  // a3: halo conv, halo rows from the stale conv input (fresh at the synchronous step)
+  rc = run_conv(y, sync ? y : st->y_stale, wts->w_conv, h, p.B, p.H, p.W, p.C, p.C, p.P, p.dtype,
+                status, s);
+  if (rc || (rc = mark(2))) return rc;
+  // a4: Q, K, V projections (one GEMM over the packed [3C, C] weight)
+  rc = run_linear(h, wts->w_qkv, q, k, v, M, 3 * p.C, p.C, p.dtype, status, s);
+  if (rc || (rc = mark(3))) return rc;
+  // a5: stale-KV attention
+  rc = run_attention(q, k, v, sync ? k : st->k_stale, sync ? v : st->v_stale, o, p.B, L, p.heads,
+                     p.P, p.dtype, status, s);
+  if (rc || (rc = mark(4))) return rc;
+  // a6: output projection
+  rc = run_linear(o, wts->w_o, out, nullptr, nullptr, M, p.C, p.C, p.dtype, status, s);
+  if (rc || (rc = mark(5))) return rc;
+
+  // a7/a8: state update, after every virtual rank has read the old state
+  const size_t es = esize(p.dtype);
+  const size_t act = (size_t)M * p.C * es;
+  const size_t gn_bytes = (size_t)p.B * p.P * p.G * 2 * sizeof(float);
+  const size_t halo_bytes = 2ull * p.W * p.C * es;            // rows r-1 and r
+  const size_t band_bytes = (size_t)(p.H / p.P) * p.W * p.C * es;
+  const size_t img_bytes = (size_t)p.H * p.W * p.C * es;
+  if (sync) {
+    DPP_CUDA_CHECK(cudaMemcpyAsync(st->k_stale, k, act, cudaMemcpyDeviceToDevice, s));
+    DPP_CUDA_CHECK(cudaMemcpyAsync(st->v_stale, v, act, cudaMemcpyDeviceToDevice, s));
+    DPP_CUDA_CHECK(cudaMemcpyAsync(st->gn_stats, gn_fresh, gn_bytes, cudaMemcpyDeviceToDevice, s));
+    if (p.P > 1) {
+      for (int b = 0; b < p.B; ++b) {
+        const size_t off = b * img_bytes + band_bytes - halo_bytes / 2;  // row Hp-1 of batch b
+        DPP_CUDA_CHECK(cudaMemcpy2DAsync(static_cast<char*>(st->y_stale) + off, band_bytes,
+                                         static_cast<char*>(y) + off, band_bytes, halo_bytes,
+                                         p.P - 1, cudaMemcpyDeviceToDevice, s));
+      }
+    }
+    return mark(6);
+  }
+  if (!refresh) return mark(6);
+  const long long blc = M * p.C;
+  const int nseg = 2 + p.B * (p.P - 1);
+  dpp::RefreshSeg* segs = static_cast<dpp::RefreshSeg*>(malloc(sizeof(dpp::RefreshSeg) * nseg));
+  if (!segs) return DPP_ERR_UNSUPPORTED;
+  long long coff = 0, soff = 0;
+  auto add = [&](int i, const void* fr, void* stl, long long n) {
+    const bool ok = aligned16(fr) && aligned16(stl) && aligned16(st->codes + coff);
+    segs[i] = dpp::RefreshSeg{fr, stl, st->codes + coff, st->scales + soff, n, ok ? 1 : 0, 0};
+    coff += n;
+    soff += cdiv(n, 128);
+  };
+  add(0, k, st->k_stale, blc);
+  add(1, v, st->v_stale, blc);
+  int i = 2;
+  for (int b = 0; b < p.B; ++b)
+    for (int pp = 1; pp < p.P; ++pp) {
+      const size_t off = b * img_bytes + pp * band_bytes - halo_bytes / 2;
+      add(i++, static_cast<char*>(y) + off, static_cast<char*>(st->y_stale) + off,
+          2ll * p.W * p.C);
+    }
+  rc = refresh_segments(segs, nseg, p.dtype, s);
+  free(segs);
+  if (rc) return rc;
+  DPP_CUDA_CHECK(cudaMemcpyAsync(st->gn_stats, gn_fresh, gn_bytes, cudaMemcpyDeviceToDevice, s));
+  return mark(6);
+}
+
+int dpp_read_device_status(const void* workspace, void* stream) {
+  if (!workspace) return DPP_ERR_NULL;
+  int v = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DPP_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DPP_ERR_CUDA;
+  return v;
+}
+
+}  // extern "C"

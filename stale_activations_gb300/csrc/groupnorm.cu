@@ -1,0 +1,177 @@
+// GroupNorm with spliced stale statistics ("OTIL for SDXL on 4x L40S", What is
+// implemented where: DistriGroupNorm carries stale context; GroupNorm sync
+// without the rest: two scalars per group).
+//
+// gn_stats: per (batch, patch, chunk of the patch's pixels) the fp32 sums
+//   (sum x, sum x^2) of every group.  Each thread owns one 16-byte channel
+//   vector and walks pixels, so loads are 128-bit and coalesced along C; the
+//   per-channel sums are reduced across the block in shared memory and then
+//   folded into groups in a fixed order (deterministic, no atomics).
+// gn_apply: patch p's statistics = its own fresh sums (summed over chunks) +
+//   the other patches' stale sums (fresh ones at the synchronous step);
+//   mu = S1/N, var = max(S2/N - mu^2, 0), y = (x - mu) * rstd * gamma + beta.
+// Both are HBM-bound streams: stats reads 1 element, apply reads 1 and writes 1.
+#include "groupnorm.cuh"
+
+namespace dpp {
+
+template <typename T>
+__global__ void __launch_bounds__(256) gn_stats_kernel(const T* __restrict__ x,
+                                                       float* __restrict__ partial, GnDims g,
+                                                       int* status_to_zero) {
+  constexpr int VEC = Vec<T>::N;
+  extern __shared__ float red[];  // [2][PIX][C]
+  const int chunk = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
+  if (status_to_zero && chunk == 0 && p == 0 && b == 0 && threadIdx.x == 0) *status_to_zero = 0;
+  const int NV = g.C / VEC;
+  const int PIX = 256 / NV;
+  const int tid = threadIdx.x;
+  const int pl = tid / NV, v = tid % NV;
+  const long long band_pix = (long long)g.Hp * g.W;
+  const long long p0 = (long long)chunk * g.chunk_pix;
+  const long long p1 = min(band_pix, p0 + g.chunk_pix);
+  float s1[VEC], s2[VEC];
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) { s1[i] = 0.f; s2[i] = 0.f; }
+  if (pl < PIX) {
+    const T* base = x + (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C + v * VEC;
+    for (long long px = p0 + pl; px < p1; px += PIX) {
+      uint4 u = __ldg(reinterpret_cast<const uint4*>(base + px * g.C));
+      float f[VEC];
+      unpack16(u, f);
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) { s1[i] += f[i]; s2[i] = fmaf(f[i], f[i], s2[i]); }
+    }
+    float* r1 = red + (long long)pl * g.C + v * VEC;
+    float* r2 = red + (long long)PIX * g.C + (long long)pl * g.C + v * VEC;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) { r1[i] = s1[i]; r2[i] = s2[i]; }
+  }
+  __syncthreads();
+  const int cg = g.C / g.G;
+  for (int gi = tid; gi < g.G; gi += blockDim.x) {
+    float a = 0.f, q = 0.f;
+    for (int k = 0; k < PIX; ++k)
+      for (int c = gi * cg; c < (gi + 1) * cg; ++c) {
+        a += red[(long long)k * g.C + c];
+        q += red[(long long)PIX * g.C + (long long)k * g.C + c];
+      }
+    float* out = partial + ((((long long)b * g.P + p) * g.nchunk + chunk) * g.G + gi) * 2;
+    out[0] = a;
+    out[1] = q;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, T* __restrict__ y,
+                                                       const float* __restrict__ partial,
+                                                       const float* __restrict__ stale_stats,
+                                                       float* __restrict__ fresh_out,
+                                                       const float* __restrict__ gamma,
+                                                       const float* __restrict__ beta, GnDims g,
+                                                       float eps, int sync) {
+  constexpr int VEC = Vec<T>::N;
+  extern __shared__ float sm[];  // mean[C], scale[C], beta[C], group sums [P][G][2]
+  float* s_mu = sm;
+  float* s_sc = sm + g.C;
+  float* s_be = sm + 2 * g.C;
+  float* s_tot = sm + 3 * g.C;  // [P][G][2] fresh sums of every patch (sync) or own
+  const int chunk = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  // fresh sums over chunks, for own patch (and every patch at the synchronous step)
+  for (int idx = tid; idx < g.P * g.G * 2; idx += blockDim.x) {
+    const int q = idx / (g.G * 2), r = idx % (g.G * 2);
+    float v = 0.f;
+    if (sync || q == p) {
+      const float* src = partial + (((long long)b * g.P + q) * g.nchunk) * g.G * 2 + r;
+      for (int c = 0; c < g.nchunk; ++c) v += src[(long long)c * g.G * 2];
+    } else {
+      v = stale_stats[((long long)b * g.P + q) * g.G * 2 + r];
+    }
+    s_tot[idx] = v;
+  }
+  __syncthreads();
+  if (chunk == 0 && fresh_out) {
+    for (int r = tid; r < g.G * 2; r += blockDim.x)
+      fresh_out[((long long)b * g.P + p) * g.G * 2 + r] = s_tot[p * g.G * 2 + r];
+  }
+  const int cg = g.C / g.G;
+  const double invN = 1.0 / ((double)g.H * g.W * cg);
+  for (int c = tid; c < g.C; c += blockDim.x) {
+    const int gi = c / cg;
+    float S1 = s_tot[p * g.G * 2 + gi * 2], S2 = s_tot[p * g.G * 2 + gi * 2 + 1];
+    for (int q = 0; q < g.P; ++q)
+      if (q != p) { S1 += s_tot[q * g.G * 2 + gi * 2]; S2 += s_tot[q * g.G * 2 + gi * 2 + 1]; }
+    const float mu = (float)(S1 * invN);
+    const float var = fmaxf((float)(S2 * invN) - mu * mu, 0.f);
+    const float rstd = rsqrtf(var + eps);
+    s_mu[c] = mu;
+    s_sc[c] = rstd * gamma[c];
+    s_be[c] = beta[c];
+  }
+  __syncthreads();
+  const int NV = g.C / VEC;
+  const long long band_pix = (long long)g.Hp * g.W;
+  const long long p0 = (long long)chunk * g.chunk_pix;
+  const long long p1 = min(band_pix, p0 + g.chunk_pix);
+  const long long base = (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C;
+  const long long nvec = (p1 - p0) * NV;
+  for (long long i = tid; i < nvec; i += blockDim.x) {
+    const long long px = p0 + i / NV;
+    const int v = (int)(i % NV);
+    const long long off = base + px * g.C + v * VEC;
+    uint4 u = __ldcs(reinterpret_cast<const uint4*>(x + off));
+    float f[VEC];
+    unpack16(u, f);
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      const int c = v * VEC + k;
+      f[k] = fmaf(f[k] - s_mu[c], s_sc[c], s_be[c]);
+    }
+    *reinterpret_cast<uint4*>(y + off) = pack16(f);
+  }
+}
+
+GnDims make_gn_dims(int B, int H, int W, int C, int P, int G) {
+  GnDims g;
+  g.B = B; g.H = H; g.W = W; g.C = C; g.P = P; g.G = G;
+  g.Hp = H / P;
+  const long long band_pix = (long long)g.Hp * W;
+  long long nchunk = (2ll * kNumSMs + (long long)B * P - 1) / ((long long)B * P);
+  if (nchunk > band_pix) nchunk = band_pix;
+  if (nchunk < 1) nchunk = 1;
+  g.chunk_pix = (band_pix + nchunk - 1) / nchunk;
+  g.nchunk = (int)((band_pix + g.chunk_pix - 1) / g.chunk_pix);
+  return g;
+}
+
+size_t gn_partial_bytes(const GnDims& g) {
+  return (size_t)g.B * g.P * g.nchunk * g.G * 2 * sizeof(float);
+}
+
+int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, float* fresh_out,
+              const float* gamma, const float* beta, const GnDims& g, float eps, int sync,
+              int dtype, int* status_to_zero, cudaStream_t stream) {
+  dim3 grid(g.nchunk, g.P, g.B);
+  const int VEC = dtype == DPP_BF16 ? 8 : 4;
+  const int NV = g.C / VEC;
+  const int PIX = 256 / NV;
+  const size_t red_bytes = 2ull * PIX * g.C * sizeof(float);
+  const size_t app_bytes = (3ull * g.C + 2ull * g.P * g.G) * sizeof(float);
+  if (dtype == DPP_BF16) {
+    auto* xs = static_cast<const __nv_bfloat16*>(x);
+    gn_stats_kernel<__nv_bfloat16><<<grid, 256, red_bytes, stream>>>(xs, partial, g,
+                                                                     status_to_zero);
+    gn_apply_kernel<__nv_bfloat16><<<grid, 256, app_bytes, stream>>>(
+        xs, static_cast<__nv_bfloat16*>(y), partial, stale_stats, fresh_out, gamma, beta, g, eps,
+        sync);
+  } else {
+    auto* xs = static_cast<const float*>(x);
+    gn_stats_kernel<float><<<grid, 256, red_bytes, stream>>>(xs, partial, g, status_to_zero);
+    gn_apply_kernel<float><<<grid, 256, app_bytes, stream>>>(
+        xs, static_cast<float*>(y), partial, stale_stats, fresh_out, gamma, beta, g, eps, sync);
+  }
+  return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+}
+
+}  // namespace dpp

@@ -1,0 +1,23 @@
+#pragma once
+#include "common.cuh"
+
+namespace dpp {
+
+struct GnDims {
+  int B, H, W, C, P, G;
+  int Hp;              // rows per patch
+  int nchunk;          // pixel chunks per (batch, patch)
+  long long chunk_pix; // pixels per chunk
+};
+
+GnDims make_gn_dims(int B, int H, int W, int C, int P, int G);
+size_t gn_partial_bytes(const GnDims& g);
+
+// Launches the stats and apply kernels.  stale_stats may be NULL when sync != 0.
+// fresh_out (may be NULL) receives the [B,P,G,2] fresh sums.  The stats kernel
+// zeroes *status_to_zero first (if non-NULL).
+int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, float* fresh_out,
+              const float* gamma, const float* beta, const GnDims& g, float eps, int sync,
+              int dtype, int* status_to_zero, cudaStream_t stream);
+
+}  // namespace dpp

@@ -1,0 +1,215 @@
+// fp32 SIMT kernels: the arithmetic path of fp32-storage layers (tcgen05 has no
+// full-precision fp32 kind, and TF32 cannot meet fp32 tolerances).
+//
+// simt_gemm: C[m, n] = sum_k A[m, k] * Wt[n, k] with a 64x64 output tile per
+//   block, 16-wide K slices staged in shared memory, 4x4 outputs per thread.
+//   A is either a plain row-major matrix (projections) or the implicit im2col
+//   view of the halo conv: row m = pixel (b, r, c), column k = (tap, cin), the
+//   tap's source row taken from the fresh map inside r's band, from the stale
+//   map for the band's two halo rows, zero outside the image ("Benchmarking
+//   DistVAE", Glossary: halo rows of a sharded convolution).
+// simt_attention: one thread per query row of one patch and head; 64-key tiles
+//   of the spliced K/V (own patch fresh, other rows stale) in shared memory;
+//   online softmax in fp32.
+#include "simt.cuh"
+
+namespace dpp {
+
+struct ALinear {
+  const void* a;
+  int K;
+  template <typename T>
+  __device__ __forceinline__ float load(long long m, int k) const {
+    return to_f32(static_cast<const T*>(a)[m * K + k]);
+  }
+};
+
+struct AConv {
+  const void* yf;
+  const void* ys;
+  int H, W, Cin, Hp;
+  template <typename T>
+  __device__ __forceinline__ float load(long long m, int k) const {
+    const int tap = k / Cin, ci = k - tap * Cin;
+    const int di = tap / 3 - 1, dj = tap % 3 - 1;
+    const long long hw = (long long)H * W;
+    const long long b = m / hw;
+    const int rem = (int)(m - b * hw);
+    const int r = rem / W, c = rem - (rem / W) * W;
+    const int rr = r + di, cc = c + dj;
+    if (rr < 0 || rr >= H || cc < 0 || cc >= W) return 0.f;
+    const bool own = (rr / Hp) == (r / Hp);
+    const T* src = static_cast<const T*>(own ? yf : ys);
+    return to_f32(src[((b * H + rr) * W + cc) * (long long)Cin + ci]);
+  }
+};
+
+template <typename T, typename ALoad>
+__global__ void __launch_bounds__(256) simt_gemm_kernel(ALoad A, const T* __restrict__ Wt,
+                                                        SimtOut out, long long M, int N, int K) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const long long m0 = (long long)blockIdx.y * 64;
+  const int n0 = blockIdx.x * 64;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+      const int mm = i / 16, kk = i % 16;
+      const long long m = m0 + mm;
+      const int k = k0 + kk;
+      As[kk][mm] = (m < M && k < K) ? A.template load<T>(m, k) : 0.f;
+      const int n = n0 + mm;
+      Bs[kk][mm] = (n < N && k < K) ? to_f32(Wt[(long long)n * K + k]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { a[i] = As[kk][ty * 4 + i]; bv[i] = Bs[kk][tx * 4 + i]; }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const long long m = m0 + ty * 4 + i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n >= N) continue;
+      const int which = n / out.ncols;
+      const int col = n - which * out.ncols;
+      static_cast<T*>(out.ptr[which])[m * out.ncols + col] = from_f32<T>(acc[i][j]);
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) simt_attention_kernel(const T* __restrict__ q,
+                                                             const T* __restrict__ kf,
+                                                             const T* __restrict__ vf,
+                                                             const T* __restrict__ ks,
+                                                             const T* __restrict__ vs,
+                                                             T* __restrict__ o, int L, int heads,
+                                                             int P) {
+  constexpr int D = 64, KT = 64;
+  __shared__ float Ks[KT][D + 1];
+  __shared__ float Vs[KT][D];
+  const int Lp = L / P;
+  const int tiles_per_patch = (Lp + 127) / 128;
+  const int p = blockIdx.x / tiles_per_patch;
+  const int qt = blockIdx.x - p * tiles_per_patch;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int C = heads * D;
+  const int t = p * Lp + qt * 128 + threadIdx.x;
+  const bool valid = qt * 128 + threadIdx.x < Lp;
+  const long long rowbase = (long long)b * L;
+  float qr[D], acc[D];
+  for (int e = 0; e < D; ++e) {
+    qr[e] = valid ? to_f32(q[(rowbase + t) * C + h * D + e]) * 0.125f : 0.f;  // 1/sqrt(64)
+    acc[e] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+  for (int s0 = 0; s0 < L; s0 += KT) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < KT * D; i += 128) {
+      const int kk = i / D, e = i % D;
+      const int s = s0 + kk;
+      float kv = 0.f, vv = 0.f;
+      if (s < L) {
+        const bool own = s / Lp == p;
+        const long long off = (rowbase + s) * C + h * D + e;
+        kv = to_f32(own ? kf[off] : ks[off]);
+        vv = to_f32(own ? vf[off] : vs[off]);
+      }
+      Ks[kk][e] = kv;
+      Vs[kk][e] = vv;
+    }
+    __syncthreads();
+    const int nk = min(KT, L - s0);
+    float sc[KT];
+    float mt = m;
+#pragma unroll 4
+    for (int kk = 0; kk < KT; ++kk) {
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < D; ++e) dot = fmaf(qr[e], Ks[kk][e], dot);
+      sc[kk] = kk < nk ? dot : -INFINITY;
+      mt = fmaxf(mt, sc[kk]);
+    }
+    const float corr = expf(m - mt);  // m = -inf on the first tile gives 0
+    l *= corr;
+#pragma unroll
+    for (int e = 0; e < D; ++e) acc[e] *= corr;
+    m = mt;
+#pragma unroll 4
+    for (int kk = 0; kk < KT; ++kk) {
+      const float pk = expf(sc[kk] - m);
+      l += pk;
+#pragma unroll
+      for (int e = 0; e < D; ++e) acc[e] = fmaf(pk, Vs[kk][e], acc[e]);
+    }
+  }
+  if (valid) {
+    const float inv = 1.f / l;
+    for (int e = 0; e < D; ++e) o[(rowbase + t) * C + h * D + e] = from_f32<T>(acc[e] * inv);
+  }
+}
+
+int launch_simt_linear(const void* a, const void* w, const SimtOut& out, long long M, int N, int K,
+                       int dtype, cudaStream_t stream) {
+  dim3 grid((N + 63) / 64, (unsigned)((M + 63) / 64));
+  ALinear A{a, K};
+  if (dtype == DPP_BF16)
+    simt_gemm_kernel<__nv_bfloat16, ALinear><<<grid, 256, 0, stream>>>(
+        A, static_cast<const __nv_bfloat16*>(w), out, M, N, K);
+  else
+    simt_gemm_kernel<float, ALinear><<<grid, 256, 0, stream>>>(A, static_cast<const float*>(w),
+                                                               out, M, N, K);
+  return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+}
+
+int launch_simt_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,
+                     int Cin, int Cout, int P, int dtype, cudaStream_t stream) {
+  const long long M = (long long)B * H * W;
+  const int K = 9 * Cin;
+  dim3 grid((Cout + 63) / 64, (unsigned)((M + 63) / 64));
+  AConv A{yf, ys, H, W, Cin, H / P};
+  SimtOut o{};
+  o.ptr[0] = out;
+  o.ncols = Cout;
+  if (dtype == DPP_BF16)
+    simt_gemm_kernel<__nv_bfloat16, AConv><<<grid, 256, 0, stream>>>(
+        A, static_cast<const __nv_bfloat16*>(w), o, M, Cout, K);
+  else
+    simt_gemm_kernel<float, AConv><<<grid, 256, 0, stream>>>(A, static_cast<const float*>(w), o,
+                                                             M, Cout, K);
+  return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+}
+
+int launch_simt_attention(const void* q, const void* kf, const void* vf, const void* ks,
+                          const void* vs, void* o, int B, int L, int heads, int P, int dtype,
+                          cudaStream_t stream) {
+  const int Lp = L / P;
+  dim3 grid(P * ((Lp + 127) / 128), heads, B);
+  if (dtype == DPP_BF16) {
+    using T = __nv_bfloat16;
+    simt_attention_kernel<T><<<grid, 128, 0, stream>>>(
+        static_cast<const T*>(q), static_cast<const T*>(kf), static_cast<const T*>(vf),
+        static_cast<const T*>(ks), static_cast<const T*>(vs), static_cast<T*>(o), L, heads, P);
+  } else {
+    simt_attention_kernel<float><<<grid, 128, 0, stream>>>(
+        static_cast<const float*>(q), static_cast<const float*>(kf),
+        static_cast<const float*>(vf), static_cast<const float*>(ks),
+        static_cast<const float*>(vs), static_cast<float*>(o), L, heads, P);
+  }
+  return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+}
+
+}  // namespace dpp

@@ -1,0 +1,25 @@
+// Tensor-core (tcgen05 + TMA) kernels of the bf16 path.
+#pragma once
+#include "common.cuh"
+
+namespace dpp {
+
+// Shape checks (host).
+bool tc_conv_supported(int B, int H, int W, int Cin, int Cout, int P);
+bool tc_linear_supported(long long M, int C);
+
+// out[M, N] = a[M, K] * w[N, K]^T (bf16, fp32 accumulation).  If o1/o2 are
+// non-NULL, N is split into three equal column blocks written to o0, o1, o2.
+int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2, long long M,
+                     int N, int K, int* status, long long wait_limit, cudaStream_t s);
+
+// Implicit-GEMM halo conv3x3 (see halo_conv3x3 in dpp.h).
+int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,
+                   int Cin, int Cout, int P, int* status, long long wait_limit, cudaStream_t s);
+
+// Stale-KV flash attention (see stale_kv_attention in dpp.h), head_dim 64.
+int launch_tc_attention(const void* q, const void* kf, const void* vf, const void* ks,
+                        const void* vs, void* o, int B, int L, int heads, int P, int* status,
+                        long long wait_limit, cudaStream_t s);
+
+}  // namespace dpp

@@ -1,0 +1,447 @@
+// Stale-KV flash attention on tcgen05 tensor cores (bf16 inputs, head_dim 64).
+//
+// ("OTIL for SDXL on 4x L40S", item 3 and Periodic layer-context refresh: the
+// cross-slice attention K/V are stale; Self-tests: a rank's own slice is fresh,
+// other positions stale, never a blend.)  Query token t of patch p attends over
+// all L keys; key row s comes from the fresh K/V if s lies in patch p, else
+// from the stale K/V.
+//
+// One CTA = two 128-row query tiles of one (batch, head, patch), 12 warps:
+//   warps 0-3 / 4-7  softmax of query tile 0 / 1 (thread = query row = TMEM lane)
+//   warp 8           TMA producer: Q tiles once, then a 3-stage ring of K and V
+//                    tiles; each 128-key tile is fetched in sub-boxes of g rows
+//                    (g = largest power of two <= 128 dividing L/P), each sub-box
+//                    from the fresh or the stale tensor map -- the splice.
+//   warp 9           MMA issuer: S = Q K^T (M=128, N=128, K=16 steps over d=64)
+//                    into TMEM, O += P V (M=128, N=64, K=16 steps over keys).
+//   warps 10-11      convert each landed V tile from bf16 to fp16 in place.
+// P is rounded to fp16, not bf16: its 11-bit significand keeps the rounding of
+// the probabilities well inside the 2e-3 output tolerance (bf16's 8 bits would
+// not), and V is widened to fp16 exactly so that P V runs as kind::f16 with
+// both operands fp16 (|V| must stay below 65504).
+// Online softmax in the log2 domain with a lazily moved reference maximum: the
+// running O is rescaled only when a row's maximum grows by more than 2^8.
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace dpp {
+
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn();  // tc_gemm.cu
+
+namespace {
+
+constexpr int D = 64;                 // head dim
+constexpr int QT = 128;               // query rows per tile
+constexpr int KT = 128;               // keys per tile
+constexpr int KV_STAGES = 3;
+constexpr int TILE_BYTES = KT * D * 2;  // 16 KB (K or V tile, Q tile)
+constexpr int P_BYTES = QT * KT * 2;    // 32 KB (fp16 probabilities of one query tile)
+constexpr int ATTN_THREADS = 384;
+// smem: Q0 Q1 | P0 P1 | (K V) x stages | barriers
+constexpr int OFF_Q = 0;
+constexpr int OFF_P = 2 * TILE_BYTES;
+constexpr int OFF_KV = OFF_P + 2 * P_BYTES;
+constexpr int OFF_BAR = OFF_KV + KV_STAGES * 2 * TILE_BYTES;
+constexpr int ATTN_SMEM = OFF_BAR + 512 + 1024;
+constexpr float kScaleLog2 = 0.18033688011112042f;  // log2(e) / sqrt(64)
+constexpr float kRescaleThreshold = 8.0f;           // log2 units
+
+struct AttnArgs {
+  int L, heads, P, Lp, g, n_qt, n_pairs, nkt;
+  __nv_bfloat16* o;
+  int* status;
+  long long wait_limit;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[KV_STAGES], v_full[KV_STAGES], v_conv[KV_STAGES], kv_empty[KV_STAGES];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  uint64_t drain;
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const AttnArgs& a,
+                                              Bars* bars) {
+  if (ptx::mbar_wait(bar, parity, a.wait_limit, &bars->abort_flag)) return true;
+  set_status(a.status, DPP_ERR_TIMEOUT);
+  bars->abort_flag = 1;
+  return false;
+}
+
+__global__ void __launch_bounds__(ATTN_THREADS, 1)
+    tc_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKf,
+                   const __grid_constant__ CUtensorMap tmKs, const __grid_constant__ CUtensorMap tmVf,
+                   const __grid_constant__ CUtensorMap tmVs, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = blockIdx.x % a.n_pairs;
+  const int p = blockIdx.x / a.n_pairs;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int patch0 = p * a.Lp;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < KV_STAGES; ++s) {
+      ptx::mbar_init(&bars->k_full[s], 1);
+      ptx::mbar_init(&bars->v_full[s], 1);
+      ptx::mbar_init(&bars->v_conv[s], 2);
+      ptx::mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(&bars->s_full[t], 1);
+      ptx::mbar_init(&bars->s_free[t], 4);
+      ptx::mbar_init(&bars->p_full[t], 4);
+      ptx::mbar_init(&bars->pv_done[t], 1);
+    }
+    ptx::mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 8 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmQ);
+    ptx::tma_prefetch_desc(&tmKf);
+    ptx::tma_prefetch_desc(&tmKs);
+    ptx::tma_prefetch_desc(&tmVf);
+    ptx::tma_prefetch_desc(&tmVs);
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(&bars->tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  const uint32_t tS[2] = {tmem, tmem + 128};
+  const uint32_t tO[2] = {tmem + 256, tmem + 320};
+  const int nkt = a.nkt;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      ptx::mbar_arrive_expect_tx(&bars->q_full, 2 * TILE_BYTES);
+      for (int t = 0; t < 2; ++t)
+        ptx::tma_load_3d(smem + OFF_Q + t * TILE_BYTES, &tmQ, &bars->q_full, h * D,
+                         patch0 + (2 * pair + t) * QT, b);
+      const int nsub = KT / a.g;
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int st = j % KV_STAGES;
+        if (!wait_or_abort(&bars->kv_empty[st], ((j / KV_STAGES) & 1) ^ 1, a, bars)) {
+          ok = false;
+          break;
+        }
+        uint8_t* kdst = smem + OFF_KV + st * 2 * TILE_BYTES;
+        uint8_t* vdst = kdst + TILE_BYTES;
+        ptx::mbar_arrive_expect_tx(&bars->k_full[st], TILE_BYTES);
+        ptx::mbar_arrive_expect_tx(&bars->v_full[st], TILE_BYTES);
+        for (int i = 0; i < nsub; ++i) {
+          const int row = j * KT + i * a.g;
+          const bool fresh = row >= patch0 && row < patch0 + a.Lp;
+          ptx::tma_load_3d(kdst + i * a.g * 128, fresh ? &tmKf : &tmKs, &bars->k_full[st], h * D,
+                           row, b);
+        }
+        for (int i = 0; i < nsub; ++i) {
+          const int row = j * KT + i * a.g;
+          const bool fresh = row >= patch0 && row < patch0 + a.Lp;
+          ptx::tma_load_3d(vdst + i * a.g * 128, fresh ? &tmVf : &tmVs, &bars->v_full[st], h * D,
+                           row, b);
+        }
+        ++issued;
+      }
+      if (bars->abort_flag) {  // wait for own copies in flight before exiting
+        ptx::mbar_wait(&bars->q_full, 0, kDrainWaitLimit, nullptr);
+        const int first = issued > KV_STAGES ? issued - KV_STAGES : 0;
+        for (int j = first; j < issued; ++j) {
+          ptx::mbar_wait(&bars->k_full[j % KV_STAGES], (j / KV_STAGES) & 1, kDrainWaitLimit,
+                         nullptr);
+          ptx::mbar_wait(&bars->v_full[j % KV_STAGES], (j / KV_STAGES) & 1, kDrainWaitLimit,
+                         nullptr);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = ptx::idesc_f16(QT, KT, 1, 0, 0);
+      constexpr uint32_t idesc_pv = ptx::idesc_f16(QT, D, 0, 0, 1);
+      const uint32_t q_addr = ptx::smem_u32(smem + OFF_Q);
+      const uint32_t p_addr = ptx::smem_u32(smem + OFF_P);
+      const uint32_t kv_addr = ptx::smem_u32(smem + OFF_KV);
+      bool any = false;
+      auto issue_qk = [&](int t, int j) {
+        const uint32_t k_addr = kv_addr + (j % KV_STAGES) * 2 * TILE_BYTES;
+        const uint32_t qa = q_addr + t * TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          ptx::mma_ss(tS[t], ptx::sw128_desc(qa + k * 32, 16, 1024),
+                      ptx::sw128_desc(k_addr + k * 32, 16, 1024), idesc_qk, k ? 1u : 0u);
+        ptx::mma_commit(&bars->s_full[t]);
+        any = true;
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t v_addr = kv_addr + (j % KV_STAGES) * 2 * TILE_BYTES + TILE_BYTES;
+        const uint32_t pa = p_addr + t * P_BYTES;
+#pragma unroll
+        for (int k = 0; k < KT / 16; ++k)
+          ptx::mma_ss(tO[t], ptx::sw128_desc(pa + (k >> 2) * (QT * 128) + (k & 3) * 32, 16, 1024),
+                      ptx::sw128_desc(v_addr + k * 2048, TILE_BYTES, 1024), idesc_pv,
+                      (j | k) ? 1u : 0u);
+        ptx::mma_commit(&bars->pv_done[t]);
+        any = true;
+      };
+      bool ok = wait_or_abort(&bars->q_full, 0, a, bars) &&
+                wait_or_abort(&bars->k_full[0], 0, a, bars);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_qk(0, 0);
+        issue_qk(1, 0);
+      }
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int st = j % KV_STAGES;
+        const uint32_t ph = j & 1;
+        if (!wait_or_abort(&bars->p_full[0], ph, a, bars) ||
+            !wait_or_abort(&bars->v_conv[st], (j / KV_STAGES) & 1, a, bars)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        issue_pv(0, j);
+        if (j + 1 < nkt) {
+          if (!wait_or_abort(&bars->k_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1, a,
+                             bars) ||
+              !wait_or_abort(&bars->s_free[0], ph, a, bars)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          issue_qk(0, j + 1);
+        }
+        if (!wait_or_abort(&bars->p_full[1], ph, a, bars)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        issue_pv(1, j);
+        ptx::mma_commit(&bars->kv_empty[st]);
+        if (j + 1 < nkt) {
+          if (!wait_or_abort(&bars->s_free[1], ph, a, bars)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          issue_qk(1, j + 1);
+        }
+      }
+      if (!ok && any) {  // let issued MMAs finish before TMEM is released
+        ptx::mma_commit(&bars->drain);
+        ptx::mbar_wait(&bars->drain, 0, kDrainWaitLimit, nullptr);
+      }
+    }
+  } else if (warp >= 10) {
+    // ------------------------------------------------------------ V: bf16 -> fp16 in place
+    const int ct = threadIdx.x - 320;  // 0..63
+    for (int j = 0; j < nkt; ++j) {
+      const int st = j % KV_STAGES;
+      if (!wait_or_abort(&bars->v_full[st], (j / KV_STAGES) & 1, a, bars)) break;
+      uint4* v = reinterpret_cast<uint4*>(smem + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES);
+#pragma unroll 4
+      for (int i = ct; i < TILE_BYTES / 16; i += 64) {
+        uint4 u = v[i];
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+          __half2 hv = __floats2half2_rn(lo, hi);
+          w[e] = *reinterpret_cast<uint32_t*>(&hv);
+        }
+        v[i] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->v_conv[st]);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const int t = warp >> 2;             // query tile of this warpgroup
+    const int quarter = warp & 3;        // TMEM lanes [32*quarter, +32)
+    const int r = quarter * 32 + lane;   // row within the query tile
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    uint8_t* pbuf = smem + OFF_P + t * P_BYTES;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkt; ++j) {
+      const uint32_t ph = j & 1;
+      if (!wait_or_abort(&bars->s_full[t], ph, a, bars)) { ok = false; break; }
+      ptx::tc_fence_after();
+      uint32_t s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        ptx::tmem_ld32(tS[t] + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->s_free[t]);
+      const int nvalid = min(KT, a.L - j * KT);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        float v = __uint_as_float(s[i]);
+        if (i >= nvalid) v = -INFINITY;
+        s[i] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      const float m_new = mx * kScaleLog2;
+      const bool resc = m_new > m_ref + kRescaleThreshold;
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2(m_ref - m_new);  // 0 on the first tile
+        m_ref = m_new;
+        l *= alpha;
+      }
+      uint32_t pk[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float p0 = ex2(fmaf(__uint_as_float(s[2 * i]), kScaleLog2, -m_ref));
+        const float p1 = ex2(fmaf(__uint_as_float(s[2 * i + 1]), kScaleLog2, -m_ref));
+        l += p0 + p1;
+        __half2 hv = __floats2half2_rn(p0, p1);
+        pk[i] = *reinterpret_cast<uint32_t*>(&hv);
+      }
+      if (j > 0) {
+        // P buffer free and O quiescent once the previous P V has completed
+        if (!wait_or_abort(&bars->pv_done[t], ph ^ 1, a, bars)) { ok = false; break; }
+        ptx::tc_fence_after();
+        if (__any_sync(0xffffffffu, resc)) {
+          uint32_t o[32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            ptx::tmem_ld32(tO[t] + lane_off + c * 32, o);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            ptx::tmem_st32(tO[t] + lane_off + c * 32, o);
+          }
+          ptx::tmem_st_wait();
+        }
+      }
+      // fp16 P row r, K-major 128-byte swizzled: keys [0,64) then [64,128)
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        uint8_t* dst = pbuf + (c >> 3) * (QT * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->p_full[t]);
+    }
+    if (ok && wait_or_abort(&bars->pv_done[t], (nkt - 1) & 1, a, bars)) {
+      ptx::tc_fence_after();
+      const int row_in_patch = (2 * pair + t) * QT + r;
+      const bool valid = row_in_patch < a.Lp;
+      const float inv = 1.f / l;
+      __nv_bfloat16* dst =
+          a.o + ((long long)b * a.L + patch0 + row_in_patch) * (long long)(a.heads * D) + h * D;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        ptx::tmem_ld32(tO[t] + lane_off + c * 32, o);
+        ptx::tmem_ld_wait();
+        if (valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            d4[i] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * i]) * inv,
+                                           __uint_as_float(o[8 * i + 1]) * inv),
+                               pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv,
+                                           __uint_as_float(o[8 * i + 3]) * inv),
+                               pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv,
+                                           __uint_as_float(o[8 * i + 5]) * inv),
+                               pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv,
+                                           __uint_as_float(o[8 * i + 7]) * inv));
+          }
+        }
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+bool make_map3(CUtensorMap* m, const void* base, int L, int B, int C, int box_rows) {
+  auto fn = tc_encode_fn();
+  if (!fn) return false;
+  const uint64_t dims[3] = {(uint64_t)C, (uint64_t)L, (uint64_t)B};
+  const uint64_t strides[2] = {(uint64_t)C * 2, (uint64_t)L * C * 2};
+  const uint32_t box[3] = {64, (uint32_t)box_rows, 1};
+  const uint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int set_attn_smem() {
+  static std::once_flag once;
+  static int rc = DPP_OK;
+  std::call_once(once, [] {
+    if (cudaFuncSetAttribute(tc_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             ATTN_SMEM) != cudaSuccess)
+      rc = DPP_ERR_CUDA;
+  });
+  return rc;
+}
+
+}  // namespace
+
+int launch_tc_attention(const void* q, const void* kf, const void* vf, const void* ks,
+                        const void* vs, void* o, int B, int L, int heads, int P, int* status,
+                        long long wait_limit, cudaStream_t s) {
+  const int Lp = L / P;
+  if (L % P || Lp % 8) return DPP_ERR_SHAPE;
+  int g = 128;
+  while (Lp % g) g >>= 1;
+  const int C = heads * D;
+  int rc = set_attn_smem();
+  if (rc) return rc;
+  CUtensorMap mq, mkf, mks, mvf, mvs;
+  if (!make_map3(&mq, q, L, B, C, QT) || !make_map3(&mkf, kf, L, B, C, g) ||
+      !make_map3(&mks, ks, L, B, C, g) || !make_map3(&mvf, vf, L, B, C, g) ||
+      !make_map3(&mvs, vs, L, B, C, g))
+    return DPP_ERR_CUDA;
+  AttnArgs a{};
+  a.L = L; a.heads = heads; a.P = P; a.Lp = Lp; a.g = g;
+  a.n_qt = (Lp + QT - 1) / QT;
+  a.n_pairs = (a.n_qt + 1) / 2;
+  a.nkt = (L + KT - 1) / KT;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.status = status;
+  a.wait_limit = wait_limit;
+  dim3 grid(a.n_pairs * P, heads, B);
+  tc_attn_kernel<<<grid, ATTN_THREADS, ATTN_SMEM, s>>>(mq, mkf, mks, mvf, mvs, a);
+  return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+}
+
+}  // namespace dpp

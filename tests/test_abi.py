@@ -1,0 +1,103 @@
+"""The C-ABI library loads and exports every function include/dpp.h declares;
+host-side argument checks (no GPU needed: they fail before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import stale_activations_gb300 as dpp
+from stale_activations_gb300 import build as dbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dbuild.build_library()
+    return dpp.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "dpp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_four_calls():
+    names = _declared_functions()
+    for n in ("patch_layer_step", "halo_conv3x3", "stale_kv_attention", "refresh_residual"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), f"libdpp.so does not export {n}"
+    assert set(dpp.EXPORTS) <= set(names)
+
+
+def test_status_strings(lib):
+    assert dpp.status_string(0) == "ok"
+    assert "timeout" in dpp.status_string(6)
+    assert lib.dpp_version() >= 100
+
+
+def _params(**kw):
+    base = dict(B=2, H=64, W=64, C=640, P=4, G=32, heads=10, dtype=dpp.BF16)
+    base.update(kw)
+    return dpp.make_params(**base)
+
+
+def test_workspace_layout_sizes(lib):
+    prm = _params()
+    lo = dpp.workspace_layout(prm)
+    act = 2 * 64 * 64 * 640 * 2
+    assert lo.total >= 6 * act
+    offs = [lo.status, lo.gn_partial, lo.gn_fresh, lo.y, lo.h, lo.q, lo.k, lo.v, lo.o]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    n, nb = dpp.message_sizes(prm)
+    blc = 2 * 4096 * 640
+    assert n == 2 * blc + 2 * 3 * 2 * 64 * 640
+    assert nb == 2 * blc // 128 + 2 * 3 * (2 * 64 * 640 // 128)
+
+
+@pytest.mark.parametrize("kw", [dict(H=63), dict(P=3), dict(C=600, heads=10), dict(G=7),
+                                dict(heads=5), dict(dtype=7), dict(W=48)])
+def test_invalid_params_rejected(lib, kw):
+    prm = _params(**kw)
+    assert lib.dpp_workspace_size(ctypes.byref(prm)) == 0
+    lo = dpp.WorkspaceLayout()
+    assert lib.dpp_workspace_query(ctypes.byref(prm), ctypes.byref(lo)) != 0
+
+
+def test_fp32_tiny_params_accepted(lib):
+    prm = _params(B=1, H=32, W=32, C=64, P=2, G=8, heads=1, dtype=dpp.F32)
+    assert dpp.workspace_size(prm) > 0
+    assert dpp.layer_kernel_count(prm, dpp.SYNC) == 6
+    assert dpp.layer_kernel_count(prm, dpp.STALE) == 7
+
+
+def test_host_checks_without_launch(lib):
+    vp = ctypes.c_void_p
+    # n == 0 is a no-op, null pointers / bad dtype / bad sizes are rejected
+    assert lib.refresh_residual(None, None, None, None, 0, dpp.BF16, None) == 0
+    assert lib.refresh_residual(None, None, None, None, 5, dpp.BF16, None) == 1
+    assert lib.refresh_residual(vp(16), vp(16), vp(16), vp(16), 5, 9, None) == 4
+    assert lib.refresh_residual(vp(16), vp(16), vp(16), vp(16), -1, dpp.BF16, None) == 2
+    assert lib.refresh_residual(vp(16), vp(24), vp(16), vp(16), 5, dpp.BF16, None) == 3
+    assert lib.halo_conv3x3(None, None, None, None, 1, 8, 8, 64, 128, 2, dpp.BF16, None, None) == 1
+    a = vp(256)
+    assert lib.halo_conv3x3(a, a, a, a, 1, 9, 64, 64, 128, 2, dpp.BF16, None, None) == 2
+    assert lib.halo_conv3x3(a, a, a, a, 1, 8, 64, 64, 100, 2, dpp.BF16, None, None) == 2
+    assert lib.stale_kv_attention(a, a, a, a, a, a, 1, 1024, 2, 32, 2, dpp.BF16, None, None) == 2
+    assert lib.stale_kv_attention(a, a, a, a, a, a, 1, 1000, 2, 64, 3, dpp.BF16, None, None) == 2
+    assert lib.stale_kv_attention(a, a, a, a, a, vp(8), 1, 1024, 2, 64, 2, dpp.BF16, None,
+                                  None) == 3
+    prm = _params()
+    w = dpp.LayerWeights()
+    st = dpp.LayerState()
+    assert lib.patch_layer_step(ctypes.byref(prm), ctypes.byref(w), ctypes.byref(st), a, a, 0, a,
+                                None) == 1

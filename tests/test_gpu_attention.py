@@ -1,0 +1,65 @@
+"""GPU parity: stale_kv_attention against the CPU oracle; the fresh/stale splice
+range pinned bit-exactly with a uniform-softmax sentinel."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import stale_activations_gb300 as dpp
+import synth
+from tests.util import TOL_BF16, TOL_F32, np64, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _attn_gpu(q, kf, vf, ks, vs, heads, P):
+    o = torch.empty_like(q, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dpp.stale_kv_attention(q.cuda(), kf.cuda(), vf.cuda(), ks.cuda(), vs.cuda(), o, heads, P,
+                           dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return o
+
+
+@pytest.mark.parametrize("dtype,B,L,heads,P", [
+    ("bf16", 1, 1024, 2, 4),
+    ("bf16", 2, 960, 1, 8),     # 120-token patches: ragged query tiles, straddling key tiles
+    ("bf16", 1, 4096, 10, 4),   # the SDXL-1024 mid-level attention
+    ("f32", 1, 1024, 1, 2),
+    ("f32", 1, 96, 2, 3),
+])
+def test_attention_matches_oracle(dtype, B, L, heads, P):
+    q, kf, vf, ks, vs = synth.attention_inputs(B, L, heads, 64, dtype, seed=L + heads)
+    o = _attn_gpu(q, kf, vf, ks, vs, heads, P)
+    ref = oracle.stale_kv_attention(*(np64(t) for t in (q, kf, vf, ks, vs)), heads, P, dtype)
+    assert rel_err(np64(o), ref) < (TOL_BF16 if dtype == "bf16" else TOL_F32)
+
+
+@pytest.mark.parametrize("L,P", [(1024, 4), (960, 8), (14400, 8)])
+def test_attention_splice_sentinel_bitexact(L, P):
+    """Q = 0 gives a uniform softmax; V_fresh = +1 and V_stale = -1 then give
+    (2*Lp - L)/L in every output (exact in bf16 for these sizes).  L/P = 1800 makes
+    the splice granularity 8 rows (sub-boxes of 8 keys)."""
+    heads = 2
+    C = heads * 64
+    q = torch.zeros(1, L, C, dtype=torch.bfloat16)
+    k = synth.attention_inputs(1, L, heads, 64, "bf16", seed=3)[1]
+    vf = torch.ones(1, L, C, dtype=torch.bfloat16)
+    vs = -torch.ones(1, L, C, dtype=torch.bfloat16)
+    o = _attn_gpu(q, k, vf, k, vs, heads, P).float().cpu()
+    Lp = L // P
+    exp = (2 * Lp - L) / L
+    np.testing.assert_array_equal(o.numpy(), float(torch.tensor(exp).to(torch.bfloat16)))
+
+
+def test_attention_sdxl3840_sampled_rows():
+    """The SDXL-3840 attention level: B=2, L=57600, 10 heads, P=8 (7200-token
+    patches).  Sampled query rows (patch edges, tile edges, interiors) vs the oracle."""
+    B, L, heads, P = 2, 57600, 10, 8
+    q, kf, vf, ks, vs = synth.attention_inputs(B, L, heads, 64, "bf16", seed=0)
+    o = _attn_gpu(q, kf, vf, ks, vs, heads, P)
+    rows = np.array([0, 127, 128, 7199, 7200, 7327, 7328, 14399, 30000, 50399, 50400, 57599])
+    ref = oracle.stale_kv_attention(*(np64(t) for t in (q, kf, vf, ks, vs)), heads, P, "bf16",
+                                    rows=rows)
+    assert rel_err(np64(o)[:, rows], ref) < TOL_BF16

@@ -414,3 +414,14 @@ def test_multirank_copies_stay_identical():
         # own rows of the reconstruction are the quantised fresh rows; never a blend
         # of two steps: every element is either the old value or old + code*scale
         shared = shared_new
+
+
+def test_conv_rows_subset_matches_full():
+    B, H, W, Ci, Co, P = 1, 12, 5, 4, 3, 3
+    yf = RNG.standard_normal((B, H, W, Ci))
+    ys = RNG.standard_normal((B, H, W, Ci))
+    w = RNG.standard_normal((Co, 3, 3, Ci))
+    full = oracle.halo_conv3x3(yf, ys, w, P, "f64")
+    rows = np.array([0, 3, 4, 7, 11])
+    np.testing.assert_allclose(oracle.halo_conv3x3(yf, ys, w, P, "f64", rows=rows), full[:, rows],
+                               rtol=1e-13, atol=1e-13)
