@@ -158,6 +158,9 @@ def run_gpu(args):
 
     K = args.steps
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(K)]
+    for row in events:      # create the events (the library re-records them in the step)
+        for e in row:
+            e.record(stream)
 
     def barrier():
         if ws_n > 1:

@@ -299,15 +299,15 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bars->s_free[t]);
-      const int nvalid = min(KT, a.L - j * KT);
+      const int nvalid = a.L - j * KT;
+      if (nvalid < KT) {  // only the last key tile can be partial: mask keys >= L
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= nvalid) s[i] = __float_as_uint(-INFINITY);
+      }
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        float v = __uint_as_float(s[i]);
-        if (i >= nvalid) v = -INFINITY;
-        s[i] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
-      }
+      for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
       const float m_new = mx * kScaleLog2;
       const bool resc = m_new > m_ref + kRescaleThreshold;
       float alpha = 1.f;
