@@ -259,6 +259,9 @@ def run_gpu(args):
         "wall_s_timed_region": wall,
     }
     line["clocks"] = clocks.summary()
+    if not args.no_secondary:
+        line["secondary"] = {"attention_sdxl3840": measure_attention_3840(dev, peaks),
+                             "refresh_sweep": measure_refresh_sweep(dev, peaks)}
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
     if ws_n > 1:
@@ -266,6 +269,80 @@ def run_gpu(args):
         tdist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line))
+
+
+def _randn_bf16(shape, gen, dev):
+    import torch
+    return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+
+def measure_attention_3840(dev, peaks, iters=5):
+    """stale_kv_attention alone at the SDXL-3840 attention level: B=2, L=57600,
+    10 heads x 64, P=8; K/V_stale = fresh + N(0, 0.05^2).  Inputs (0.74 GB) exceed L2."""
+    import torch
+
+    import stale_activations_gb300 as dpp
+    B, L, heads, P = 2, 57600, 10, 8
+    g = torch.Generator(device=dev).manual_seed(1)
+    q, kf, vf = (_randn_bf16((B, L, 640), g, dev) for _ in range(3))
+    ks = (kf.float() + 0.05 * torch.randn(kf.shape, generator=g, device=dev)).to(torch.bfloat16)
+    vs = (vf.float() + 0.05 * torch.randn(vf.shape, generator=g, device=dev)).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(2):
+        dpp.stale_kv_attention(q, kf, vf, ks, vs, o, heads, P, dev_status=st)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
+    torch.cuda.synchronize()
+    ev[0].record()
+    for i in range(iters):
+        dpp.stale_kv_attention(q, kf, vf, ks, vs, o, heads, P, dev_status=st)
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    if st.item() != 0:
+        raise RuntimeError("attention device status set")
+    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(iters)]
+    flop = 4.0 * B * heads * L * L * 64
+    tfs = flop / (statistics.mean(ms) * 1e-3) / 1e12
+    return {"ms_mean": statistics.mean(ms), "ms_min": min(ms), "TFLOP/s": tfs,
+            "frac_of_burst_bf16": tfs / peaks["bf16"], "peak_burst": peaks["bf16"],
+            "frac_of_sustained_bf16": tfs / peaks["bf16_sus"], "flop_per_launch": flop,
+            "launches": iters, "note": "back-to-back launches, inputs > L2"}
+
+
+def measure_refresh_sweep(dev, peaks, iters=5):
+    """refresh_residual alone over 200 MiB of bf16 stale buffers + the 2x4x128x128 noise
+    prediction (one flat buffer); stale restored and L2 flushed before each launch."""
+    import torch
+
+    import stale_activations_gb300 as dpp
+    n = 200 * 1024 * 1024 // 2 + 2 * 4 * 128 * 128
+    g = torch.Generator(device=dev).manual_seed(2)
+    stale0 = _randn_bf16((n,), g, dev)
+    nblk = n // 128
+    spike = (torch.rand(nblk, generator=g, device=dev) < 0.1).repeat_interleave(128)
+    std = torch.where(spike, 1.0, 0.05)
+    fresh = (stale0.float() + std * torch.randn(n, generator=g, device=dev)).to(torch.bfloat16)
+    del spike, std
+    stale = torch.empty_like(stale0)
+    codes = torch.empty(n, dtype=torch.int8, device=dev)
+    scales = torch.empty(nblk, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    ms = []
+    for i in range(iters + 2):
+        stale.copy_(stale0)
+        flush.fill_(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dpp.refresh_residual(fresh, stale, codes, scales)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 2:
+            ms.append(e0.elapsed_time(e1))
+    nbytes = 7.03125 * n
+    gbs = nbytes / (statistics.mean(ms) * 1e-3) / 1e9
+    return {"ms_mean": statistics.mean(ms), "ms_min": min(ms), "GB/s": gbs,
+            "frac_hbm": gbs / peaks["hbm"], "peak_hbm": peaks["hbm"], "elements": n,
+            "bytes_per_launch": nbytes, "launches": iters}
 
 
 # ------------------------------------------------------------------ CPU oracle (reference arm)
@@ -342,6 +419,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the standalone SDXL-3840 attention and refresh-sweep lines")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

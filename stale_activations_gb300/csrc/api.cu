@@ -340,29 +340,36 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
     return mark(6);
   }
   if (!refresh) return mark(6);
+  // Segments in message order (K, V, then each batch's P-1 halo ranges), packed
+  // into fixed-size tables on the stack and launched whenever a table fills up.
   const long long blc = M * p.C;
-  const int nseg = 2 + p.B * (p.P - 1);
-  dpp::RefreshSeg* segs = static_cast<dpp::RefreshSeg*>(malloc(sizeof(dpp::RefreshSeg) * nseg));
-  if (!segs) return DPP_ERR_UNSUPPORTED;
+  dpp::RefreshTable tab{};
   long long coff = 0, soff = 0;
-  auto add = [&](int i, const void* fr, void* stl, long long n) {
+  auto add = [&](const void* fr, void* stl, long long n) -> int {
     const bool ok = aligned16(fr) && aligned16(stl) && aligned16(st->codes + coff);
-    segs[i] = dpp::RefreshSeg{fr, stl, st->codes + coff, st->scales + soff, n, ok ? 1 : 0, 0};
+    tab.seg[tab.nseg] =
+        dpp::RefreshSeg{fr, stl, st->codes + coff, st->scales + soff, n, ok ? 1 : 0, 0};
+    tab.blk_start[tab.nseg + 1] = tab.blk_start[tab.nseg] + cdiv(n, 128);
+    ++tab.nseg;
     coff += n;
     soff += cdiv(n, 128);
+    if (tab.nseg == dpp::kMaxRefreshSegs) {
+      const int r = dpp::launch_refresh(tab, p.dtype, s);
+      tab.nseg = 0;
+      tab.blk_start[0] = 0;
+      return r;
+    }
+    return DPP_OK;
   };
-  add(0, k, st->k_stale, blc);
-  add(1, v, st->v_stale, blc);
-  int i = 2;
+  if ((rc = add(k, st->k_stale, blc)) || (rc = add(v, st->v_stale, blc))) return rc;
   for (int b = 0; b < p.B; ++b)
     for (int pp = 1; pp < p.P; ++pp) {
       const size_t off = b * img_bytes + pp * band_bytes - halo_bytes / 2;
-      add(i++, static_cast<char*>(y) + off, static_cast<char*>(st->y_stale) + off,
-          2ll * p.W * p.C);
+      rc = add(static_cast<char*>(y) + off, static_cast<char*>(st->y_stale) + off,
+               2ll * p.W * p.C);
+      if (rc) return rc;
     }
-  rc = refresh_segments(segs, nseg, p.dtype, s);
-  free(segs);
-  if (rc) return rc;
+  if (tab.nseg > 0 && (rc = dpp::launch_refresh(tab, p.dtype, s))) return rc;
   DPP_CUDA_CHECK(cudaMemcpyAsync(st->gn_stats, gn_fresh, gn_bytes, cudaMemcpyDeviceToDevice, s));
   return mark(6);
 }
