@@ -56,6 +56,8 @@ extern "C" {
 #define DPP_ERR_BOUNDS 7      /* device status: an index check failed (debug builds) */
 #define DPP_ERR_UNSUPPORTED 8 /* the combination is not implemented */
 #define DPP_ERR_ARG 9         /* an enum/flag argument is invalid */
+#define DPP_ERR_SCRATCH_LIMIT 10 /* the layer needs more workspace than the fixed
+                                    scratch of patch_layer_step_noalloc */
 
 #define DPP_F32 0
 #define DPP_BF16 1
@@ -209,6 +211,33 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
 /* Synchronizes `stream` and returns the workspace's device status word
  * (DPP_OK, DPP_ERR_TIMEOUT, ...), or DPP_ERR_CUDA if the copy fails. */
 int dpp_read_device_status(const void* workspace, void* stream);
+
+/*
+ * patch_layer_step_noalloc -- patch_layer_step without a caller workspace.
+ * (The pages have no counterpart of this call; it exists for callers that cannot
+ * allocate device memory when they run a layer: a plugin in a host framework
+ * whose own allocator and budget own all device memory, or a latency-critical
+ * loop where cudaMalloc's implicit synchronisation is not allowed.)
+ *
+ * Same arguments, semantics and results as patch_layer_step, except that the
+ * workspace is one fixed 64 MiB array of device memory inside the library; no
+ * cudaMalloc, cudaFree or other allocating routine is called.  Every GPU that
+ * loads this part of the library holds the 64 MiB until the process exits.
+ *   - Layers whose dpp_workspace_size() exceeds 64 MiB return
+ *     DPP_ERR_SCRATCH_LIMIT before anything is launched (the SDXL-1024
+ *     mid-level layer, B=2 x 64x64 x 640 bf16, needs about 60 MiB).
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture on that device.
+ *   - All calls share the one array and it keeps the last call's contents:
+ *     calls whose work overlaps on the GPU (different streams, or another
+ *     thread) race on it and must be serialised by the caller.
+ *   - The device status word lives inside the array and is not readable by the
+ *     caller; a kernel that gives up still returns early, as with patch_layer_step.
+ */
+int patch_layer_step_noalloc(const dpp_layer_params* prm, const dpp_layer_weights* wts,
+                             const dpp_layer_state* st, const void* x, void* out, int mode,
+                             void* stream);
 
 /* Number of kernels one patch_layer_step launches for these params and mode. */
 int dpp_layer_kernel_count(const dpp_layer_params* prm, int mode);

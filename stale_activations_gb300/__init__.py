@@ -58,7 +58,7 @@ _lib = None
 EXPORTS = ("dpp_status_string", "dpp_version", "refresh_residual", "halo_conv3x3",
            "stale_kv_attention", "dpp_workspace_query", "dpp_workspace_size", "dpp_message_elems",
            "dpp_message_blocks", "patch_layer_step", "patch_layer_step_timed",
-           "dpp_read_device_status", "dpp_layer_kernel_count")
+           "dpp_read_device_status", "dpp_layer_kernel_count", "patch_layer_step_noalloc")
 
 
 def load(build_if_missing: bool = False):
@@ -96,6 +96,9 @@ def load(build_if_missing: bool = False):
     lib.patch_layer_step_timed.restype = _c_int
     lib.patch_layer_step_timed.argtypes = [P(LayerParams), P(LayerWeights), P(LayerState), _c_void,
                                            _c_void, _c_int, _c_void, _c_void, _c_void]
+    lib.patch_layer_step_noalloc.restype = _c_int
+    lib.patch_layer_step_noalloc.argtypes = [P(LayerParams), P(LayerWeights), P(LayerState),
+                                             _c_void, _c_void, _c_int, _c_void]
     lib.dpp_read_device_status.restype = _c_int
     lib.dpp_read_device_status.argtypes = [_c_void, _c_void]
     lib.dpp_layer_kernel_count.restype = _c_int
@@ -220,6 +223,24 @@ def patch_layer_step(prm: LayerParams, weights: dict, state: dict, x, out, mode:
                                       _ptr(x), _ptr(out), mode, _ptr(workspace), _stream(stream),
                                       evs),
            "patch_layer_step_timed")
+
+
+def patch_layer_step_noalloc(prm: LayerParams, weights: dict, state: dict, x, out, mode: int,
+                             stream=None):
+    """patch_layer_step with the library's fixed 64 MiB device scratch as workspace.
+
+    For callers that cannot allocate device memory when they run a layer; nothing
+    is allocated here or in the library.  Calls that overlap on the GPU share the
+    scratch and race; the first call on a device should precede any stream capture.
+    """
+    lib = load()
+    w = LayerWeights(_ptr(weights["gamma"]), _ptr(weights["beta"]), _ptr(weights["w_conv"]),
+                     _ptr(weights["w_qkv"]), _ptr(weights["w_o"]))
+    s = LayerState(_ptr(state["gn_stats"]), _ptr(state["y_stale"]), _ptr(state["k_stale"]),
+                   _ptr(state["v_stale"]), _ptr(state.get("codes")), _ptr(state.get("scales")))
+    _check(lib.patch_layer_step_noalloc(ctypes.byref(prm), ctypes.byref(w), ctypes.byref(s),
+                                        _ptr(x), _ptr(out), mode, _stream(stream)),
+           "patch_layer_step_noalloc")
 
 
 def read_device_status(workspace, stream=None) -> int:

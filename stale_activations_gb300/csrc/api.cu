@@ -167,6 +167,7 @@ const char* dpp_status_string(int status) {
     case DPP_ERR_BOUNDS: return "device index check failed";
     case DPP_ERR_UNSUPPORTED: return "unsupported combination";
     case DPP_ERR_ARG: return "invalid argument";
+    case DPP_ERR_SCRATCH_LIMIT: return "layer workspace exceeds the fixed no-alloc scratch";
     default: return "unknown status";
   }
 }
