@@ -214,41 +214,33 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         issue_qk(0, 0);
         issue_qk(1, 0);
       }
+      // Per key tile j and query tile t: S_t(j+1) = Q_t K(j+1)^T is issued as soon as
+      // softmax t has read S_t(j), before O_t += P_t(j) V(j), so the tensor pipe
+      // computes the next scores while the softmax warps exponentiate.
       for (int j = 0; j < nkt && ok; ++j) {
         const int st = j % KV_STAGES;
         const uint32_t ph = j & 1;
-        if (!wait_or_abort(&bars->p_full[0], ph, a, bars) ||
-            !wait_or_abort(&bars->v_conv[st], (j / KV_STAGES) & 1, a, bars)) {
+        const bool more = j + 1 < nkt;
+        if (more && !wait_or_abort(&bars->k_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1,
+                                   a, bars)) {
           ok = false;
           break;
         }
-        ptx::tc_fence_after();
-        issue_pv(0, j);
-        if (j + 1 < nkt) {
-          if (!wait_or_abort(&bars->k_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1, a,
-                             bars) ||
-              !wait_or_abort(&bars->s_free[0], ph, a, bars)) {
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (more) {
+            if (!wait_or_abort(&bars->s_free[t], ph, a, bars)) { ok = false; break; }
+            ptx::tc_fence_after();
+            issue_qk(t, j + 1);
+          }
+          if (!wait_or_abort(&bars->p_full[t], ph, a, bars) ||
+              (t == 0 && !wait_or_abort(&bars->v_conv[st], (j / KV_STAGES) & 1, a, bars))) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          issue_qk(0, j + 1);
+          issue_pv(t, j);
         }
-        if (!wait_or_abort(&bars->p_full[1], ph, a, bars)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        issue_pv(1, j);
-        ptx::mma_commit(&bars->kv_empty[st]);
-        if (j + 1 < nkt) {
-          if (!wait_or_abort(&bars->s_free[1], ph, a, bars)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          issue_qk(1, j + 1);
-        }
+        if (ok) ptx::mma_commit(&bars->kv_empty[st]);
       }
       if (!ok && any) {  // let issued MMAs finish before TMEM is released
         ptx::mma_commit(&bars->drain);
@@ -305,9 +297,13 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         for (int i = 0; i < 128; ++i)
           if (i >= nvalid) s[i] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 independent chains
 #pragma unroll
-      for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
+      for (int i = 0; i < 128; i += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mq[u] = fmaxf(mq[u], __uint_as_float(s[i + u]));
+      }
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       const float m_new = mx * kScaleLog2;
       const bool resc = m_new > m_ref + kRescaleThreshold;
       float alpha = 1.f;
@@ -317,14 +313,17 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         l *= alpha;
       }
       uint32_t pk[64];
+      float lq[4] = {0.f, 0.f, 0.f, 0.f};  // 4 independent partial row sums
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
         const float p0 = ex2(fmaf(__uint_as_float(s[2 * i]), kScaleLog2, -m_ref));
         const float p1 = ex2(fmaf(__uint_as_float(s[2 * i + 1]), kScaleLog2, -m_ref));
-        l += p0 + p1;
+        lq[(2 * i) & 3] += p0;
+        lq[(2 * i + 1) & 3] += p1;
         __half2 hv = __floats2half2_rn(p0, p1);
         pk[i] = *reinterpret_cast<uint32_t*>(&hv);
       }
+      l += (lq[0] + lq[1]) + (lq[2] + lq[3]);
       if (j > 0) {
         // P buffer free and O quiescent once the previous P V has completed
         if (!wait_or_abort(&bars->pv_done[t], ph ^ 1, a, bars)) { ok = false; break; }
