@@ -109,6 +109,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_max(x: float, dev) -> float:
+    """Max of a per-rank float over all ranks (the job is as slow as its slowest rank)."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(steps: int, world: int, max_total_ms: float) -> float:
+    """Steps per second of the whole job: every rank ran `steps` steps, timed by the slowest."""
+    return world * steps / (max_total_ms / 1e3)
+
+
 def _layer_setup(dev):
     import torch
 
@@ -181,13 +197,9 @@ def run_gpu(args):
     stage_ms = [[events[i][s].elapsed_time(events[i][s + 1]) for s in range(nst - 1)]
                 for i in range(K)]
     step_ms = [events[i][0].elapsed_time(events[i][nst - 1]) for i in range(K)]
-    tot_ms = sum(step_ms)
-    if ws_n > 1:
-        t = torch.tensor([tot_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        tot_ms = t.item()
+    tot_ms = reduce_max(sum(step_ms), dev)
     ms_per_step = tot_ms / K
-    value = ws_n * K / (tot_ms / 1e3)
+    value = whole_job_rate(K, ws_n, tot_ms)
 
     # per-stage averages and the roofline of the dominant kernel (attention)
     avg = {name: sum(r[i] for r in stage_ms) / K for i, name in enumerate(dpp.STAGES)}
@@ -238,11 +250,8 @@ def run_gpu(args):
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
     barrier()
-    if ws_n > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_ms = t.item()
-    e2e = {"value": ws_n * K / (e2e_ms / 1e3), "unit": "steps/s",
+    e2e_ms = reduce_max(e2e_ms, dev)
+    e2e = {"value": whole_job_rate(K, ws_n, e2e_ms), "unit": "steps/s",
            "h2d_bytes_per_step": x_pin.numel() * x_pin.element_size(),
            "d2h_bytes_per_step": out_pin.numel() * out_pin.element_size()}
 
@@ -261,7 +270,8 @@ def run_gpu(args):
     line["clocks"] = clocks.summary()
     if not args.no_secondary:
         line["secondary"] = {"attention_sdxl3840": measure_attention_3840(dev, peaks),
-                             "refresh_sweep": measure_refresh_sweep(dev, peaks)}
+                             "refresh_sweep": measure_refresh_sweep(dev, peaks),
+                             "layer_2x256x256x640_p8": measure_large_layer(dev, peaks)}
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
     if ws_n > 1:
@@ -343,6 +353,52 @@ def measure_refresh_sweep(dev, peaks, iters=5):
     return {"ms_mean": statistics.mean(ms), "ms_min": min(ms), "GB/s": gbs,
             "frac_hbm": gbs / peaks["hbm"], "peak_hbm": peaks["hbm"], "elements": n,
             "bytes_per_launch": nbytes, "launches": iters}
+
+
+def measure_large_layer(dev, peaks, iters=3):
+    """One STALE layer step on a map larger than L2 (B=2, 256x256, C=640, P=8, 10 heads):
+    the GroupNorm and refresh stages as HBM streams, with per-stage CUDA events."""
+    import torch
+
+    import stale_activations_gb300 as dpp
+    B, H, W, C, P, G, heads = 2, 256, 256, 640, 8, 32, 10
+    prm = dpp.make_params(B, H, W, C, P, G, heads, dpp.BF16, refresh=True)
+    state, ws = dpp.alloc_layer(prm, device=dev)
+    g = torch.Generator(device=dev).manual_seed(3)
+    wts = {"gamma": torch.ones(C, device=dev), "beta": torch.zeros(C, device=dev),
+           "w_conv": (0.02 * torch.randn(C, 3, 3, C, generator=g, device=dev)).to(torch.bfloat16),
+           "w_qkv": (0.02 * torch.randn(3 * C, C, generator=g, device=dev)).to(torch.bfloat16),
+           "w_o": (0.02 * torch.randn(C, C, generator=g, device=dev)).to(torch.bfloat16)}
+    x = _randn_bf16((B, H, W, C), g, dev)
+    xp = (x.float() + 0.05 * torch.randn(x.shape, generator=g, device=dev)).to(torch.bfloat16)
+    out = torch.empty_like(x)
+    dpp.patch_layer_step(prm, wts, state, xp, out, dpp.SYNC, ws)
+    dpp.patch_layer_step(prm, wts, state, x, out, dpp.STALE, ws)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(dpp.NUM_STAGE_EVENTS)]
+           for _ in range(iters)]
+    for row in evs:
+        for e in row:
+            e.record()
+    for i in range(iters):
+        dpp.patch_layer_step(prm, wts, state, x, out, dpp.STALE, ws, stage_events=evs[i])
+    torch.cuda.synchronize()
+    if dpp.read_device_status(ws) != 0:
+        raise RuntimeError("device status set in the large layer")
+    avg = {n: sum(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(iters)) / iters
+           for k, n in enumerate(dpp.STAGES)}
+    act = B * H * W * C
+    L = H * W
+    gn_gbs = 3 * act * 2 / (avg["groupnorm"] * 1e-3) / 1e9
+    ref_bytes = 7.03125 * (2 * act + B * (P - 1) * 2 * W * C)
+    ref_gbs = ref_bytes / (avg["state_update"] * 1e-3) / 1e9
+    attn_tfs = 4.0 * B * heads * L * L * 64 / (avg["attention"] * 1e-3) / 1e12
+    conv_tfs = 2.0 * B * L * C * 9 * C / (avg["halo_conv"] * 1e-3) / 1e12
+    step_ms = sum(avg.values())
+    return {"ms_per_step": step_ms, "stage_ms": avg,
+            "groupnorm_GB/s": gn_gbs, "groupnorm_frac_hbm": gn_gbs / peaks["hbm"],
+            "refresh_GB/s": ref_gbs, "refresh_frac_hbm": ref_gbs / peaks["hbm"],
+            "attention_TFLOP/s": attn_tfs, "conv_TFLOP/s": conv_tfs,
+            "note": "GroupNorm algorithmic bytes 6 B/elem (stats read, apply read+write)"}
 
 
 # ------------------------------------------------------------------ CPU oracle (reference arm)

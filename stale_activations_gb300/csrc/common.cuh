@@ -10,10 +10,11 @@
 namespace dpp {
 
 constexpr int kNumSMs = 152;              // GB300: 2 dies x 76 SMs (grid sizing hint)
-// Bounded waits: no legitimate wait in these kernels lasts more than microseconds;
-// a try_wait may suspend the thread for a short system-dependent time per try.
-constexpr long long kDefaultWaitLimit = 1ll << 21;  // bounded-wait iterations
-constexpr long long kDrainWaitLimit = 1ll << 21;    // waits for own copies before exit
+// Bounded waits: no legitimate wait in these kernels lasts more than microseconds.
+// Each try may suspend the waiting thread for up to ~20 us (it wakes as soon as
+// the phase completes), so 2^16 tries bound a wait to about a second.
+constexpr long long kDefaultWaitLimit = 1ll << 16;  // bounded-wait iterations
+constexpr long long kDrainWaitLimit = 1ll << 16;    // waits for own copies before exit
 
 // ------------------------------------------------------------ storage types
 template <typename T> struct Vec;  // 16-byte vector of T

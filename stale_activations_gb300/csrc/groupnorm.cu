@@ -35,7 +35,21 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const T* __restrict__ x,
   for (int i = 0; i < VEC; ++i) { s1[i] = 0.f; s2[i] = 0.f; }
   if (pl < PIX) {
     const T* base = x + (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C + v * VEC;
-    for (long long px = p0 + pl; px < p1; px += PIX) {
+    long long px = p0 + pl;
+    for (; px + 3 * PIX < p1; px += 4 * PIX) {  // four independent loads in flight
+      uint4 u[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        u[k] = __ldg(reinterpret_cast<const uint4*>(base + (px + k * PIX) * g.C));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float f[VEC];
+        unpack16(u[k], f);
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) { s1[i] += f[i]; s2[i] = fmaf(f[i], f[i], s2[i]); }
+      }
+    }
+    for (; px < p1; px += PIX) {
       uint4 u = __ldg(reinterpret_cast<const uint4*>(base + px * g.C));
       float f[VEC];
       unpack16(u, f);
@@ -116,11 +130,11 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
   const long long p1 = min(band_pix, p0 + g.chunk_pix);
   const long long base = (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C;
   const long long nvec = (p1 - p0) * NV;
-  for (long long i = tid; i < nvec; i += blockDim.x) {
+  const long long bd = blockDim.x;
+  auto apply_one = [&](const uint4& u, long long i) {
     const long long px = p0 + i / NV;
     const int v = (int)(i % NV);
     const long long off = base + px * g.C + v * VEC;
-    uint4 u = __ldcs(reinterpret_cast<const uint4*>(x + off));
     float f[VEC];
     unpack16(u, f);
 #pragma unroll
@@ -129,7 +143,19 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
       f[k] = fmaf(f[k] - s_mu[c], s_sc[c], s_be[c]);
     }
     *reinterpret_cast<uint4*>(y + off) = pack16(f);
+  };
+  auto src = [&](long long i) {
+    return reinterpret_cast<const uint4*>(x + base + (p0 + i / NV) * g.C + (i % NV) * VEC);
+  };
+  long long i = tid;
+  for (; i + 3 * bd < nvec; i += 4 * bd) {  // four independent loads in flight
+    uint4 u[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) u[k] = __ldcs(src(i + k * bd));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) apply_one(u[k], i + k * bd);
   }
+  for (; i < nvec; i += bd) apply_one(__ldcs(src(i)), i);
 }
 
 GnDims make_gn_dims(int B, int H, int W, int C, int P, int G) {

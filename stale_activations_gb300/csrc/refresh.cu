@@ -5,10 +5,11 @@
 // s = absmax(delta)/127 per block, int8 codes q = rint(delta/s) (ties to even,
 // clamped to +-127, 0 when s == 0), stale <- store(fmaf(q, s, stale)).
 //
-// HBM-bound streaming kernel: one block of 128 elements per 16 lanes, 8
-// elements (one or two 128-bit accesses) per lane; the block maximum is a
-// 16-lane xor-shuffle reduction.  Algorithmic traffic per element: read fresh
-// and stale, write stale and the int8 code, plus 4 bytes of scale per 128.
+// HBM-bound streaming kernel: one block of 128 elements per half warp, 8
+// elements (one or two 128-bit accesses) per lane, two blocks in flight per half
+// warp; the block maximum is a 16-lane xor-shuffle reduction.  Algorithmic
+// traffic per element: read fresh and stale, write stale and the int8 code, plus
+// 4 bytes of scale per 128.
 #include "refresh.cuh"
 
 namespace dpp {
@@ -20,23 +21,18 @@ __device__ __forceinline__ int quantise(float d, float s) {
   return max(-127, min(127, q));
 }
 
-template <typename T>
-__device__ __forceinline__ void load8(const T* p, float (&f)[8]);
-template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&f)[8]) {
-  uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
-  unpack16(u, f);
+// Same result as quantise(d, s), cheaper: with r = rn(1/s) the product t = rn(d*r)
+// is within 2e-5 of rn(d/s) (|d/s| <= 127.0001 and three roundings of relative
+// size 2^-24 each), so both round to the same integer unless t lies within 1e-4 of
+// a half-integer; only then is the IEEE quotient formed.  Needs s >= FLT_MIN so
+// that r is finite.
+__device__ __forceinline__ int quantise_fast(float d, float s, float r) {
+  const float t = d * r;
+  float rt = rintf(t);
+  if (0.5f - fabsf(t - rt) < 1e-4f) rt = rintf(__fdiv_rn(d, s));
+  return max(-127, min(127, (int)rt));
 }
-template <>
-__device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
-  uint4 a = __ldcs(reinterpret_cast<const uint4*>(p));
-  uint4 b = __ldcs(reinterpret_cast<const uint4*>(p) + 1);
-  float fa[4], fb[4];
-  unpack16(a, fa);
-  unpack16(b, fb);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) { f[i] = fa[i]; f[4 + i] = fb[i]; }
-}
+
 template <typename T>
 __device__ __forceinline__ void store8(T* p, const float (&f)[8]);
 template <>
@@ -50,73 +46,135 @@ __device__ __forceinline__ void store8<float>(float* p, const float (&f)[8]) {
   __stcs(reinterpret_cast<uint4*>(p) + 1, pack16(b));
 }
 
+// One 128-element block, done by the 16 lanes of a half warp (`hmask` names them):
+// elements strided by 16 so that any length nb <= 128 is covered.  Used for ragged
+// last blocks and misaligned segments only.
 template <typename T>
-__global__ void __launch_bounds__(256) refresh_kernel(const __grid_constant__ RefreshTable tab) {
+__device__ __noinline__ void refresh_block_scalar(const T* fr, T* st, int8_t* cd, float* scale,
+                                                  int nb, int sub, unsigned hmask) {
+  float d[8], sv[8];
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = sub + 16 * i;
+    sv[i] = e < nb ? to_f32(st[e]) : 0.0f;
+    d[i] = e < nb ? to_f32(fr[e]) - sv[i] : 0.0f;
+    a = fmaxf(a, fabsf(d[i]));
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(hmask, a, o));
+  const float s = __fdiv_rn(a, 127.0f);
+  if (sub == 0) *scale = s;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = sub + 16 * i;
+    if (e < nb) {
+      const int q = quantise(d[i], s);
+      st[e] = from_f32<T>(__fmaf_rn((float)q, s, sv[i]));
+      cd[e] = (int8_t)q;
+    }
+  }
+}
+
+// A full, aligned block: each lane holds 8 consecutive elements as raw 128-bit vectors.
+struct VecBlock {
+  uint4 fr[2], st[2];
+  void* stale;
+  int8_t* codes;
+  float* scale;
+  bool live;
+};
+
+template <typename T>
+__device__ __forceinline__ void unpack8(const uint4 (&u)[2], float (&f)[8]);
+template <>
+__device__ __forceinline__ void unpack8<__nv_bfloat16>(const uint4 (&u)[2], float (&f)[8]) {
+  unpack16(u[0], f);
+}
+template <>
+__device__ __forceinline__ void unpack8<float>(const uint4 (&u)[2], float (&f)[8]) {
+  float a[4], b[4];
+  unpack16(u[0], a);
+  unpack16(u[1], b);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) { f[i] = a[i]; f[4 + i] = b[i]; }
+}
+
+// Looks up block gb; issues the loads of a full aligned block (returned in v), or
+// refreshes a ragged/misaligned block at once.
+template <typename T>
+__device__ __forceinline__ void start_block(const RefreshTable& tab, long long gb, long long total,
+                                            int& seg, int sub, unsigned hmask, VecBlock& v) {
+  v.live = false;
+  if (gb >= total) return;
+  while (gb >= tab.blk_start[seg + 1]) ++seg;  // gb only grows: segments in order
+  const RefreshSeg& sg = tab.seg[seg];
+  const long long j = gb - tab.blk_start[seg];
+  const long long e0 = j * 128;
+  const int nb = (int)min(128ll, sg.n - e0);
+  const T* fr = reinterpret_cast<const T*>(sg.fresh) + e0;
+  T* st = reinterpret_cast<T*>(sg.stale) + e0;
+  if (nb == 128 && sg.vec_ok) {
+    constexpr int NV = 8 / Vec<T>::N;  // 16-byte vectors per lane: 1 (bf16) or 2 (fp32)
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      v.fr[k] = __ldcs(reinterpret_cast<const uint4*>(fr + sub * 8) + k);
+      v.st[k] = __ldcs(reinterpret_cast<const uint4*>(st + sub * 8) + k);
+    }
+    v.stale = st + sub * 8;
+    v.codes = sg.codes + e0 + sub * 8;
+    v.scale = sg.scales + j;
+    v.live = true;
+  } else {
+    refresh_block_scalar<T>(fr, st, sg.codes + e0, sg.scales + j, nb, sub, hmask);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void finish_block(const VecBlock& v, int sub, unsigned hmask) {
+  float f[8], sv[8], d[8];
+  unpack8<T>(v.fr, f);
+  unpack8<T>(v.st, sv);
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) { d[i] = f[i] - sv[i]; a = fmaxf(a, fabsf(d[i])); }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(hmask, a, o));
+  const float s = __fdiv_rn(a, 127.0f);
+  if (sub == 0) *v.scale = s;
+  const bool fast = s >= 1.17549435e-38f;  // FLT_MIN: 1/s is finite (s == 0 is not fast)
+  const float rc = fast ? __frcp_rn(s) : 0.0f;
+  float nv[8];
+  uint32_t c0 = 0, c1 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int q = fast ? quantise_fast(d[i], s, rc) : quantise(d[i], s);
+    nv[i] = __fmaf_rn((float)q, s, sv[i]);
+    const uint32_t b = (uint32_t)(q & 0xFF);
+    if (i < 4) c0 |= b << (8 * i); else c1 |= b << (8 * (i - 4));
+  }
+  store8<T>(static_cast<T*>(v.stale), nv);
+  __stcs(reinterpret_cast<uint2*>(v.codes), make_uint2(c0, c1));
+}
+
+// Each half warp takes two blocks per pass, issuing all four 128-bit loads before
+// finishing either block, to keep more bytes in flight per thread.
+template <typename T>
+__global__ void __launch_bounds__(256, 4) refresh_kernel(const __grid_constant__ RefreshTable tab) {
   const int lane = threadIdx.x & 31;
-  const int sub = lane & 15;                 // lane within the 16-lane block group
+  const int sub = lane & 15;
+  const unsigned hmask = 0xFFFFu << (lane & 16);
   const long long group = (long long)(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 2 +
                           (lane >> 4);
   const long long stride = (long long)gridDim.x * (blockDim.x >> 5) * 2;
   const long long total = tab.blk_start[tab.nseg];
   int seg = 0;
-  for (long long gb = group; gb < total; gb += stride) {
-    while (gb >= tab.blk_start[seg + 1]) ++seg;  // gb only grows: segments in order
-    const RefreshSeg& sg = tab.seg[seg];
-    const long long j = gb - tab.blk_start[seg];    // block within the segment
-    const long long e0 = j * 128;
-    const int nb = (int)min(128ll, sg.n - e0);
-    const T* fr = reinterpret_cast<const T*>(sg.fresh) + e0;
-    T* st = reinterpret_cast<T*>(sg.stale) + e0;
-    int8_t* cd = sg.codes + e0;
-    const bool vec = nb == 128 && sg.vec_ok;
-    float d[8], sv[8];
-    float a = 0.0f;
-    if (vec) {
-      float fv[8];
-      load8<T>(fr + sub * 8, fv);
-      load8<T>(st + sub * 8, sv);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) { d[i] = fv[i] - sv[i]; a = fmaxf(a, fabsf(d[i])); }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = sub + 16 * i;               // strided so that any nb is covered
-        if (e < nb) {
-          sv[i] = to_f32(st[e]);
-          d[i] = to_f32(fr[e]) - sv[i];
-          a = fmaxf(a, fabsf(d[i]));
-        } else {
-          sv[i] = 0.0f; d[i] = 0.0f;
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    const float s = __fdiv_rn(a, 127.0f);
-    if (sub == 0) sg.scales[j] = s;
-    if (vec) {
-      float nv[8];
-      uint32_t c0 = 0, c1 = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int q = quantise(d[i], s);
-        nv[i] = __fmaf_rn((float)q, s, sv[i]);
-        const uint32_t b = (uint32_t)(q & 0xFF);
-        if (i < 4) c0 |= b << (8 * i); else c1 |= b << (8 * (i - 4));
-      }
-      store8<T>(st + sub * 8, nv);
-      __stcs(reinterpret_cast<uint2*>(cd + sub * 8), make_uint2(c0, c1));
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = sub + 16 * i;
-        if (e < nb) {
-          const int q = quantise(d[i], s);
-          st[e] = from_f32<T>(__fmaf_rn((float)q, s, sv[i]));
-          cd[e] = (int8_t)q;
-        }
-      }
-    }
+  for (long long gb = group; gb < total; gb += 2 * stride) {
+    VecBlock v0, v1;
+    start_block<T>(tab, gb, total, seg, sub, hmask, v0);
+    start_block<T>(tab, gb + stride, total, seg, sub, hmask, v1);
+    if (v0.live) finish_block<T>(v0, sub, hmask);
+    if (v1.live) finish_block<T>(v1, sub, hmask);
   }
 }
 
@@ -124,9 +182,9 @@ int launch_refresh(const RefreshTable& tab, int dtype, cudaStream_t stream) {
   const long long total = tab.blk_start[tab.nseg];
   if (total == 0) return DPP_OK;
   const int threads = 256;
-  const long long groups_per_cta = threads / 32 * 2;
+  const long long groups_per_cta = threads / 32 * 2 * 2;  // two blocks per group and pass
   long long want = (total + groups_per_cta - 1) / groups_per_cta;
-  const long long cap = (long long)dpp_host::sm_count() * 8;  // 8 CTAs of 256 per SM
+  const long long cap = (long long)dpp_host::sm_count() * 4;  // 4 resident CTAs of 256 per SM
   const int grid = (int)(want < cap ? want : cap);
   if (dtype == DPP_BF16)
     refresh_kernel<__nv_bfloat16><<<grid, threads, 0, stream>>>(tab);

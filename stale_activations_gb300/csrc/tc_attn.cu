@@ -7,14 +7,21 @@
 // from the stale K/V.
 //
 // One CTA = two 128-row query tiles of one (batch, head, patch), 12 warps:
-//   warps 0-3 / 4-7  softmax of query tile 0 / 1 (thread = query row = TMEM lane)
-//   warp 8           TMA producer: Q tiles once, then a 3-stage ring of K and V
+//   warps 0-3 / 4-7  softmax of query tile 0 / 1 (thread = query row = TMEM lane):
+//                    read S_t from TMEM, write fp16 P_t back to TMEM.
+//   warp 8           TMA producer: Q tiles once, then a 5-stage ring of K and V
 //                    tiles; each 128-key tile is fetched in sub-boxes of g rows
 //                    (g = largest power of two <= 128 dividing L/P), each sub-box
 //                    from the fresh or the stale tensor map -- the splice.
-//   warp 9           MMA issuer: S = Q K^T (M=128, N=128, K=16 steps over d=64)
-//                    into TMEM, O += P V (M=128, N=64, K=16 steps over keys).
-//   warps 10-11      convert each landed V tile from bf16 to fp16 in place.
+//   warp 9           MMA issuer (one thread) and TMEM owner.  Per key tile j and
+//                    query tile t, once softmax t has written P_t(j):
+//                    O_t += P_t(j) V(j) (M=128, N=64, K=16 steps over keys, P from
+//                    TMEM), then S_t = Q_t K(j+1)^T (M=128, N=128, K=16 steps over
+//                    d=64).  The two query tiles alternate, so the tensor pipe works
+//                    on one tile while the other's softmax runs; and because the
+//                    tensor pipe completes one thread's MMAs in order, "S_t(j+1)
+//                    ready" also means P_t(j) and O_t are free again.
+//   warps 10-11      widen each landed V tile from bf16 to fp16 in place.
 // P is rounded to fp16, not bf16: its 11-bit significand keeps the rounding of
 // the probabilities well inside the 2e-3 output tolerance (bf16's 8 bits would
 // not), and V is widened to fp16 exactly so that P V runs as kind::f16 with
@@ -35,17 +42,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn();  // tc_gemm.cu
 
 namespace {
 
-constexpr int D = 64;                 // head dim
-constexpr int QT = 128;               // query rows per tile
-constexpr int KT = 128;               // keys per tile
-constexpr int KV_STAGES = 3;
+constexpr int D = 64;                   // head dim
+constexpr int QT = 128;                 // query rows per tile
+constexpr int KT = 128;                 // keys per tile
+constexpr int KV_STAGES = 5;
 constexpr int TILE_BYTES = KT * D * 2;  // 16 KB (K or V tile, Q tile)
-constexpr int P_BYTES = QT * KT * 2;    // 32 KB (fp16 probabilities of one query tile)
 constexpr int ATTN_THREADS = 384;
-// smem: Q0 Q1 | P0 P1 | (K V) x stages | barriers
+constexpr int NUM_CONVERTERS = 2;       // warps 10-11
+// smem: Q0 Q1 | (K V) x stages | barriers.  TMEM (512 columns): S0 S1 (128 each),
+// O0 O1 (64 each), P0 P1 (64 each: 128 fp16 probabilities per row, two per column).
 constexpr int OFF_Q = 0;
-constexpr int OFF_P = 2 * TILE_BYTES;
-constexpr int OFF_KV = OFF_P + 2 * P_BYTES;
+constexpr int OFF_KV = 2 * TILE_BYTES;
 constexpr int OFF_BAR = OFF_KV + KV_STAGES * 2 * TILE_BYTES;
 constexpr int ATTN_SMEM = OFF_BAR + 512 + 1024;
 constexpr float kScaleLog2 = 0.18033688011112042f;  // log2(e) / sqrt(64)
@@ -61,8 +68,7 @@ struct AttnArgs {
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[KV_STAGES], v_full[KV_STAGES], v_conv[KV_STAGES], kv_empty[KV_STAGES];
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-  uint64_t drain;
+  uint64_t s_full[2], p_full[2], o_done[2], drain;
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -100,14 +106,13 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     for (int s = 0; s < KV_STAGES; ++s) {
       ptx::mbar_init(&bars->k_full[s], 1);
       ptx::mbar_init(&bars->v_full[s], 1);
-      ptx::mbar_init(&bars->v_conv[s], 2);
+      ptx::mbar_init(&bars->v_conv[s], NUM_CONVERTERS);
       ptx::mbar_init(&bars->kv_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(&bars->s_full[t], 1);
-      ptx::mbar_init(&bars->s_free[t], 4);
-      ptx::mbar_init(&bars->p_full[t], 4);
-      ptx::mbar_init(&bars->pv_done[t], 1);
+      ptx::mbar_init(&bars->p_full[t], 4);  // one arrival per softmax warp
+      ptx::mbar_init(&bars->o_done[t], 1);  // committed once, after the last P V
     }
     ptx::mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -128,169 +133,165 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
-  const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO[2] = {tmem + 256, tmem + 320};
   const int nkt = a.nkt;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int issued = 0;
-      bool ok = true;
-      ptx::mbar_arrive_expect_tx(&bars->q_full, 2 * TILE_BYTES);
-      for (int t = 0; t < 2; ++t)
-        ptx::tma_load_3d(smem + OFF_Q + t * TILE_BYTES, &tmQ, &bars->q_full, h * D,
-                         patch0 + (2 * pair + t) * QT, b);
-      const int nsub = KT / a.g;
-      for (int j = 0; j < nkt && ok; ++j) {
-        const int st = j % KV_STAGES;
-        if (!wait_or_abort(&bars->kv_empty[st], ((j / KV_STAGES) & 1) ^ 1, a, bars)) {
-          ok = false;
-          break;
-        }
-        uint8_t* kdst = smem + OFF_KV + st * 2 * TILE_BYTES;
-        uint8_t* vdst = kdst + TILE_BYTES;
-        ptx::mbar_arrive_expect_tx(&bars->k_full[st], TILE_BYTES);
-        ptx::mbar_arrive_expect_tx(&bars->v_full[st], TILE_BYTES);
-        for (int i = 0; i < nsub; ++i) {
-          const int row = j * KT + i * a.g;
-          const bool fresh = row >= patch0 && row < patch0 + a.Lp;
-          ptx::tma_load_3d(kdst + i * a.g * 128, fresh ? &tmKf : &tmKs, &bars->k_full[st], h * D,
-                           row, b);
-        }
-        for (int i = 0; i < nsub; ++i) {
-          const int row = j * KT + i * a.g;
-          const bool fresh = row >= patch0 && row < patch0 + a.Lp;
-          ptx::tma_load_3d(vdst + i * a.g * 128, fresh ? &tmVf : &tmVs, &bars->v_full[st], h * D,
-                           row, b);
-        }
-        ++issued;
-      }
-      if (bars->abort_flag) {  // wait for own copies in flight before exiting
-        ptx::mbar_wait(&bars->q_full, 0, kDrainWaitLimit, nullptr);
-        const int first = issued > KV_STAGES ? issued - KV_STAGES : 0;
-        for (int j = first; j < issued; ++j) {
-          ptx::mbar_wait(&bars->k_full[j % KV_STAGES], (j / KV_STAGES) & 1, kDrainWaitLimit,
-                         nullptr);
-          ptx::mbar_wait(&bars->v_full[j % KV_STAGES], (j / KV_STAGES) & 1, kDrainWaitLimit,
-                         nullptr);
-        }
-      }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = ptx::idesc_f16(QT, KT, 1, 0, 0);
-      constexpr uint32_t idesc_pv = ptx::idesc_f16(QT, D, 0, 0, 1);
-      const uint32_t q_addr = ptx::smem_u32(smem + OFF_Q);
-      const uint32_t p_addr = ptx::smem_u32(smem + OFF_P);
-      const uint32_t kv_addr = ptx::smem_u32(smem + OFF_KV);
-      bool any = false;
-      auto issue_qk = [&](int t, int j) {
-        const uint32_t k_addr = kv_addr + (j % KV_STAGES) * 2 * TILE_BYTES;
-        const uint32_t qa = q_addr + t * TILE_BYTES;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          ptx::mma_ss(tS[t], ptx::sw128_desc(qa + k * 32, 16, 1024),
-                      ptx::sw128_desc(k_addr + k * 32, 16, 1024), idesc_qk, k ? 1u : 0u);
-        ptx::mma_commit(&bars->s_full[t]);
-        any = true;
-      };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t v_addr = kv_addr + (j % KV_STAGES) * 2 * TILE_BYTES + TILE_BYTES;
-        const uint32_t pa = p_addr + t * P_BYTES;
-#pragma unroll
-        for (int k = 0; k < KT / 16; ++k)
-          ptx::mma_ss(tO[t], ptx::sw128_desc(pa + (k >> 2) * (QT * 128) + (k & 3) * 32, 16, 1024),
-                      ptx::sw128_desc(v_addr + k * 2048, TILE_BYTES, 1024), idesc_pv,
-                      (j | k) ? 1u : 0u);
-        ptx::mma_commit(&bars->pv_done[t]);
-        any = true;
-      };
-      bool ok = wait_or_abort(&bars->q_full, 0, a, bars) &&
-                wait_or_abort(&bars->k_full[0], 0, a, bars);
-      if (ok) {
-        ptx::tc_fence_after();
-        issue_qk(0, 0);
-        issue_qk(1, 0);
-      }
-      // Per key tile j and query tile t: S_t(j+1) = Q_t K(j+1)^T is issued as soon as
-      // softmax t has read S_t(j), before O_t += P_t(j) V(j), so the tensor pipe
-      // computes the next scores while the softmax warps exponentiate.
-      for (int j = 0; j < nkt && ok; ++j) {
-        const int st = j % KV_STAGES;
-        const uint32_t ph = j & 1;
-        const bool more = j + 1 < nkt;
-        if (more && !wait_or_abort(&bars->k_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1,
-                                   a, bars)) {
-          ok = false;
-          break;
-        }
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (more) {
-            if (!wait_or_abort(&bars->s_free[t], ph, a, bars)) { ok = false; break; }
-            ptx::tc_fence_after();
-            issue_qk(t, j + 1);
+  if (warp >= 8) {
+    // Register split (launch: 384 threads x 168): this warpgroup drops to 56 per
+    // thread, the two softmax warpgroups rise to 216: 128 x 56 + 256 x 216 <= 64512.
+    ptx::regs_dec<56>();
+    if (warp == 8) {
+      // ---------------------------------------------------------- TMA producer
+      if (lane == 0) {
+        int issued = 0;
+        ptx::mbar_arrive_expect_tx(&bars->q_full, 2 * TILE_BYTES);
+        for (int t = 0; t < 2; ++t)
+          ptx::tma_load_3d(smem + OFF_Q + t * TILE_BYTES, &tmQ, &bars->q_full, h * D,
+                           patch0 + (2 * pair + t) * QT, b);
+        const int nsub = KT / a.g;
+        for (int j = 0; j < nkt; ++j) {
+          const int st = j % KV_STAGES;
+          if (!wait_or_abort(&bars->kv_empty[st], ((j / KV_STAGES) & 1) ^ 1, a, bars)) break;
+          uint8_t* kdst = smem + OFF_KV + st * 2 * TILE_BYTES;
+          uint8_t* vdst = kdst + TILE_BYTES;
+          ptx::mbar_arrive_expect_tx(&bars->k_full[st], TILE_BYTES);
+          ptx::mbar_arrive_expect_tx(&bars->v_full[st], TILE_BYTES);
+          for (int i = 0; i < nsub; ++i) {
+            const int row = j * KT + i * a.g;
+            const bool fresh = row >= patch0 && row < patch0 + a.Lp;
+            ptx::tma_load_3d(kdst + i * a.g * 128, fresh ? &tmKf : &tmKs, &bars->k_full[st],
+                             h * D, row, b);
           }
-          if (!wait_or_abort(&bars->p_full[t], ph, a, bars) ||
-              (t == 0 && !wait_or_abort(&bars->v_conv[st], (j / KV_STAGES) & 1, a, bars))) {
-            ok = false;
-            break;
+          for (int i = 0; i < nsub; ++i) {
+            const int row = j * KT + i * a.g;
+            const bool fresh = row >= patch0 && row < patch0 + a.Lp;
+            ptx::tma_load_3d(vdst + i * a.g * 128, fresh ? &tmVf : &tmVs, &bars->v_full[st],
+                             h * D, row, b);
           }
+          ++issued;
+        }
+        if (bars->abort_flag) {  // wait for own copies in flight before exiting
+          ptx::mbar_wait(&bars->q_full, 0, kDrainWaitLimit, nullptr);
+          const int first = issued > KV_STAGES ? issued - KV_STAGES : 0;
+          for (int j = first; j < issued; ++j) {
+            ptx::mbar_wait(&bars->k_full[j % KV_STAGES], (j / KV_STAGES) & 1, kDrainWaitLimit,
+                           nullptr);
+            ptx::mbar_wait(&bars->v_full[j % KV_STAGES], (j / KV_STAGES) & 1, kDrainWaitLimit,
+                           nullptr);
+          }
+        }
+      }
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = ptx::idesc_f16(QT, KT, 1, 0, 0);
+        constexpr uint32_t idesc_pv = ptx::idesc_f16(QT, D, 0, 0, 1);
+        const uint32_t q_addr = ptx::smem_u32(smem + OFF_Q);
+        const uint32_t kv_addr = ptx::smem_u32(smem + OFF_KV);
+        bool any = false;
+        bool ok = wait_or_abort(&bars->q_full, 0, a, bars) &&
+                  wait_or_abort(&bars->k_full[0], 0, a, bars);
+        if (ok) {
           ptx::tc_fence_after();
-          issue_pv(t, j);
-        }
-        if (ok) ptx::mma_commit(&bars->kv_empty[st]);
-      }
-      if (!ok && any) {  // let issued MMAs finish before TMEM is released
-        ptx::mma_commit(&bars->drain);
-        ptx::mbar_wait(&bars->drain, 0, kDrainWaitLimit, nullptr);
-      }
-    }
-  } else if (warp >= 10) {
-    // ------------------------------------------------------------ V: bf16 -> fp16 in place
-    const int ct = threadIdx.x - 320;  // 0..63
-    for (int j = 0; j < nkt; ++j) {
-      const int st = j % KV_STAGES;
-      if (!wait_or_abort(&bars->v_full[st], (j / KV_STAGES) & 1, a, bars)) break;
-      uint4* v = reinterpret_cast<uint4*>(smem + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES);
-#pragma unroll 4
-      for (int i = ct; i < TILE_BYTES / 16; i += 64) {
-        uint4 u = v[i];
-        uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
-          __half2 hv = __floats2half2_rn(lo, hi);
-          w[e] = *reinterpret_cast<uint32_t*>(&hv);
+          for (int t = 0; t < 2; ++t) {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+              ptx::mma_ss(tmem + 128u * t, ptx::sw128_desc(q_addr + t * TILE_BYTES + k * 32, 16, 1024),
+                          ptx::sw128_desc(kv_addr + k * 32, 16, 1024), idesc_qk, k ? 1u : 0u);
+            ptx::mma_commit(&bars->s_full[t]);
+          }
+          any = true;
         }
-        v[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int j = 0; j < nkt && ok; ++j) {
+          const int st = j % KV_STAGES;
+          const bool more = j + 1 < nkt;
+          const uint32_t v_addr = kv_addr + (uint32_t)(st * 2 * TILE_BYTES + TILE_BYTES);
+          const uint32_t k_next = kv_addr + (uint32_t)(((j + 1) % KV_STAGES) * 2 * TILE_BYTES);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!wait_or_abort(&bars->p_full[t], j & 1, a, bars) ||
+                (t == 0 && !wait_or_abort(&bars->v_conv[st], (j / KV_STAGES) & 1, a, bars)) ||
+                (t == 0 && more &&
+                 !wait_or_abort(&bars->k_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1, a,
+                                bars))) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t tO = tmem + 256u + 64u * t, tP = tmem + 384u + 64u * t;
+#pragma unroll
+            for (int k = 0; k < KT / 16; ++k)  // O_t += P_t(j) V(j)
+              ptx::mma_ts(tO, tP + k * 8, ptx::sw128_desc(v_addr + k * 2048, TILE_BYTES, 1024),
+                          idesc_pv, (j | k) ? 1u : 0u);
+            if (more) {                         // S_t = Q_t K(j+1)^T
+#pragma unroll
+              for (int k = 0; k < D / 16; ++k)
+                ptx::mma_ss(tmem + 128u * t,
+                            ptx::sw128_desc(q_addr + t * TILE_BYTES + k * 32, 16, 1024),
+                            ptx::sw128_desc(k_next + k * 32, 16, 1024), idesc_qk, k ? 1u : 0u);
+              ptx::mma_commit(&bars->s_full[t]);
+            } else {
+              ptx::mma_commit(&bars->o_done[t]);
+            }
+          }
+          if (ok) ptx::mma_commit(&bars->kv_empty[st]);
+        }
+        if (!ok && any) {  // let issued MMAs finish before TMEM is released
+          ptx::mma_commit(&bars->drain);
+          ptx::mbar_wait(&bars->drain, 0, kDrainWaitLimit, nullptr);
+        }
       }
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars->v_conv[st]);
+    } else {
+      // ---------------------------------------------------------- V: bf16 -> fp16 in place
+      const int ct = threadIdx.x - 10 * 32;  // 0..63
+      for (int j = 0; j < nkt; ++j) {
+        const int st = j % KV_STAGES;
+        // lane 0 sleeps on the barrier; then every lane observes the completed phase
+        // (returns at once) so that all lanes see the landed tile
+        int ok = 1;
+        if (lane == 0) ok = wait_or_abort(&bars->v_full[st], (j / KV_STAGES) & 1, a, bars);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (!wait_or_abort(&bars->v_full[st], (j / KV_STAGES) & 1, a, bars)) break;
+        uint4* v = reinterpret_cast<uint4*>(smem + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES);
+#pragma unroll 4
+        for (int i = ct; i < TILE_BYTES / 16; i += 32 * NUM_CONVERTERS) {
+          uint4 u = v[i];
+          uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+            __half2 hv = __floats2half2_rn(lo, hi);
+            w[e] = *reinterpret_cast<uint32_t*>(&hv);
+          }
+          v[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->v_conv[st]);
+      }
     }
   } else {
+    ptx::regs_inc<216>();
     // ------------------------------------------------------------ softmax (warps 0-7)
     const int t = warp >> 2;             // query tile of this warpgroup
     const int quarter = warp & 3;        // TMEM lanes [32*quarter, +32)
     const int r = quarter * 32 + lane;   // row within the query tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    uint8_t* pbuf = smem + OFF_P + t * P_BYTES;
+    const uint32_t tS = tmem + 128u * (uint32_t)t;        // S_t: 128 columns
+    const uint32_t tO = tmem + 256u + 64u * (uint32_t)t;  // O_t: 64 columns
+    const uint32_t tP = tmem + 384u + 64u * (uint32_t)t;  // P_t: 64 columns
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkt; ++j) {
-      const uint32_t ph = j & 1;
-      if (!wait_or_abort(&bars->s_full[t], ph, a, bars)) { ok = false; break; }
+      // S_t(j) ready; the MMA thread issued it after P_t(j-1) V(j-1), so that
+      // product has completed too: P_t and O_t may be touched.
+      if (!wait_or_abort(&bars->s_full[t], j & 1, a, bars)) { ok = false; break; }
       ptx::tc_fence_after();
       uint32_t s[128];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        ptx::tmem_ld32(tS[t] + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+        ptx::tmem_ld32(tS + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
       ptx::tmem_ld_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars->s_free[t]);
       const int nvalid = a.L - j * KT;
       if (nvalid < KT) {  // only the last key tile can be partial: mask keys >= L
 #pragma unroll
@@ -299,11 +300,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       }
       float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 independent chains
 #pragma unroll
-      for (int i = 0; i < 128; i += 4) {
+      for (int i = 0; i < 128; i += 8) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) mq[u] = fmaxf(mq[u], __uint_as_float(s[i + u]));
+        for (int u = 0; u < 4; ++u)
+          mq[u] = ptx::max3(mq[u], __uint_as_float(s[i + 2 * u]), __uint_as_float(s[i + 2 * u + 1]));
       }
-      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      const float mx = ptx::max3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
       const float m_new = mx * kScaleLog2;
       const bool resc = m_new > m_ref + kRescaleThreshold;
       float alpha = 1.f;
@@ -312,48 +314,41 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         m_ref = m_new;
         l *= alpha;
       }
-      uint32_t pk[64];
-      float lq[4] = {0.f, 0.f, 0.f, 0.f};  // 4 independent partial row sums
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {  // rescale the running O_t
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[16];
+          ptx::tmem_ld16(tO + lane_off + c * 16, o);
+          ptx::tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float p0 = ex2(fmaf(__uint_as_float(s[2 * i]), kScaleLog2, -m_ref));
-        const float p1 = ex2(fmaf(__uint_as_float(s[2 * i + 1]), kScaleLog2, -m_ref));
-        lq[(2 * i) & 3] += p0;
-        lq[(2 * i + 1) & 3] += p1;
-        __half2 hv = __floats2half2_rn(p0, p1);
-        pk[i] = *reinterpret_cast<uint32_t*>(&hv);
-      }
-      l += (lq[0] + lq[1]) + (lq[2] + lq[3]);
-      if (j > 0) {
-        // P buffer free and O quiescent once the previous P V has completed
-        if (!wait_or_abort(&bars->pv_done[t], ph ^ 1, a, bars)) { ok = false; break; }
-        ptx::tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
-          uint32_t o[32];
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            ptx::tmem_ld32(tO[t] + lane_off + c * 32, o);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            ptx::tmem_st32(tO[t] + lane_off + c * 32, o);
-          }
-          ptx::tmem_st_wait();
+          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          ptx::tmem_st16(tO + lane_off + c * 16, o);
         }
       }
-      // fp16 P row r, K-major 128-byte swizzled: keys [0,64) then [64,128)
+      // exponentials 32 keys at a time, stored at once as fp16 P into TMEM (column c
+      // holds keys 2c in the low half and 2c+1 in the high half)
+      float lq[4] = {0.f, 0.f, 0.f, 0.f};  // 4 independent partial row sums
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        uint8_t* dst = pbuf + (c >> 3) * (QT * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(fmaf(__uint_as_float(s[32 * c + 2 * i]), kScaleLog2, -m_ref));
+          const float p1 = ex2(fmaf(__uint_as_float(s[32 * c + 2 * i + 1]), kScaleLog2, -m_ref));
+          lq[(2 * i) & 3] += p0;
+          lq[(2 * i + 1) & 3] += p1;
+          __half2 hv = __floats2half2_rn(p0, p1);
+          pk[i] = *reinterpret_cast<uint32_t*>(&hv);
+        }
+        ptx::tmem_st16(tP + lane_off + 16 * c, pk);
       }
-      ptx::fence_proxy_async_smem();
+      l += (lq[0] + lq[1]) + (lq[2] + lq[3]);
+      ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bars->p_full[t]);
     }
-    if (ok && wait_or_abort(&bars->pv_done[t], (nkt - 1) & 1, a, bars)) {
+    if (ok && wait_or_abort(&bars->o_done[t], 0, a, bars)) {
       ptx::tc_fence_after();
       const int row_in_patch = (2 * pair + t) * QT + r;
       const bool valid = row_in_patch < a.Lp;
@@ -361,14 +356,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       __nv_bfloat16* dst =
           a.o + ((long long)b * a.L + patch0 + row_in_patch) * (long long)(a.heads * D) + h * D;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o[32];
-        ptx::tmem_ld32(tO[t] + lane_off + c * 32, o);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[16];
+        ptx::tmem_ld16(tO + lane_off + c * 16, o);
         ptx::tmem_ld_wait();
         if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 16);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < 2; ++i) {
             d4[i] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * i]) * inv,
                                            __uint_as_float(o[8 * i + 1]) * inv),
                                pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv,

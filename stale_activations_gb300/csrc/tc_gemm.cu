@@ -1,11 +1,13 @@
 // tcgen05 GEMM engine for the bf16 path: the Q/K/V and output projections, and
 // the halo conv3x3 as an implicit GEMM (M = B*H*W pixels, N = Cout, K = 9*Cin).
 //
-// One 128 x 128 fp32 accumulator tile per CTA lives in tensor memory.  Warp 0
-// streams 64-wide K slices of A and B into a 6-stage shared-memory ring with
-// TMA (128-byte swizzle); warp 1 issues tcgen05.mma (M=128, N=128, K=16) and
-// releases each stage with tcgen05.commit; warps 2-5 read the accumulator back
-// with tcgen05.ld and store bf16.
+// Persistent: one CTA per SM walks output tiles of 128 x BN (BN = 256, 160 or
+// 128, the largest that divides N).  Warp 0 streams 64-wide K slices of A and B
+// into a shared-memory ring with TMA (128-byte swizzle); warp 1 issues
+// tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM accumulators and releases
+// each stage with tcgen05.commit; warps 2-5 drain the other accumulator
+// (tcgen05.ld -> bf16 -> global), so a tile's epilogue overlaps the next tile's
+// main loop.
 //
 // Halo conv staging ("Benchmarking DistVAE", Glossary: the halo rows a sharded
 // convolution needs; "OTIL for SDXL on 4x L40S", item 3: the conv halo buffers
@@ -25,14 +27,23 @@ namespace dpp {
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 6;
-constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BM = 128, BK = 64;
 constexpr int GEMM_THREADS = 192;
-constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
+};
 
 struct GemmArgs {
   long long M;
   int N, K, nkb;
+  int m_tiles, n_tiles;
   void* out[3];
   int ncols;
   int* status;
@@ -41,29 +52,36 @@ struct GemmArgs {
   int H, W, Cin, Hp, cin_blocks, boxes, box_px;
 };
 
-template <bool CONV>
+template <bool CONV, int BN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+  using C = Cfg<BN>;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* done = empty + STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* acc_full = empty + STAGES;   // [2] MMA -> epilogue
+  uint64_t* acc_empty = acc_full + 2;    // [2] epilogue -> MMA (4 warps)
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long m0 = (long long)blockIdx.x * BM;
-  const int n0 = blockIdx.y * BN;
+  const int ntiles = args.m_tiles * args.n_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
-    ptx::mbar_init(done, 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&acc_full[b], 1);
+      ptx::mbar_init(&acc_empty[b], 4);
+    }
+    ptx::mbar_init(drain, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -73,7 +91,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     ptx::tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(tmem_slot, BN);
+    ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -84,97 +102,126 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = 0;
-      int b = 0, r = 0, c0 = 0;
-      if (CONV) {
-        const long long hw = (long long)args.H * args.W;
-        b = (int)(m0 / hw);
-        const int rem = (int)(m0 - (long long)b * hw);
-        r = rem / args.W;
-        c0 = rem - r * args.W;
-      }
-      for (int kb = 0; kb < args.nkb; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
-        if (!ptx::mbar_wait(&empty[s], ph ^ 1, args.wait_limit, abort_flag)) {
-          set_status(args.status, DPP_ERR_TIMEOUT);
-          *abort_flag = 1;
-          break;
-        }
-        uint8_t* a_dst = smem + s * STAGE_BYTES;
-        uint8_t* b_dst = a_dst + A_BYTES;
-        ptx::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+      long long g = 0;  // global K-slice counter across tiles
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int mt = tile / args.n_tiles, nt = tile - mt * args.n_tiles;
+        const long long m0 = (long long)mt * BM;
+        const int n0 = nt * BN;
+        int b = 0, r = 0, c0 = 0;
         if (CONV) {
-          const int tap = kb / args.cin_blocks;
-          const int cb = kb - tap * args.cin_blocks;
-          const int di = tap / 3 - 1, dj = tap % 3 - 1;
-          for (int bx = 0; bx < args.boxes; ++bx) {
-            const int rk = r + bx;          // image row of this box's pixels
-            const int rr = rk + di;         // source row
-            const bool stale = rr >= 0 && rr < args.H && (rr / args.Hp) != (rk / args.Hp);
-            ptx::tma_load_4d(a_dst + bx * args.box_px * 128, stale ? &tmA2 : &tmA, &full[s],
-                             cb * BK, c0 + dj, rr, b);
+          const long long hw = (long long)args.H * args.W;
+          b = (int)(m0 / hw);
+          const int rem = (int)(m0 - (long long)b * hw);
+          r = rem / args.W;
+          c0 = rem - r * args.W;
+        }
+        // K slices in a rotated order that depends only on the tile, so that CTAs
+        // working on the same B tile at the same time fetch different slices (no
+        // hot spot on one L2 slice) while a given tile always sums in one order.
+        const int rot = (int)(mt % args.nkb);
+        for (int kq = 0; kq < args.nkb; ++kq, ++g) {
+          const int kb = kq + rot < args.nkb ? kq + rot : kq + rot - args.nkb;
+          const int s = (int)(g % STAGES);
+          const uint32_t ph = (uint32_t)((g / STAGES) & 1);
+          if (!ptx::mbar_wait(&empty[s], ph ^ 1, args.wait_limit, abort_flag)) {
+            set_status(args.status, DPP_ERR_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          uint8_t* a_dst = smem + s * C::STAGE_BYTES;
+          uint8_t* b_dst = a_dst + C::A_BYTES;
+          ptx::mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          if (CONV) {
+            const int tap = kb / args.cin_blocks;
+            const int cb = kb - tap * args.cin_blocks;
+            const int di = tap / 3 - 1, dj = tap % 3 - 1;
+            for (int bx = 0; bx < args.boxes; ++bx) {
+              const int rk = r + bx;   // image row of this box's pixels
+              const int rr = rk + di;  // source row
+              const bool stale = rr >= 0 && rr < args.H && (rr / args.Hp) != (rk / args.Hp);
+              ptx::tma_load_4d(a_dst + bx * args.box_px * 128, stale ? &tmA2 : &tmA, &full[s],
+                               cb * BK, c0 + dj, rr, b);
+            }
+          } else {
+            ptx::tma_load_2d(a_dst, &tmA, &full[s], kb * BK, (int)m0);
           }
           ptx::tma_load_2d(b_dst, &tmB, &full[s], kb * BK, n0);
-        } else {
-          ptx::tma_load_2d(a_dst, &tmA, &full[s], kb * BK, (int)m0);
-          ptx::tma_load_2d(b_dst, &tmB, &full[s], kb * BK, n0);
         }
-        ++issued;
       }
-      // wait for own copies still in flight before the CTA may exit
-      if (*abort_flag) {
-        const int first = issued > STAGES ? issued - STAGES : 0;
-        for (int kb = first; kb < issued; ++kb)
-          ptx::mbar_wait(&full[kb % STAGES], (kb / STAGES) & 1, kDrainWaitLimit, nullptr);
+      if (*abort_flag) {  // wait for own copies still in flight before the CTA may exit
+        const long long first = g > STAGES ? g - STAGES : 0;
+        for (long long q = first; q < g; ++q)
+          ptx::mbar_wait(&full[q % STAGES], (uint32_t)((q / STAGES) & 1), kDrainWaitLimit,
+                         nullptr);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = ptx::idesc_f16(BM, BN, 1, 0, 0);
-      bool any = false;
-      for (int kb = 0; kb < args.nkb; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
-        if (!ptx::mbar_wait(&full[s], ph, args.wait_limit, abort_flag)) {
+      bool any = false, ok = true;
+      long long g = 0;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
+        const int ab = it & 1;
+        if (!ptx::mbar_wait(&acc_empty[ab], ((it >> 1) & 1) ^ 1, args.wait_limit, abort_flag)) {
           set_status(args.status, DPP_ERR_TIMEOUT);
           *abort_flag = 1;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t a_addr = ptx::smem_u32(smem + s * STAGE_BYTES);
-        const uint32_t b_addr = a_addr + A_BYTES;
+        const uint32_t d_tmem = tmem + ab * BN;
+        for (int kb = 0; kb < args.nkb; ++kb, ++g) {
+          const int s = (int)(g % STAGES);
+          const uint32_t ph = (uint32_t)((g / STAGES) & 1);
+          if (!ptx::mbar_wait(&full[s], ph, args.wait_limit, abort_flag)) {
+            set_status(args.status, DPP_ERR_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + C::A_BYTES;
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          const uint64_t ad = ptx::sw128_desc(a_addr + k * 32, 16, 1024);
-          const uint64_t bd = ptx::sw128_desc(b_addr + k * 32, 16, 1024);
-          ptx::mma_ss(tmem, ad, bd, idesc, (kb | k) ? 1u : 0u);
+          for (int k = 0; k < BK / 16; ++k)
+            ptx::mma_ss(d_tmem, ptx::sw128_desc(a_addr + k * 32, 16, 1024),
+                        ptx::sw128_desc(b_addr + k * 32, 16, 1024), idesc, (kb | k) ? 1u : 0u);
+          any = true;
+          ptx::mma_commit(&empty[s]);
         }
-        any = true;
-        ptx::mma_commit(&empty[s]);
+        if (ok) ptx::mma_commit(&acc_full[ab]);
       }
-      if (any) ptx::mma_commit(done);
-      if (*abort_flag && any) ptx::mbar_wait(done, 0, kDrainWaitLimit, nullptr);
+      if (*abort_flag && any) {  // let issued MMAs finish before TMEM is released
+        ptx::mma_commit(drain);
+        ptx::mbar_wait(drain, 0, kDrainWaitLimit, nullptr);
+      }
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
-    const bool ok = ptx::mbar_wait(done, 0, args.wait_limit, abort_flag);
-    if (!ok) {
-      set_status(args.status, DPP_ERR_TIMEOUT);
-      *abort_flag = 1;
-    } else {
+    int it = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+      const int ab = it & 1;
+      if (!ptx::mbar_wait(&acc_full[ab], (it >> 1) & 1, args.wait_limit, abort_flag)) {
+        set_status(args.status, DPP_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
       ptx::tc_fence_after();
-      const long long row = m0 + quarter * 32 + lane;
+      const int mt = tile / args.n_tiles, nt = tile - mt * args.n_tiles;
+      const long long row = (long long)mt * BM + quarter * 32 + lane;
+      const int n0 = nt * BN;
       const int which = n0 / args.ncols;
       const int col0 = n0 - which * args.ncols;
-      __nv_bfloat16* dst =
-          static_cast<__nv_bfloat16*>(args.out[which]) + row * args.ncols + col0;
-#pragma unroll
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.out[which]) + row * args.ncols + col0;
+      const uint32_t t_base = tmem + ab * BN + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t v[32];
-        ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + ch * 32, v);
+        ptx::tmem_ld32(t_base + ch * 32, v);
         ptx::tmem_ld_wait();
         uint4 pk[4];
 #pragma unroll
@@ -190,13 +237,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           for (int i = 0; i < 4; ++i) d4[i] = pk[i];
         }
       }
+      // accumulator drained: the MMA warp may reuse it
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);
     }
   }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, BN);
+    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -231,27 +282,56 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
   return r == CUDA_SUCCESS;
 }
 
-int set_smem_attr() {
+template <bool CONV, int BN>
+int prepare() {
   static std::once_flag once;
   static int rc = DPP_OK;
   std::call_once(once, [] {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             GEMM_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             GEMM_SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(tc_gemm_kernel<CONV, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<BN>::SMEM) != cudaSuccess)
       rc = DPP_ERR_CUDA;
   });
   return rc;
 }
 
+int pick_bn(int N, int ncols) {
+  // the tile must not straddle two of the split outputs
+  for (int bn : {256, 160, 128})
+    if (N % bn == 0 && ncols % bn == 0) return bn;
+  return 0;
+}
+
+template <bool CONV, int BN>
+int launch(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, GemmArgs g,
+           cudaStream_t s) {
+  int rc = prepare<CONV, BN>();
+  if (rc) return rc;
+  g.n_tiles = g.N / BN;
+  const long long ntiles = (long long)g.m_tiles * g.n_tiles;
+  const int grid = (int)(ntiles < dpp_host::sm_count() ? ntiles : dpp_host::sm_count());
+  tc_gemm_kernel<CONV, BN><<<grid, GEMM_THREADS, Cfg<BN>::SMEM, s>>>(ta, ta2, tb, g);
+  return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+}
+
+template <bool CONV>
+int dispatch(int bn, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
+             const GemmArgs& g, cudaStream_t s) {
+  switch (bn) {
+    case 256: return launch<CONV, 256>(ta, ta2, tb, g, s);
+    case 160: return launch<CONV, 160>(ta, ta2, tb, g, s);
+    case 128: return launch<CONV, 128>(ta, ta2, tb, g, s);
+    default: return DPP_ERR_SHAPE;
+  }
+}
+
 }  // namespace
 
 bool tc_linear_supported(long long M, int C) {
-  return M % BM == 0 && C % BN == 0 && C % BK == 0 && M < (1ll << 31);
+  return M % BM == 0 && C % 128 == 0 && C % BK == 0 && M < (1ll << 31);
 }
 
 bool tc_conv_supported(int B, int H, int W, int Cin, int Cout, int P) {
-  if (Cin % BK || Cout % BN) return false;
+  if (Cin % BK || Cout % 128) return false;
   if (!(W % 128 == 0 || (128 % W == 0 && W >= 8))) return false;
   if (((long long)(H / P) * W) % BM) return false;
   (void)B;
@@ -260,32 +340,31 @@ bool tc_conv_supported(int B, int H, int W, int Cin, int Cout, int P) {
 
 int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2, long long M,
                      int N, int K, int* status, long long wait_limit, cudaStream_t s) {
-  if (M % BM || N % BN || K % BK) return DPP_ERR_SHAPE;
-  int rc = set_smem_attr();
-  if (rc) return rc;
+  if (M % BM || N % 128 || K % BK) return DPP_ERR_SHAPE;
+  const int ncols = o1 ? N / 3 : N;
+  const int bn = pick_bn(N, ncols);
+  if (!bn) return DPP_ERR_SHAPE;
   CUtensorMap ta, tb;
   const uint64_t da[2] = {(uint64_t)K, (uint64_t)M}, sa[1] = {(uint64_t)K * 2};
   const uint32_t ba[2] = {BK, BM};
   const uint64_t db[2] = {(uint64_t)K, (uint64_t)N}, sb[1] = {(uint64_t)K * 2};
-  const uint32_t bb[2] = {BK, BN};
+  const uint32_t bb[2] = {BK, (uint32_t)bn};
   if (!make_map(&ta, a, 2, da, sa, ba) || !make_map(&tb, w, 2, db, sb, bb)) return DPP_ERR_CUDA;
   GemmArgs g{};
   g.M = M; g.N = N; g.K = K; g.nkb = K / BK;
+  g.m_tiles = (int)(M / BM);
   g.out[0] = o0; g.out[1] = o1; g.out[2] = o2;
-  g.ncols = o1 ? N / 3 : N;
-  if (o1 && (g.ncols % BN)) return DPP_ERR_SHAPE;
+  g.ncols = ncols;
   g.status = status;
   g.wait_limit = wait_limit;
-  dim3 grid((unsigned)(M / BM), N / BN);
-  tc_gemm_kernel<false><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, ta, tb, g);
-  return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+  return dispatch<false>(bn, ta, ta, tb, g, s);
 }
 
 int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,
                    int Cin, int Cout, int P, int* status, long long wait_limit, cudaStream_t s) {
   if (!tc_conv_supported(B, H, W, Cin, Cout, P)) return DPP_ERR_SHAPE;
-  int rc = set_smem_attr();
-  if (rc) return rc;
+  const int bn = pick_bn(Cout, Cout);
+  if (!bn) return DPP_ERR_SHAPE;
   const int box_px = W < 128 ? W : 128;
   CUtensorMap tf, ts, tw;
   const uint64_t dy[4] = {(uint64_t)Cin, (uint64_t)W, (uint64_t)H, (uint64_t)B};
@@ -293,21 +372,20 @@ int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int
   const uint32_t by[4] = {BK, (uint32_t)box_px, 1, 1};
   const int K = 9 * Cin;
   const uint64_t dw[2] = {(uint64_t)K, (uint64_t)Cout}, sw[1] = {(uint64_t)K * 2};
-  const uint32_t bw[2] = {BK, BN};
+  const uint32_t bw[2] = {BK, (uint32_t)bn};
   if (!make_map(&tf, yf, 4, dy, sy, by) || !make_map(&ts, ys, 4, dy, sy, by) ||
       !make_map(&tw, w, 2, dw, sw, bw))
     return DPP_ERR_CUDA;
   GemmArgs g{};
   g.M = (long long)B * H * W; g.N = Cout; g.K = K; g.nkb = K / BK;
+  g.m_tiles = (int)(g.M / BM);
   g.out[0] = out; g.ncols = Cout;
   g.status = status;
   g.wait_limit = wait_limit;
   g.H = H; g.W = W; g.Cin = Cin; g.Hp = H / P; g.cin_blocks = Cin / BK;
   g.boxes = BM / box_px;
   g.box_px = box_px;
-  dim3 grid((unsigned)(g.M / BM), Cout / BN);
-  tc_gemm_kernel<true><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(tf, ts, tw, g);
-  return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+  return dispatch<true>(bn, tf, ts, tw, g, s);
 }
 
 }  // namespace dpp
