@@ -92,13 +92,21 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
   float* s_tot = sm + 3 * g.C;  // [P][G][2] fresh sums of every patch (sync) or own
   const int chunk = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
-  // fresh sums over chunks, for own patch (and every patch at the synchronous step)
+  // fresh sums over chunks, for own patch (and every patch at the synchronous step);
+  // eight independent partial sums so that the chunk loads are in flight together
   for (int idx = tid; idx < g.P * g.G * 2; idx += blockDim.x) {
     const int q = idx / (g.G * 2), r = idx % (g.G * 2);
     float v = 0.f;
     if (sync || q == p) {
       const float* src = partial + (((long long)b * g.P + q) * g.nchunk) * g.G * 2 + r;
-      for (int c = 0; c < g.nchunk; ++c) v += src[(long long)c * g.G * 2];
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      int c = 0;
+      for (; c + 8 <= g.nchunk; c += 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] += src[(long long)(c + u) * g.G * 2];
+      }
+      for (; c < g.nchunk; ++c) acc[c & 7] += src[(long long)c * g.G * 2];
+      v = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     } else {
       v = stale_stats[((long long)b * g.P + q) * g.G * 2 + r];
     }
@@ -124,38 +132,39 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
     s_be[c] = beta[c];
   }
   __syncthreads();
+  // each thread keeps one 16-byte channel vector (and its GroupNorm parameters in
+  // registers) and walks pixels, four loads in flight
   const int NV = g.C / VEC;
+  const int PIX = 256 / NV;
+  const int pl = tid / NV, v = tid % NV;
+  if (pl >= PIX) return;
+  float mu[VEC], sc[VEC], be[VEC];
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) {
+    mu[k] = s_mu[v * VEC + k];
+    sc[k] = s_sc[v * VEC + k];
+    be[k] = s_be[v * VEC + k];
+  }
   const long long band_pix = (long long)g.Hp * g.W;
   const long long p0 = (long long)chunk * g.chunk_pix;
   const long long p1 = min(band_pix, p0 + g.chunk_pix);
-  const long long base = (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C;
-  const long long nvec = (p1 - p0) * NV;
-  const long long bd = blockDim.x;
-  auto apply_one = [&](const uint4& u, long long i) {
-    const long long px = p0 + i / NV;
-    const int v = (int)(i % NV);
-    const long long off = base + px * g.C + v * VEC;
+  const long long base = (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C + v * VEC;
+  auto apply_one = [&](const uint4& u, long long px) {
     float f[VEC];
     unpack16(u, f);
 #pragma unroll
-    for (int k = 0; k < VEC; ++k) {
-      const int c = v * VEC + k;
-      f[k] = fmaf(f[k] - s_mu[c], s_sc[c], s_be[c]);
-    }
-    *reinterpret_cast<uint4*>(y + off) = pack16(f);
+    for (int k = 0; k < VEC; ++k) f[k] = fmaf(f[k] - mu[k], sc[k], be[k]);
+    *reinterpret_cast<uint4*>(y + base + px * g.C) = pack16(f);
   };
-  auto src = [&](long long i) {
-    return reinterpret_cast<const uint4*>(x + base + (p0 + i / NV) * g.C + (i % NV) * VEC);
-  };
-  long long i = tid;
-  for (; i + 3 * bd < nvec; i += 4 * bd) {  // four independent loads in flight
+  long long px = p0 + pl;
+  for (; px + 3 * PIX < p1; px += 4 * PIX) {
     uint4 u[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) u[k] = __ldcs(src(i + k * bd));
+    for (int k = 0; k < 4; ++k) u[k] = __ldcs(reinterpret_cast<const uint4*>(x + base + (px + k * PIX) * g.C));
 #pragma unroll
-    for (int k = 0; k < 4; ++k) apply_one(u[k], i + k * bd);
+    for (int k = 0; k < 4; ++k) apply_one(u[k], px + k * PIX);
   }
-  for (; i < nvec; i += bd) apply_one(__ldcs(src(i)), i);
+  for (; px < p1; px += PIX) apply_one(__ldcs(reinterpret_cast<const uint4*>(x + base + px * g.C)), px);
 }
 
 GnDims make_gn_dims(int B, int H, int W, int C, int P, int G) {

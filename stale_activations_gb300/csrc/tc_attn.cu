@@ -136,9 +136,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   const int nkt = a.nkt;
 
   if (warp >= 8) {
-    // Register split (launch: 384 threads x 168): this warpgroup drops to 56 per
-    // thread, the two softmax warpgroups rise to 216: 128 x 56 + 256 x 216 <= 64512.
-    ptx::regs_dec<56>();
+    // Register split (launch: 384 threads x 168): this warpgroup drops to 64 per
+    // thread, the two softmax warpgroups rise to 208: 128 x 64 + 256 x 208 <= 64512.
+    ptx::regs_dec<64>();
     if (warp == 8) {
       // ---------------------------------------------------------- TMA producer
       if (lane == 0) {
@@ -185,8 +185,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       if (lane == 0) {
         constexpr uint32_t idesc_qk = ptx::idesc_f16(QT, KT, 1, 0, 0);
         constexpr uint32_t idesc_pv = ptx::idesc_f16(QT, D, 0, 0, 1);
-        const uint32_t q_addr = ptx::smem_u32(smem + OFF_Q);
-        const uint32_t kv_addr = ptx::smem_u32(smem + OFF_KV);
+        // Descriptors are affine in the smem address (address field = bytes >> 4, no
+        // carry out for offsets inside shared memory): precompute the bases once.
+        const uint64_t q_desc = ptx::sw128_desc(ptx::smem_u32(smem + OFF_Q), 16, 1024);
+        const uint64_t k_desc = ptx::sw128_desc(ptx::smem_u32(smem + OFF_KV), 16, 1024);
+        const uint64_t v_desc =
+            ptx::sw128_desc(ptx::smem_u32(smem + OFF_KV + TILE_BYTES), TILE_BYTES, 1024);
+        constexpr uint64_t kStageStep = (2 * TILE_BYTES) >> 4;  // next K/V stage
+        constexpr uint64_t kQTile = TILE_BYTES >> 4;            // next query tile
         bool any = false;
         bool ok = wait_or_abort(&bars->q_full, 0, a, bars) &&
                   wait_or_abort(&bars->k_full[0], 0, a, bars);
@@ -196,8 +202,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           for (int t = 0; t < 2; ++t) {
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              ptx::mma_ss(tmem + 128u * t, ptx::sw128_desc(q_addr + t * TILE_BYTES + k * 32, 16, 1024),
-                          ptx::sw128_desc(kv_addr + k * 32, 16, 1024), idesc_qk, k ? 1u : 0u);
+              ptx::mma_ss(tmem + 128u * t, q_desc + t * kQTile + 2 * k, k_desc + 2 * k, idesc_qk,
+                          k ? 1u : 0u);
             ptx::mma_commit(&bars->s_full[t]);
           }
           any = true;
@@ -205,8 +211,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         for (int j = 0; j < nkt && ok; ++j) {
           const int st = j % KV_STAGES;
           const bool more = j + 1 < nkt;
-          const uint32_t v_addr = kv_addr + (uint32_t)(st * 2 * TILE_BYTES + TILE_BYTES);
-          const uint32_t k_next = kv_addr + (uint32_t)(((j + 1) % KV_STAGES) * 2 * TILE_BYTES);
+          const uint64_t vd = v_desc + (uint64_t)st * kStageStep;
+          const uint64_t kd = k_desc + (uint64_t)((j + 1) % KV_STAGES) * kStageStep;
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (!wait_or_abort(&bars->p_full[t], j & 1, a, bars) ||
@@ -221,14 +228,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
             const uint32_t tO = tmem + 256u + 64u * t, tP = tmem + 384u + 64u * t;
 #pragma unroll
             for (int k = 0; k < KT / 16; ++k)  // O_t += P_t(j) V(j)
-              ptx::mma_ts(tO, tP + k * 8, ptx::sw128_desc(v_addr + k * 2048, TILE_BYTES, 1024),
-                          idesc_pv, (j | k) ? 1u : 0u);
+              ptx::mma_ts(tO, tP + k * 8, vd + 128 * k, idesc_pv, k ? 1u : acc0);
             if (more) {                         // S_t = Q_t K(j+1)^T
 #pragma unroll
               for (int k = 0; k < D / 16; ++k)
-                ptx::mma_ss(tmem + 128u * t,
-                            ptx::sw128_desc(q_addr + t * TILE_BYTES + k * 32, 16, 1024),
-                            ptx::sw128_desc(k_next + k * 32, 16, 1024), idesc_qk, k ? 1u : 0u);
+                ptx::mma_ss(tmem + 128u * t, q_desc + t * kQTile + 2 * k, kd + 2 * k, idesc_qk,
+                            k ? 1u : 0u);
               ptx::mma_commit(&bars->s_full[t]);
             } else {
               ptx::mma_commit(&bars->o_done[t]);
@@ -271,7 +276,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       }
     }
   } else {
-    ptx::regs_inc<216>();
+    ptx::regs_inc<208>();
     // ------------------------------------------------------------ softmax (warps 0-7)
     const int t = warp >> 2;             // query tile of this warpgroup
     const int quarter = warp & 3;        // TMEM lanes [32*quarter, +32)
@@ -327,22 +332,32 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       }
       // exponentials 32 keys at a time, stored at once as fp16 P into TMEM (column c
       // holds keys 2c in the low half and 2c+1 in the high half)
-      float lq[4] = {0.f, 0.f, 0.f, 0.f};  // 4 independent partial row sums
+      // pairs of keys in packed fp32x2: one FMA and one add per two keys
+      const uint64_t c2 = ptx::pack_f32x2(kScaleLog2, kScaleLog2);
+      const uint64_t nm2 = ptx::pack_f32x2(-m_ref, -m_ref);
+      uint64_t lq[2] = {ptx::pack_f32x2(0.f, 0.f), ptx::pack_f32x2(0.f, 0.f)};  // row sums
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(__uint_as_float(s[32 * c + 2 * i]), kScaleLog2, -m_ref));
-          const float p1 = ex2(fmaf(__uint_as_float(s[32 * c + 2 * i + 1]), kScaleLog2, -m_ref));
-          lq[(2 * i) & 3] += p0;
-          lq[(2 * i + 1) & 3] += p1;
+          const uint64_t sv = ptx::pack_f32x2(__uint_as_float(s[32 * c + 2 * i]),
+                                              __uint_as_float(s[32 * c + 2 * i + 1]));
+          float a0, a1;
+          ptx::unpack_f32x2(ptx::fma_f32x2(sv, c2, nm2), a0, a1);
+          const float p0 = ex2(a0), p1 = ex2(a1);
+          lq[i & 1] = ptx::add_f32x2(lq[i & 1], ptx::pack_f32x2(p0, p1));
           __half2 hv = __floats2half2_rn(p0, p1);
           pk[i] = *reinterpret_cast<uint32_t*>(&hv);
         }
         ptx::tmem_st16(tP + lane_off + 16 * c, pk);
       }
-      l += (lq[0] + lq[1]) + (lq[2] + lq[3]);
+      {
+        float x0, x1, y0, y1;
+        ptx::unpack_f32x2(lq[0], x0, x1);
+        ptx::unpack_f32x2(lq[1], y0, y1);
+        l += (x0 + x1) + (y0 + y1);
+      }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
