@@ -53,6 +53,81 @@ def _dist():
     return ws, rank, lrank
 
 
+class NvmlClockSampler:
+    """Polls SM clock and clock-event reasons through NVML (read-only queries) every
+    millisecond while the timed region runs; falls back to nvidia-smi sampling."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int, period_s: float = 0.001):
+        self.index, self.period = index, period_s
+        self.samples, self.reason_bits = [], 0
+        self.max_mhz = None
+        self.ok = False
+        self.fallback = None
+
+    def _setup(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        n = ctypes.c_uint(0)
+        lib.nvmlDeviceGetCount_v2(ctypes.byref(n))
+        h = ctypes.c_void_p()
+        idx = 0 if n.value == 1 else self.index
+        if lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) != 0:
+            raise OSError("nvml handle")
+        mx = ctypes.c_uint(0)
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = mx.value
+        try:
+            self.reasons_fn = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self.reasons_fn = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.lib, self.h = lib, h
+
+    def _poll(self):
+        import ctypes
+        mhz = ctypes.c_uint(0)
+        reasons = ctypes.c_ulonglong(0)
+        while not self.stop:
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(mhz.value)
+            if self.reasons_fn(self.h, ctypes.byref(reasons)) == 0:
+                self.reason_bits |= reasons.value
+            time.sleep(self.period)
+
+    def __enter__(self):
+        try:
+            self._setup()
+            self.stop = False
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+            self.ok = True
+        except Exception:
+            self.fallback = ClockSampler(self.index).__enter__()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self.stop = True
+            self.t.join(timeout=2)
+        elif self.fallback:
+            self.fallback.__exit__(*a)
+
+    def summary(self):
+        if not self.ok:
+            out = self.fallback.summary() if self.fallback else {"reasons": ["unsampled"]}
+            out["source"] = "nvidia-smi"
+            return out
+        reasons = sorted(v for k, v in self.REASONS.items() if self.reason_bits & k)
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
+                    "samples": 0, "source": "nvml"}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples), "source": "nvml"}
+
+
 class ClockSampler:
     """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -183,7 +258,7 @@ def run_gpu(args):
             tdist.barrier()
         torch.cuda.synchronize()
 
-    with ClockSampler(lrank) as clocks:
+    with NvmlClockSampler(lrank) as clocks:
         barrier()
         t0 = time.perf_counter()
         for i in range(K):

@@ -21,7 +21,10 @@
 //                    on one tile while the other's softmax runs; and because the
 //                    tensor pipe completes one thread's MMAs in order, "S_t(j+1)
 //                    ready" also means P_t(j) and O_t are free again.
-//   warps 10-11      widen each landed V tile from bf16 to fp16 in place.
+//   warps 10-11      idle (they keep the warpgroup whole for the register split).
+// Each softmax warp also widens a 1/8 share of the next V tile from bf16 to fp16 in
+// place, one key tile ahead, so that this work is spread evenly over the four SM
+// quarters instead of slowing the softmax warps that share a quarter with helpers.
 // P is rounded to fp16, not bf16: its 11-bit significand keeps the rounding of
 // the probabilities well inside the 2e-3 output tolerance (bf16's 8 bits would
 // not), and V is widened to fp16 exactly so that P V runs as kind::f16 with
@@ -48,7 +51,7 @@ constexpr int KT = 128;                 // keys per tile
 constexpr int KV_STAGES = 5;
 constexpr int TILE_BYTES = KT * D * 2;  // 16 KB (K or V tile, Q tile)
 constexpr int ATTN_THREADS = 384;
-constexpr int NUM_CONVERTERS = 2;       // warps 10-11
+constexpr int NUM_CONVERTERS = 8;       // the softmax warps, a 1/8 share each
 // smem: Q0 Q1 | (K V) x stages | barriers.  TMEM (512 columns): S0 S1 (128 each),
 // O0 O1 (64 each), P0 P1 (64 each: 128 fp16 probabilities per row, two per column).
 constexpr int OFF_Q = 0;
@@ -246,35 +249,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           ptx::mbar_wait(&bars->drain, 0, kDrainWaitLimit, nullptr);
         }
       }
-    } else {
-      // ---------------------------------------------------------- V: bf16 -> fp16 in place
-      const int ct = threadIdx.x - 10 * 32;  // 0..63
-      for (int j = 0; j < nkt; ++j) {
-        const int st = j % KV_STAGES;
-        // lane 0 sleeps on the barrier; then every lane observes the completed phase
-        // (returns at once) so that all lanes see the landed tile
-        int ok = 1;
-        if (lane == 0) ok = wait_or_abort(&bars->v_full[st], (j / KV_STAGES) & 1, a, bars);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        if (!wait_or_abort(&bars->v_full[st], (j / KV_STAGES) & 1, a, bars)) break;
-        uint4* v = reinterpret_cast<uint4*>(smem + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES);
-#pragma unroll 4
-        for (int i = ct; i < TILE_BYTES / 16; i += 32 * NUM_CONVERTERS) {
-          uint4 u = v[i];
-          uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
-            __half2 hv = __floats2half2_rn(lo, hi);
-            w[e] = *reinterpret_cast<uint32_t*>(&hv);
-          }
-          v[i] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bars->v_conv[st]);
-      }
     }
+    // warps 10-11: nothing to do
   } else {
     ptx::regs_inc<208>();
     // ------------------------------------------------------------ softmax (warps 0-7)
@@ -286,8 +262,40 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     const uint32_t tO = tmem + 256u + 64u * (uint32_t)t;  // O_t: 64 columns
     const uint32_t tP = tmem + 384u + 64u * (uint32_t)t;  // P_t: 64 columns
     float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkt; ++j) {
+    // Widens this warp's 1/8 share of V(jj) in place once the tile has landed.
+    auto convert_share = [&](int jj) -> bool {
+      const int st = jj % KV_STAGES;
+      const uint32_t par = (jj / KV_STAGES) & 1;
+      // lane 0 sleeps on the barrier; then every lane observes the completed phase
+      // (returns at once) so that all lanes see the landed tile
+      int okw = 1;
+      if (lane == 0) okw = wait_or_abort(&bars->v_full[st], par, a, bars);
+      if (!__shfl_sync(0xffffffffu, okw, 0)) return false;
+      if (!wait_or_abort(&bars->v_full[st], par, a, bars)) return false;
+      uint4* v = reinterpret_cast<uint4*>(smem + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES) +
+                 warp * (TILE_BYTES / 16 / NUM_CONVERTERS);
+      uint4 u[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) u[i] = v[lane + 32 * i];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+          __half2 hv = __floats2half2_rn(lo, hi);
+          w[e] = *reinterpret_cast<uint32_t*>(&hv);
+        }
+        v[lane + 32 * i] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->v_conv[st]);
+      return true;
+    };
+    bool ok = convert_share(0);
+    for (int j = 0; j < nkt && ok; ++j) {
+      if (j + 1 < nkt && !convert_share(j + 1)) { ok = false; break; }
       // S_t(j) ready; the MMA thread issued it after P_t(j-1) V(j-1), so that
       // product has completed too: P_t and O_t may be touched.
       if (!wait_or_abort(&bars->s_full[t], j & 1, a, bars)) { ok = false; break; }

@@ -63,3 +63,22 @@ def test_attention_sdxl3840_sampled_rows():
     ref = oracle.stale_kv_attention(*(np64(t) for t in (q, kf, vf, ks, vs)), heads, P, "bf16",
                                     rows=rows)
     assert rel_err(np64(o)[:, rows], ref) < TOL_BF16
+
+
+@pytest.mark.parametrize("P", [1, 2])
+def test_attention_late_large_scores_rescale(P):
+    """Scores in a late key tile far above those of the first tiles: the running
+    reference maximum must move (O and the row sum rescaled) and the result still
+    matches the oracle."""
+    B, L, heads = 1, 1024, 1
+    g = torch.Generator().manual_seed(11)
+    q = (0.5 + 0.05 * torch.randn(B, L, 64, generator=g)).to(torch.bfloat16)
+    k = (0.1 * torch.randn(B, L, 64, generator=g))
+    k[:, 640:768] += 3.0          # tile 5: scores ~ 0.5*3*64/8 = 12 above the rest
+    k[:, 900:910] += 6.0          # a few even larger keys later on
+    k = k.to(torch.bfloat16)
+    v = torch.randn(B, L, 64, generator=g).to(torch.bfloat16)
+    vs = (v.float() + 0.05 * torch.randn(B, L, 64, generator=g)).to(torch.bfloat16)
+    o = _attn_gpu(q, k, v, k, vs, heads, P)
+    ref = oracle.stale_kv_attention(*(np64(t) for t in (q, k, v, k, vs)), heads, P, "bf16")
+    assert rel_err(np64(o), ref) < TOL_BF16
