@@ -33,6 +33,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "patch-layer steps/s; attention TFLOP/s & refresh GB/s as % of GB300 roofline"
+# dram__bytes_read.sum + dram__bytes_write.sum of one SDXL-1024 attention launch from an
+# ncu capture of the current kernel version (None until one is taken)
+ATTN_TRAFFIC_BYTES = None
 WORKLOAD = "sdxl1024_mid_b2_64x64_c640_p4_bf16"
 
 
@@ -305,7 +308,9 @@ def run_gpu(args):
             v["frac_bf16_sustained"] = v["TFLOP/s"] / peaks["bf16_sus"]
     roofline = {"kernel": "stale_kv_attention (tc_attn_kernel)", "bound": "tensor",
                 "achieved": attn_tfs, "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
-                "frac": attn_tfs / peaks["bf16_sus"], "traffic": None,
+                "frac": attn_tfs / peaks["bf16_sus"], "traffic": ATTN_TRAFFIC_BYTES,
+                "traffic_note": "dram read+write bytes per launch (ncu); algorithmic 62.9e6; "
+                                "achieved includes the merge kernel of the split schedule",
                 "peak_kind": f"bf16 dense sustained, {peaks['src']}",
                 "algorithmic": f"4*B*heads*L^2*d = {attn_flop:.4g} FLOP per launch"}
 
@@ -346,7 +351,8 @@ def run_gpu(args):
     if not args.no_secondary:
         line["secondary"] = {"attention_sdxl3840": measure_attention_3840(dev, peaks),
                              "refresh_sweep": measure_refresh_sweep(dev, peaks),
-                             "layer_2x256x256x640_p8": measure_large_layer(dev, peaks)}
+                             "layer_2x256x256x640_p8": measure_large_layer(dev, peaks),
+                             "halo_conv_vae": measure_vae_conv(dev, peaks)}
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
     if ws_n > 1:
@@ -362,8 +368,10 @@ def _randn_bf16(shape, gen, dev):
 
 
 def measure_attention_3840(dev, peaks, iters=5):
-    """stale_kv_attention alone at the SDXL-3840 attention level: B=2, L=57600,
-    10 heads x 64, P=8; K/V_stale = fresh + N(0, 0.05^2).  Inputs (0.74 GB) exceed L2."""
+    """The attention alone at the SDXL-3840 attention level: B=2, L=57600, 10 heads x 64,
+    P=8; K/V_stale = fresh + N(0, 0.05^2).  Inputs (0.74 GB) exceed L2.  Timed with the
+    split schedule the layer step uses (stale_kv_attention_split, attention + merge) and
+    with whole units per CTA (stale_kv_attention)."""
     import torch
 
     import stale_activations_gb300 as dpp
@@ -374,24 +382,39 @@ def measure_attention_3840(dev, peaks, iters=5):
     vs = (vf.float() + 0.05 * torch.randn(vf.shape, generator=g, device=dev)).to(torch.bfloat16)
     o = torch.empty_like(q)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    for _ in range(2):
-        dpp.stale_kv_attention(q, kf, vf, ks, vs, o, heads, P, dev_status=st)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
-    torch.cuda.synchronize()
-    ev[0].record()
-    for i in range(iters):
-        dpp.stale_kv_attention(q, kf, vf, ks, vs, o, heads, P, dev_status=st)
-        ev[i + 1].record()
-    torch.cuda.synchronize()
-    if st.item() != 0:
-        raise RuntimeError("attention device status set")
-    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(iters)]
+    npart = dpp.attention_partials_size(B, L, heads, P)
+    part = torch.empty(max(npart, 16), dtype=torch.uint8, device=dev)
     flop = 4.0 * B * heads * L * L * 64
-    tfs = flop / (statistics.mean(ms) * 1e-3) / 1e12
-    return {"ms_mean": statistics.mean(ms), "ms_min": min(ms), "TFLOP/s": tfs,
+
+    def run(split):
+        if split:
+            dpp.stale_kv_attention_split(q, kf, vf, ks, vs, o, heads, P,
+                                         partials=part if npart else None, dev_status=st)
+        else:
+            dpp.stale_kv_attention(q, kf, vf, ks, vs, o, heads, P, dev_status=st)
+
+    res = {}
+    for split in (True, False):
+        for _ in range(2):
+            run(split)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
+        torch.cuda.synchronize()
+        ev[0].record()
+        for i in range(iters):
+            run(split)
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        if st.item() != 0:
+            raise RuntimeError("attention device status set")
+        ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(iters)]
+        res[split] = (statistics.mean(ms), min(ms), flop / (statistics.mean(ms) * 1e-3) / 1e12)
+    ms_mean, ms_min, tfs = res[True]
+    return {"ms_mean": ms_mean, "ms_min": ms_min, "TFLOP/s": tfs,
             "frac_of_burst_bf16": tfs / peaks["bf16"], "peak_burst": peaks["bf16"],
             "frac_of_sustained_bf16": tfs / peaks["bf16_sus"], "flop_per_launch": flop,
-            "launches": iters, "note": "back-to-back launches, inputs > L2"}
+            "launches": iters, "schedule": "split (attention + merge kernel)",
+            "whole_units": {"ms_mean": res[False][0], "TFLOP/s": res[False][2]},
+            "note": "back-to-back launches, inputs > L2"}
 
 
 def measure_refresh_sweep(dev, peaks, iters=5):
@@ -428,6 +451,39 @@ def measure_refresh_sweep(dev, peaks, iters=5):
     return {"ms_mean": statistics.mean(ms), "ms_min": min(ms), "GB/s": gbs,
             "frac_hbm": gbs / peaks["hbm"], "peak_hbm": peaks["hbm"], "elements": n,
             "bytes_per_launch": nbytes, "launches": iters}
+
+
+def measure_vae_conv(dev, peaks, iters=5):
+    """halo_conv3x3 alone at the VAE-decoder-like size: 1x256x256x512 -> 512, P=8 row
+    bands with stale halo rows (inputs 64 MiB each; L2 flushed before each launch)."""
+    import torch
+
+    import stale_activations_gb300 as dpp
+    B, H, W, C, P = 1, 256, 256, 512, 8
+    g = torch.Generator(device=dev).manual_seed(4)
+    y = _randn_bf16((B, H, W, C), g, dev)
+    ys = (y.float() + 0.05 * torch.randn(y.shape, generator=g, device=dev)).to(torch.bfloat16)
+    w = (0.02 * torch.randn(C, 3, 3, C, generator=g, device=dev)).to(torch.bfloat16)
+    out = torch.empty_like(y)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    ms = []
+    for i in range(iters + 2):
+        flush.fill_(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dpp.halo_conv3x3(y, ys, w, out, P, dev_status=st)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 2:
+            ms.append(e0.elapsed_time(e1))
+    if st.item() != 0:
+        raise RuntimeError("conv device status set")
+    flop = 2.0 * B * H * W * C * 9 * C
+    tfs = flop / (statistics.mean(ms) * 1e-3) / 1e12
+    return {"ms_mean": statistics.mean(ms), "ms_min": min(ms), "TFLOP/s": tfs,
+            "frac_of_sustained_bf16": tfs / peaks["bf16_sus"], "flop_per_launch": flop,
+            "launches": iters}
 
 
 def measure_large_layer(dev, peaks, iters=3):

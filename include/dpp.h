@@ -115,13 +115,43 @@ int halo_conv3x3(const void* y_fresh, const void* y_stale, const void* w, void* 
  *   o[t,h] = sum_s softmax_s(q[t,h] . Khat_p[s,h] / sqrt(head_dim)) Vhat_p[s,h]
  * Khat_p[s] = k_fresh[s] for s in patch p, else k_stale[s]; same for Vhat.  All L
  * keys, no mask.  q, k_*, v_*, o: [B, L, heads*head_dim] of `dtype`.
- * Requires head_dim == 64, L % P == 0 and (L/P) % 8 == 0.
+ * Requires head_dim == 64, L % P == 0 and (L/P) % 8 == 0; for DPP_BF16 also
+ * B*heads*P*ceil(L/P/256) * ceil(L/128) < 2^31 (the kernel's step counter).
  * dev_status: device int (may be NULL) that receives a give-up code.
  */
 int stale_kv_attention(const void* q, const void* k_fresh, const void* v_fresh,
                        const void* k_stale, const void* v_stale, void* o,
                        int B, int L, int heads, int head_dim, int P, int dtype,
                        int* dev_status, void* stream);
+
+/*
+ * stale_kv_attention_split -- the same operation and result (up to rounding) with
+ * the load spread evenly over the SMs.  (The pages have no counterpart of this
+ * call: it is a schedule of stale_kv_attention for this GPU, used by
+ * patch_layer_step.)
+ * The bf16 kernel works on units of 256 queries (two 128-row tiles of one batch,
+ * head and patch) against all L keys, one CTA per SM.  stale_kv_attention gives
+ * each CTA whole units, so when their number is not a multiple of the SM count
+ * the last round leaves SMs idle.  Here those last units are cut into runs of
+ * 128-key tiles shared evenly by all CTAs; each piece leaves a partial result
+ * (O/l rounded to fp16, the running maximum m and sum l in fp32) in `partials`,
+ * and a second kernel merges the pieces of each unit in a fixed order
+ * (deterministic).  The merge reads O/l in fp16, whose rounding (2^-11 relative)
+ * stays well below that of the bf16 output.
+ * partials: caller-owned device buffer, 16-byte aligned, of at least
+ * dpp_attention_partials_size() bytes; that size depends on the current device's
+ * SM count, so query it on the device that runs the call.  It may be NULL when
+ * the size is 0 (the units divide evenly; both calls then run the same kernel).
+ * The buffer is scratch: its contents are not used after the call.
+ * Returns DPP_ERR_ARG if the buffer is missing or too small.  DPP_F32 runs the
+ * fp32 kernel of stale_kv_attention and ignores `partials`.
+ */
+size_t dpp_attention_partials_size(int B, int L, int heads, int head_dim, int P, int dtype);
+int stale_kv_attention_split(const void* q, const void* k_fresh, const void* v_fresh,
+                             const void* k_stale, const void* v_stale, void* o,
+                             int B, int L, int heads, int head_dim, int P, int dtype,
+                             void* partials, size_t partials_bytes,
+                             int* dev_status, void* stream);
 
 /* ---------------------------------------------------------------- layer step */
 
@@ -164,6 +194,10 @@ typedef struct dpp_workspace_layout {
   size_t h;          /* [B,H,W,C] conv output */
   size_t q, k, v;    /* [B,L,C] fresh projections */
   size_t o;          /* [B,L,C] attention output */
+  size_t attn_partial;       /* partial results of the split attention schedule
+                                (dpp_attention_partials_size bytes) */
+  size_t attn_partial_bytes; /* their size, 0 when the units divide evenly (a size, not an
+                                offset) */
   size_t total;      /* bytes to allocate */
 } dpp_workspace_layout;
 
@@ -220,12 +254,12 @@ int dpp_read_device_status(const void* workspace, void* stream);
  * loop where cudaMalloc's implicit synchronisation is not allowed.)
  *
  * Same arguments, semantics and results as patch_layer_step, except that the
- * workspace is one fixed 64 MiB array of device memory inside the library; no
+ * workspace is one fixed 80 MiB array of device memory inside the library; no
  * cudaMalloc, cudaFree or other allocating routine is called.  Every GPU that
- * loads this part of the library holds the 64 MiB until the process exits.
- *   - Layers whose dpp_workspace_size() exceeds 64 MiB return
+ * loads this part of the library holds the 80 MiB until the process exits.
+ *   - Layers whose dpp_workspace_size() exceeds 80 MiB return
  *     DPP_ERR_SCRATCH_LIMIT before anything is launched (the SDXL-1024
- *     mid-level layer, B=2 x 64x64 x 640 bf16, needs about 60 MiB).
+ *     mid-level layer, B=2 x 64x64 x 640 bf16, needs about 71 MiB).
  *   - The first call on a device, with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress) and caches it; make that
  *     first call before any stream capture on that device.

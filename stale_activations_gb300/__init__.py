@@ -51,12 +51,14 @@ class LayerState(ctypes.Structure):
 
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("status", "gn_partial", "gn_fresh", "y", "h", "q", "k", "v", "o", "total")]
+                ("status", "gn_partial", "gn_fresh", "y", "h", "q", "k", "v", "o", "attn_partial",
+                 "attn_partial_bytes", "total")]
 
 
 _lib = None
 EXPORTS = ("dpp_status_string", "dpp_version", "refresh_residual", "halo_conv3x3",
-           "stale_kv_attention", "dpp_workspace_query", "dpp_workspace_size", "dpp_message_elems",
+           "stale_kv_attention", "stale_kv_attention_split", "dpp_attention_partials_size",
+           "dpp_workspace_query", "dpp_workspace_size", "dpp_message_elems",
            "dpp_message_blocks", "patch_layer_step", "patch_layer_step_timed",
            "dpp_read_device_status", "dpp_layer_kernel_count", "patch_layer_step_noalloc")
 
@@ -82,6 +84,11 @@ def load(build_if_missing: bool = False):
     lib.halo_conv3x3.argtypes = [_c_void] * 4 + [_c_int] * 7 + [_c_void, _c_void]
     lib.stale_kv_attention.restype = _c_int
     lib.stale_kv_attention.argtypes = [_c_void] * 6 + [_c_int] * 6 + [_c_void, _c_void]
+    lib.stale_kv_attention_split.restype = _c_int
+    lib.stale_kv_attention_split.argtypes = ([_c_void] * 6 + [_c_int] * 6 +
+                                             [_c_void, ctypes.c_size_t, _c_void, _c_void])
+    lib.dpp_attention_partials_size.restype = ctypes.c_size_t
+    lib.dpp_attention_partials_size.argtypes = [_c_int] * 6
     lib.dpp_workspace_query.restype = _c_int
     lib.dpp_workspace_query.argtypes = [P(LayerParams), P(WorkspaceLayout)]
     lib.dpp_workspace_size.restype = ctypes.c_size_t
@@ -170,6 +177,25 @@ def stale_kv_attention(q, k_fresh, v_fresh, k_stale, v_stale, o, heads: int, P: 
            "stale_kv_attention")
 
 
+def attention_partials_size(B: int, L: int, heads: int, P: int, dtype: int = BF16) -> int:
+    """Bytes of the partials buffer stale_kv_attention_split needs on the current device."""
+    return load().dpp_attention_partials_size(B, L, heads, 64, P, dtype)
+
+
+def stale_kv_attention_split(q, k_fresh, v_fresh, k_stale, v_stale, o, heads: int, P: int,
+                             partials=None, dev_status=None, stream=None):
+    """stale_kv_attention with the last units shared by all SMs; ``partials`` is a device
+    buffer of at least attention_partials_size() bytes (None when that is 0)."""
+    lib = load()
+    B, L, C = q.shape
+    nbytes = 0 if partials is None else partials.numel() * partials.element_size()
+    _check(lib.stale_kv_attention_split(_ptr(q), _ptr(k_fresh), _ptr(v_fresh), _ptr(k_stale),
+                                        _ptr(v_stale), _ptr(o), B, L, heads, C // heads, P,
+                                        dtype_code(q), _ptr(partials), nbytes,
+                                        _ptr(dev_status), _stream(stream)),
+           "stale_kv_attention_split")
+
+
 def make_params(B, H, W, C, P, G, heads, dtype, refresh=True, eps=1e-5, head_dim=64):
     return LayerParams(B, H, W, C, P, G, heads, head_dim, dtype, 1 if refresh else 0, eps)
 
@@ -227,7 +253,7 @@ def patch_layer_step(prm: LayerParams, weights: dict, state: dict, x, out, mode:
 
 def patch_layer_step_noalloc(prm: LayerParams, weights: dict, state: dict, x, out, mode: int,
                              stream=None):
-    """patch_layer_step with the library's fixed 64 MiB device scratch as workspace.
+    """patch_layer_step with the library's fixed 80 MiB device scratch as workspace.
 
     For callers that cannot allocate device memory when they run a layer; nothing
     is allocated here or in the library.  Calls that overlap on the GPU share the

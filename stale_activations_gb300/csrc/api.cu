@@ -65,7 +65,9 @@ int check_attn(int B, int L, int heads, int head_dim, int P, int dtype) {
   if (head_dim != 64) return DPP_ERR_SHAPE;
   if (L % P || (L / P) % 8) return DPP_ERR_SHAPE;
   if ((long long)B * L * heads * 64 >= (1ll << 40)) return DPP_ERR_SHAPE;
-  (void)dtype;
+  // the tensor-core kernel numbers its (unit, key tile) steps with 32-bit integers
+  const long long units = (long long)B * heads * P * (((L / P + 127) / 128 + 1) / 2);
+  if (dtype == DPP_BF16 && units * ((L + 127) / 128) >= (1ll << 31)) return DPP_ERR_SHAPE;
   return DPP_OK;
 }
 
@@ -105,6 +107,13 @@ int layout(const dpp_layer_params* p, dpp_workspace_layout* o) {
   o->k = off; off = align256(off + act);
   o->v = off; off = align256(off + act);
   o->o = off; off = align256(off + act);
+  // partial results of the split attention schedule (a region of their own, so that
+  // every stage's output stays readable after the step)
+  const size_t part = p->dtype == DPP_BF16 ? dpp::tc_attention_partial_bytes(
+                                                 p->B, p->H * p->W, p->heads, p->P)
+                                           : 0;
+  o->attn_partial = off; off = align256(off + part);
+  o->attn_partial_bytes = part;
   o->total = off;
   return DPP_OK;
 }
@@ -129,9 +138,10 @@ int run_linear(const void* a, const void* w, void* o0, void* o1, void* o2, long 
 }
 
 int run_attention(const void* q, const void* kf, const void* vf, const void* ks, const void* vs,
-                  void* o, int B, int L, int heads, int P, int dtype, int* st, cudaStream_t s) {
+                  void* o, int B, int L, int heads, int P, int dtype, void* part,
+                  size_t part_bytes, int* st, cudaStream_t s) {
   if (dtype == DPP_BF16)
-    return dpp::launch_tc_attention(q, kf, vf, ks, vs, o, B, L, heads, P, st,
+    return dpp::launch_tc_attention(q, kf, vf, ks, vs, o, B, L, heads, P, part, part_bytes, st,
                                     dpp_host::wait_limit_from_env(), s);
   return dpp::launch_simt_attention(q, kf, vf, ks, vs, o, B, L, heads, P, dtype, s);
 }
@@ -212,8 +222,33 @@ int stale_kv_attention(const void* q, const void* k_fresh, const void* v_fresh,
   if (!aligned16(q) || !aligned16(k_fresh) || !aligned16(v_fresh) || !aligned16(k_stale) ||
       !aligned16(v_stale) || !aligned16(o))
     return DPP_ERR_ALIGN;
+  return run_attention(q, k_fresh, v_fresh, k_stale, v_stale, o, B, L, heads, P, dtype, nullptr,
+                       0, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+size_t dpp_attention_partials_size(int B, int L, int heads, int head_dim, int P, int dtype) {
+  if (check_dtype(dtype) || check_attn(B, L, heads, head_dim, P, dtype)) return 0;
+  return dtype == DPP_BF16 ? dpp::tc_attention_partial_bytes(B, L, heads, P) : 0;
+}
+
+int stale_kv_attention_split(const void* q, const void* k_fresh, const void* v_fresh,
+                             const void* k_stale, const void* v_stale, void* o, int B, int L,
+                             int heads, int head_dim, int P, int dtype, void* partials,
+                             size_t partials_bytes, int* dev_status, void* stream) {
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  if (!q || !k_fresh || !v_fresh || !k_stale || !v_stale || !o) return DPP_ERR_NULL;
+  rc = check_attn(B, L, heads, head_dim, P, dtype);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k_fresh) || !aligned16(v_fresh) || !aligned16(k_stale) ||
+      !aligned16(v_stale) || !aligned16(o) || (partials && !aligned16(partials)))
+    return DPP_ERR_ALIGN;
+  const size_t need = dpp_attention_partials_size(B, L, heads, head_dim, P, dtype);
+  if (need && (!partials || partials_bytes < need)) return DPP_ERR_ARG;
+  // with `need` 0 the units divide evenly and both schedules are the same
   return run_attention(q, k_fresh, v_fresh, k_stale, v_stale, o, B, L, heads, P, dtype,
-                       dev_status, static_cast<cudaStream_t>(stream));
+                       need ? partials : nullptr, partials_bytes, dev_status,
+                       static_cast<cudaStream_t>(stream));
 }
 
 int dpp_workspace_query(const dpp_layer_params* prm, dpp_workspace_layout* out) {
@@ -241,6 +276,8 @@ int64_t dpp_message_blocks(const dpp_layer_params* p) {
 int dpp_layer_kernel_count(const dpp_layer_params* p, int mode) {
   if (check_layer(p)) return -1;
   int n = 2 /* gn */ + 1 /* conv */ + 1 /* qkv */ + 1 /* attention */ + 1 /* out proj */;
+  if (p->dtype == DPP_BF16)  // + the merge of the split attention schedule
+    n += dpp::tc_attention_kernel_count(p->B, p->H * p->W, p->heads, p->P, true) - 1;
   if (mode == DPP_STALE && p->refresh) {
     const long long nseg = 2 + (long long)p->B * (p->P - 1);
     n += (int)cdiv(nseg, dpp::kMaxRefreshSegs);
@@ -313,7 +350,8 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
   if (rc || (rc = mark(3))) return rc;
   // a5: stale-KV attention
   rc = run_attention(q, k, v, sync ? k : st->k_stale, sync ? v : st->v_stale, o, p.B, L, p.heads,
-                     p.P, p.dtype, status, s);
+                     p.P, p.dtype, lo.attn_partial_bytes ? ws + lo.attn_partial : nullptr,
+                     lo.attn_partial_bytes, status, s);
   if (rc || (rc = mark(4))) return rc;
   // a6: output projection
   rc = run_linear(o, wts->w_o, out, nullptr, nullptr, M, p.C, p.C, p.dtype, status, s);

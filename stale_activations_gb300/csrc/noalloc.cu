@@ -23,7 +23,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 64ull << 20;  // 64 MiB
+constexpr size_t kNoAllocScratchBytes = 80ull << 20;  // 80 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

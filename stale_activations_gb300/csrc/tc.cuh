@@ -17,9 +17,15 @@ int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2,
 int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,
                    int Cin, int Cout, int P, int* status, long long wait_limit, cudaStream_t s);
 
-// Stale-KV flash attention (see stale_kv_attention in dpp.h), head_dim 64.
+// Stale-KV flash attention (see stale_kv_attention in dpp.h), head_dim 64.  With
+// `partials` non-NULL the units that do not divide evenly over the CTAs are shared key
+// tile by key tile and merged by a second kernel; partial_bytes must then be at least
+// tc_attention_partial_bytes() (0 when the units divide evenly).
 int launch_tc_attention(const void* q, const void* kf, const void* vf, const void* ks,
-                        const void* vs, void* o, int B, int L, int heads, int P, int* status,
-                        long long wait_limit, cudaStream_t s);
+                        const void* vs, void* o, int B, int L, int heads, int P, void* partials,
+                        size_t partial_bytes, int* status, long long wait_limit, cudaStream_t s);
+size_t tc_attention_partial_bytes(int B, int L, int heads, int P);
+// Kernels launch_tc_attention launches (1, or 2 with the split schedule).
+int tc_attention_kernel_count(int B, int L, int heads, int P, bool split);
 
 }  // namespace dpp

@@ -6,10 +6,21 @@
 // all L keys; key row s comes from the fresh K/V if s lies in patch p, else
 // from the stale K/V.
 //
-// One CTA = two 128-row query tiles of one (batch, head, patch), 12 warps:
+// Work unit = two 128-row query tiles of one (batch, head, patch) against all key
+// tiles.  The kernel is persistent (one CTA per SM): CTA c first takes whole units
+// c, c+G, c+2G, ... (G CTAs; consecutive CTAs work on neighbouring units, which
+// share their K/V in L2), and when the units do not divide evenly the remaining
+// U mod G units are shared by all CTAs key tile by key tile ("split" schedule):
+// each CTA takes an equal contiguous run of their (unit, key tile) steps, a unit
+// cut between CTAs leaves one partial result per piece (O/l in fp16, the running
+// maximum m and sum l in fp32), and attn_combine_kernel merges the pieces of each
+// cut unit in CTA order (deterministic).  A CTA's steps run through one pipeline:
+// the next unit's Q is loaded into the second Q buffer while the current unit
+// finishes, and its first S = Q K^T is issued right after the last P V.
+// Per CTA, 12 warps:
 //   warps 0-3 / 4-7  softmax of query tile 0 / 1 (thread = query row = TMEM lane):
 //                    read S_t from TMEM, write fp16 P_t back to TMEM.
-//   warp 8           TMA producer: Q tiles once, then a 5-stage ring of K and V
+//   warp 8           TMA producer: Q tiles per unit (two buffers), a 5-stage ring of K and V
 //                    tiles; each 128-key tile is fetched in sub-boxes of g rows
 //                    (g = largest power of two <= 128 dividing L/P), each sub-box
 //                    from the fresh or the stale tensor map -- the splice.
@@ -52,29 +63,118 @@ constexpr int KV_STAGES = 5;
 constexpr int TILE_BYTES = KT * D * 2;  // 16 KB (K or V tile, Q tile)
 constexpr int ATTN_THREADS = 384;
 constexpr int NUM_CONVERTERS = 8;       // the softmax warps, a 1/8 share each
-// smem: Q0 Q1 | (K V) x stages | barriers.  TMEM (512 columns): S0 S1 (128 each),
-// O0 O1 (64 each), P0 P1 (64 each: 128 fp16 probabilities per row, two per column).
+// smem: two Q buffers (Q0 Q1 each) | (K V) x stages | barriers.  TMEM (512 columns):
+// S0 S1 (128 each), O0 O1 (64 each), P0 P1 (64 each: 128 fp16 probabilities per row,
+// two per column).
 constexpr int OFF_Q = 0;
-constexpr int OFF_KV = 2 * TILE_BYTES;
+constexpr int OFF_KV = 4 * TILE_BYTES;
 constexpr int OFF_BAR = OFF_KV + KV_STAGES * 2 * TILE_BYTES;
 constexpr int ATTN_SMEM = OFF_BAR + 512 + 1024;
+static_assert(ATTN_SMEM <= 227 * 1024, "shared memory per CTA");
 constexpr float kScaleLog2 = 0.18033688011112042f;  // log2(e) / sqrt(64)
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
+// Partial result of one piece of a cut unit: O/l as fp16 [2 tiles][128 rows][64],
+// then the reference maximum m (log2 units) and the sum l, fp32 [2][128] each.
+constexpr int REC_M = 2 * QT * D * 2;
+constexpr int REC_L = REC_M + 2 * QT * 4;
+constexpr int REC_BYTES = REC_L + 2 * QT * 4;
 
 struct AttnArgs {
-  int L, heads, P, Lp, g, n_qt, n_pairs, nkt;
+  int L, heads, P, Lp, g, n_pairs, nkt;
+  int U;            // units (batch, head, patch, pair of query tiles), pair fastest
+  int G;            // CTAs
+  int W;            // split: whole units per CTA (c, c+G, ...); 0 otherwise
+  int split;        // 1: units W*G .. U-1 are shared key tile by key tile
+  long long tailT;  // split: their (unit, key tile) steps
   __nv_bfloat16* o;
+  uint8_t* part;    // split: G + (U - W*G) partial records
   int* status;
   long long wait_limit;
 };
 
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full[2], q_empty[2];
   uint64_t k_full[KV_STAGES], v_full[KV_STAGES], v_conv[KV_STAGES], kv_empty[KV_STAGES];
   uint64_t s_full[2], p_full[2], o_done[2], drain;
   uint32_t tmem_slot;
   int abort_flag;
 };
+static_assert(sizeof(Bars) <= 512, "barrier area");
+
+// The steps of CTA c: nfull whole units (c, c+G, ...), then the steps [t0, t1) of
+// the shared tail, step = (unit - W*G) * nkt + key tile.
+struct Sched {
+  int nfull, nsteps;
+  long long t0;
+};
+
+__host__ __device__ __forceinline__ long long tail_bound(long long c, const AttnArgs& a) {
+  return c * a.tailT / a.G;
+}
+
+// The CTA whose tail run contains step s (ranges may be empty when tailT < G).
+__host__ __device__ __forceinline__ int tail_cta(long long s, const AttnArgs& a) {
+  return (int)(((s + 1) * a.G - 1) / a.tailT);
+}
+
+__device__ __forceinline__ Sched make_sched(const AttnArgs& a) {
+  Sched s;
+  const int c = blockIdx.x;
+  long long t1 = 0;
+  s.t0 = 0;
+  if (a.split) {
+    s.nfull = a.W;
+    s.t0 = tail_bound(c, a);
+    t1 = tail_bound(c + 1, a);
+  } else {
+    s.nfull = (a.U - c + a.G - 1) / a.G;
+  }
+  s.nsteps = s.nfull * a.nkt + (int)(t1 - s.t0);
+  return s;
+}
+
+// A segment: the run of one unit's key tiles [j0, j0 + len) that this CTA processes
+// from step v on.  Divisions happen once per segment, never inside a step.
+struct Seg {
+  int u, j0, len;
+  bool tail;  // a segment of the shared tail (may be a piece of a cut unit)
+};
+
+__device__ __forceinline__ Seg seg_at(const Sched& s, int v, const AttnArgs& a) {
+  Seg g;
+  const int vf = s.nfull * a.nkt;
+  if (v < vf) {  // v is a multiple of nkt here
+    g.u = (int)blockIdx.x + (v / a.nkt) * a.G;
+    g.j0 = 0;
+    g.len = a.nkt;
+    g.tail = false;
+  } else {
+    const long long tv = s.t0 + (v - vf);
+    const int ut = (int)(tv / a.nkt);
+    g.j0 = (int)(tv - (long long)ut * a.nkt);
+    g.u = a.W * a.G + ut;
+    g.len = min(a.nkt - g.j0, s.nsteps - v);
+    g.tail = true;
+  }
+  return g;
+}
+
+struct UnitPos {
+  int b, h, patch0, q0;  // q0: first query row of the unit within its patch
+};
+
+__host__ __device__ __forceinline__ UnitPos unit_pos(int u, const AttnArgs& a) {
+  UnitPos x;
+  const int pair = u % a.n_pairs;
+  int r = u / a.n_pairs;
+  const int p = r % a.P;
+  r /= a.P;
+  x.h = r % a.heads;
+  x.b = r / a.heads;
+  x.patch0 = p * a.Lp;
+  x.q0 = 2 * pair * QT;
+  return x;
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -90,6 +190,35 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
   return false;
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 16 fp32 values (raw bits, as read from TMEM) scaled by s, as bf16 (two 16-byte stores).
+__device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const uint32_t (&o)[16],
+                                              float s) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    d4[i] = make_uint4(
+        pack_bf16x2(__uint_as_float(o[8 * i]) * s, __uint_as_float(o[8 * i + 1]) * s),
+        pack_bf16x2(__uint_as_float(o[8 * i + 2]) * s, __uint_as_float(o[8 * i + 3]) * s),
+        pack_bf16x2(__uint_as_float(o[8 * i + 4]) * s, __uint_as_float(o[8 * i + 5]) * s),
+        pack_bf16x2(__uint_as_float(o[8 * i + 6]) * s, __uint_as_float(o[8 * i + 7]) * s));
+}
+
+// The same as fp16 (the partial results of cut units).
+__device__ __forceinline__ void store_f16x16(uint4* d4, const uint32_t (&o)[16], float s) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    d4[i] = make_uint4(
+        pack_f16x2(__uint_as_float(o[8 * i]) * s, __uint_as_float(o[8 * i + 1]) * s),
+        pack_f16x2(__uint_as_float(o[8 * i + 2]) * s, __uint_as_float(o[8 * i + 3]) * s),
+        pack_f16x2(__uint_as_float(o[8 * i + 4]) * s, __uint_as_float(o[8 * i + 5]) * s),
+        pack_f16x2(__uint_as_float(o[8 * i + 6]) * s, __uint_as_float(o[8 * i + 7]) * s));
+}
+
 __global__ void __launch_bounds__(ATTN_THREADS, 1)
     tc_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKf,
                    const __grid_constant__ CUtensorMap tmKs, const __grid_constant__ CUtensorMap tmVf,
@@ -99,13 +228,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
                                              ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = blockIdx.x % a.n_pairs;
-  const int p = blockIdx.x / a.n_pairs;
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int patch0 = p * a.Lp;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&bars->q_full, 1);
+    for (int qb = 0; qb < 2; ++qb) {
+      ptx::mbar_init(&bars->q_full[qb], 1);
+      ptx::mbar_init(&bars->q_empty[qb], 1);  // committed after a unit's last Q K^T
+    }
     for (int s = 0; s < KV_STAGES; ++s) {
       ptx::mbar_init(&bars->k_full[s], 1);
       ptx::mbar_init(&bars->v_full[s], 1);
@@ -115,7 +243,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(&bars->s_full[t], 1);
       ptx::mbar_init(&bars->p_full[t], 4);  // one arrival per softmax warp
-      ptx::mbar_init(&bars->o_done[t], 1);  // committed once, after the last P V
+      ptx::mbar_init(&bars->o_done[t], 1);  // committed after a segment's last P V
     }
     ptx::mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -136,44 +264,60 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
-  const int nkt = a.nkt;
+  const Sched sc = make_sched(a);
 
   if (warp >= 8) {
-    // Register split (launch: 384 threads x 168): this warpgroup drops to 64 per
-    // thread, the two softmax warpgroups rise to 208: 128 x 64 + 256 x 208 <= 64512.
-    ptx::regs_dec<64>();
+    // Register split (launch: 384 threads x 168): this warpgroup drops to 80 per
+    // thread, the two softmax warpgroups rise to 208: 128 x 80 + 256 x 208 <= 64512.
+    ptx::regs_dec<80>();
     if (warp == 8) {
       // ---------------------------------------------------------- TMA producer
       if (lane == 0) {
-        int issued = 0;
-        ptx::mbar_arrive_expect_tx(&bars->q_full, 2 * TILE_BYTES);
-        for (int t = 0; t < 2; ++t)
-          ptx::tma_load_3d(smem + OFF_Q + t * TILE_BYTES, &tmQ, &bars->q_full, h * D,
-                           patch0 + (2 * pair + t) * QT, b);
+        int issued = 0, q_issued = 0;
         const int nsub = KT / a.g;
-        for (int j = 0; j < nkt; ++j) {
-          const int st = j % KV_STAGES;
-          if (!wait_or_abort(&bars->kv_empty[st], ((j / KV_STAGES) & 1) ^ 1, a, bars)) break;
-          uint8_t* kdst = smem + OFF_KV + st * 2 * TILE_BYTES;
-          uint8_t* vdst = kdst + TILE_BYTES;
-          ptx::mbar_arrive_expect_tx(&bars->k_full[st], TILE_BYTES);
-          ptx::mbar_arrive_expect_tx(&bars->v_full[st], TILE_BYTES);
-          for (int i = 0; i < nsub; ++i) {
-            const int row = j * KT + i * a.g;
-            const bool fresh = row >= patch0 && row < patch0 + a.Lp;
-            ptx::tma_load_3d(kdst + i * a.g * 128, fresh ? &tmKf : &tmKs, &bars->k_full[st],
-                             h * D, row, b);
+        bool ok = true;
+        for (int v = 0; v < sc.nsteps && ok;) {
+          const Seg sg = seg_at(sc, v, a);
+          const UnitPos up = unit_pos(sg.u, a);
+          {  // Q of this unit into buffer n & 1, once its last user is done
+            const int n = q_issued, qb = n & 1;
+            if (!wait_or_abort(&bars->q_empty[qb], ((n >> 1) & 1) ^ 1, a, bars)) break;
+            ptx::mbar_arrive_expect_tx(&bars->q_full[qb], 2 * TILE_BYTES);
+            for (int t = 0; t < 2; ++t)
+              ptx::tma_load_3d(smem + OFF_Q + (2 * qb + t) * TILE_BYTES, &tmQ, &bars->q_full[qb],
+                               up.h * D, up.patch0 + up.q0 + t * QT, up.b);
+            ++q_issued;
           }
-          for (int i = 0; i < nsub; ++i) {
-            const int row = j * KT + i * a.g;
-            const bool fresh = row >= patch0 && row < patch0 + a.Lp;
-            ptx::tma_load_3d(vdst + i * a.g * 128, fresh ? &tmVf : &tmVs, &bars->v_full[st],
-                             h * D, row, b);
+          for (int j = sg.j0; j < sg.j0 + sg.len; ++j, ++v) {
+            const int st = v % KV_STAGES;
+            if (!wait_or_abort(&bars->kv_empty[st], ((v / KV_STAGES) & 1) ^ 1, a, bars)) {
+              ok = false;
+              break;
+            }
+            uint8_t* kdst = smem + OFF_KV + st * 2 * TILE_BYTES;
+            uint8_t* vdst = kdst + TILE_BYTES;
+            ptx::mbar_arrive_expect_tx(&bars->k_full[st], TILE_BYTES);
+            ptx::mbar_arrive_expect_tx(&bars->v_full[st], TILE_BYTES);
+            for (int i = 0; i < nsub; ++i) {
+              const int row = j * KT + i * a.g;
+              const bool fresh = row >= up.patch0 && row < up.patch0 + a.Lp;
+              ptx::tma_load_3d(kdst + i * a.g * 128, fresh ? &tmKf : &tmKs, &bars->k_full[st],
+                               up.h * D, row, up.b);
+            }
+            for (int i = 0; i < nsub; ++i) {
+              const int row = j * KT + i * a.g;
+              const bool fresh = row >= up.patch0 && row < up.patch0 + a.Lp;
+              ptx::tma_load_3d(vdst + i * a.g * 128, fresh ? &tmVf : &tmVs, &bars->v_full[st],
+                               up.h * D, row, up.b);
+            }
+            ++issued;
           }
-          ++issued;
         }
         if (bars->abort_flag) {  // wait for own copies in flight before exiting
-          ptx::mbar_wait(&bars->q_full, 0, kDrainWaitLimit, nullptr);
+          // a Q load is issued only after the MMAs of the unit two before it have
+          // completed, so only the last two can still be in flight
+          for (int n = q_issued > 2 ? q_issued - 2 : 0; n < q_issued; ++n)
+            ptx::mbar_wait(&bars->q_full[n & 1], (n >> 1) & 1, kDrainWaitLimit, nullptr);
           const int first = issued > KV_STAGES ? issued - KV_STAGES : 0;
           for (int j = first; j < issued; ++j) {
             ptx::mbar_wait(&bars->k_full[j % KV_STAGES], (j / KV_STAGES) & 1, kDrainWaitLimit,
@@ -185,7 +329,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       }
     } else if (warp == 9) {
       // ---------------------------------------------------------- MMA issuer
-      if (lane == 0) {
+      if (lane == 0 && sc.nsteps > 0) {
         constexpr uint32_t idesc_qk = ptx::idesc_f16(QT, KT, 1, 0, 0);
         constexpr uint32_t idesc_pv = ptx::idesc_f16(QT, D, 0, 0, 1);
         // Descriptors are affine in the smem address (address field = bytes >> 4, no
@@ -197,7 +341,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         constexpr uint64_t kStageStep = (2 * TILE_BYTES) >> 4;  // next K/V stage
         constexpr uint64_t kQTile = TILE_BYTES >> 4;            // next query tile
         bool any = false;
-        bool ok = wait_or_abort(&bars->q_full, 0, a, bars) &&
+        bool ok = wait_or_abort(&bars->q_full[0], 0, a, bars) &&
                   wait_or_abort(&bars->k_full[0], 0, a, bars);
         if (ok) {
           ptx::tc_fence_after();
@@ -211,38 +355,51 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           }
           any = true;
         }
-        for (int j = 0; j < nkt && ok; ++j) {
-          const int st = j % KV_STAGES;
-          const bool more = j + 1 < nkt;
-          const uint64_t vd = v_desc + (uint64_t)st * kStageStep;
-          const uint64_t kd = k_desc + (uint64_t)((j + 1) % KV_STAGES) * kStageStep;
-          const uint32_t acc0 = j > 0 ? 1u : 0u;
+        int n = 0;  // segment of step v
+        for (int v = 0; v < sc.nsteps && ok; ++n) {
+          const Seg sg = seg_at(sc, v, a);
+          const int vbeg = v, vend = v + sg.len;
+          for (; v < vend; ++v) {
+            const bool last = v == vend - 1;
+            const bool more = v + 1 < sc.nsteps;
+            const bool new_seg = last && more;  // step v+1 starts another unit
+            const int qn = new_seg ? n + 1 : n;   // segment of step v+1
+            const int st = v % KV_STAGES;
+            const uint64_t vd = v_desc + (uint64_t)st * kStageStep;
+            const uint64_t kd = k_desc + (uint64_t)((v + 1) % KV_STAGES) * kStageStep;
+            const uint64_t qd = q_desc + (uint64_t)(qn & 1) * 2 * kQTile;
+            const uint32_t acc0 = v > vbeg ? 1u : 0u;
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (!wait_or_abort(&bars->p_full[t], j & 1, a, bars) ||
-                (t == 0 && !wait_or_abort(&bars->v_conv[st], (j / KV_STAGES) & 1, a, bars)) ||
-                (t == 0 && more &&
-                 !wait_or_abort(&bars->k_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1, a,
-                                bars))) {
-              ok = false;
-              break;
+            for (int t = 0; t < 2; ++t) {
+              if (!wait_or_abort(&bars->p_full[t], v & 1, a, bars) ||
+                  (t == 0 && !wait_or_abort(&bars->v_conv[st], (v / KV_STAGES) & 1, a, bars)) ||
+                  (t == 0 && more &&
+                   !wait_or_abort(&bars->k_full[(v + 1) % KV_STAGES], ((v + 1) / KV_STAGES) & 1,
+                                  a, bars)) ||
+                  (t == 0 && new_seg &&
+                   !wait_or_abort(&bars->q_full[qn & 1], (qn >> 1) & 1, a, bars))) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              const uint32_t tO = tmem + 256u + 64u * t, tP = tmem + 384u + 64u * t;
+#pragma unroll
+              for (int k = 0; k < KT / 16; ++k)  // O_t += P_t(v) V(v)
+                ptx::mma_ts(tO, tP + k * 8, vd + 128 * k, idesc_pv, k ? 1u : acc0);
+              if (last) ptx::mma_commit(&bars->o_done[t]);
+              if (more) {  // S_t = Q_t K(v+1)^T, Q of the unit of step v+1
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+                  ptx::mma_ss(tmem + 128u * t, qd + t * kQTile + 2 * k, kd + 2 * k, idesc_qk,
+                              k ? 1u : 0u);
+                ptx::mma_commit(&bars->s_full[t]);
+              }
             }
-            ptx::tc_fence_after();
-            const uint32_t tO = tmem + 256u + 64u * t, tP = tmem + 384u + 64u * t;
-#pragma unroll
-            for (int k = 0; k < KT / 16; ++k)  // O_t += P_t(j) V(j)
-              ptx::mma_ts(tO, tP + k * 8, vd + 128 * k, idesc_pv, k ? 1u : acc0);
-            if (more) {                         // S_t = Q_t K(j+1)^T
-#pragma unroll
-              for (int k = 0; k < D / 16; ++k)
-                ptx::mma_ss(tmem + 128u * t, q_desc + t * kQTile + 2 * k, kd + 2 * k, idesc_qk,
-                            k ? 1u : 0u);
-              ptx::mma_commit(&bars->s_full[t]);
-            } else {
-              ptx::mma_commit(&bars->o_done[t]);
-            }
+            if (!ok) break;
+            ptx::mma_commit(&bars->kv_empty[st]);
+            // after a unit's last step every Q K^T of it has been issued: free its Q buffer
+            if (last) ptx::mma_commit(&bars->q_empty[n & 1]);
           }
-          if (ok) ptx::mma_commit(&bars->kv_empty[st]);
         }
         if (!ok && any) {  // let issued MMAs finish before TMEM is released
           ptx::mma_commit(&bars->drain);
@@ -261,11 +418,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     const uint32_t tS = tmem + 128u * (uint32_t)t;        // S_t: 128 columns
     const uint32_t tO = tmem + 256u + 64u * (uint32_t)t;  // O_t: 64 columns
     const uint32_t tP = tmem + 384u + 64u * (uint32_t)t;  // P_t: 64 columns
-    float m_ref = -INFINITY, l = 0.f;
-    // Widens this warp's 1/8 share of V(jj) in place once the tile has landed.
-    auto convert_share = [&](int jj) -> bool {
-      const int st = jj % KV_STAGES;
-      const uint32_t par = (jj / KV_STAGES) & 1;
+    // Widens this warp's 1/8 share of the V tile of step vv in place once it has landed.
+    auto convert_share = [&](int vv) -> bool {
+      const int st = vv % KV_STAGES;
+      const uint32_t par = (vv / KV_STAGES) & 1;
       // lane 0 sleeps on the barrier; then every lane observes the completed phase
       // (returns at once) so that all lanes see the landed tile
       int okw = 1;
@@ -281,11 +437,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       for (int i = 0; i < 4; ++i) {
         uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
-          __half2 hv = __floats2half2_rn(lo, hi);
-          w[e] = *reinterpret_cast<uint32_t*>(&hv);
-        }
+        for (int e = 0; e < 4; ++e)
+          w[e] = pack_f16x2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
         v[lane + 32 * i] = make_uint4(w[0], w[1], w[2], w[3]);
       }
       ptx::fence_proxy_async_smem();
@@ -293,111 +446,122 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       if (lane == 0) ptx::mbar_arrive(&bars->v_conv[st]);
       return true;
     };
-    bool ok = convert_share(0);
-    for (int j = 0; j < nkt && ok; ++j) {
-      if (j + 1 < nkt && !convert_share(j + 1)) { ok = false; break; }
-      // S_t(j) ready; the MMA thread issued it after P_t(j-1) V(j-1), so that
-      // product has completed too: P_t and O_t may be touched.
-      if (!wait_or_abort(&bars->s_full[t], j & 1, a, bars)) { ok = false; break; }
-      ptx::tc_fence_after();
-      uint32_t s[128];
+    bool ok = sc.nsteps == 0 || convert_share(0);
+    bool tail_seen = false;  // a tail segment of this CTA has ended
+    for (int v = 0, n = 0; v < sc.nsteps && ok; ++n) {
+      const Seg sg = seg_at(sc, v, a);
+      const int vbeg = v, vend = v + sg.len;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = sg.j0; v < vend; ++v, ++j) {
+        if (v + 1 < sc.nsteps && !convert_share(v + 1)) { ok = false; break; }
+        // S_t(v) ready; the MMA thread issued it after P_t(v-1) V(v-1), so that
+        // product has completed too: P_t and O_t may be touched.
+        if (!wait_or_abort(&bars->s_full[t], v & 1, a, bars)) { ok = false; break; }
+        ptx::tc_fence_after();
+        uint32_t sv[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        ptx::tmem_ld32(tS + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
-      ptx::tmem_ld_wait();
-      const int nvalid = a.L - j * KT;
-      if (nvalid < KT) {  // only the last key tile can be partial: mask keys >= L
+        for (int c = 0; c < 4; ++c)
+          ptx::tmem_ld32(tS + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+        ptx::tmem_ld_wait();
+        const int nvalid = a.L - j * KT;
+        if (nvalid < KT) {  // only the last key tile can be partial: mask keys >= L
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= nvalid) s[i] = __float_as_uint(-INFINITY);
-      }
-      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 independent chains
+          for (int i = 0; i < 128; ++i)
+            if (i >= nvalid) sv[i] = __float_as_uint(-INFINITY);
+        }
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 independent chains
 #pragma unroll
-      for (int i = 0; i < 128; i += 8) {
+        for (int i = 0; i < 128; i += 8) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          mq[u] = ptx::max3(mq[u], __uint_as_float(s[i + 2 * u]), __uint_as_float(s[i + 2 * u + 1]));
-      }
-      const float mx = ptx::max3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
-      const float m_new = mx * kScaleLog2;
-      const bool resc = m_new > m_ref + kRescaleThreshold;
-      float alpha = 1.f;
-      if (resc) {
-        alpha = ex2(m_ref - m_new);  // 0 on the first tile
-        m_ref = m_new;
-        l *= alpha;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {  // rescale the running O_t
+          for (int u = 0; u < 4; ++u)
+            mq[u] = ptx::max3(mq[u], __uint_as_float(sv[i + 2 * u]),
+                              __uint_as_float(sv[i + 2 * u + 1]));
+        }
+        const float mx = ptx::max3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+        const float m_new = mx * kScaleLog2;
+        const bool resc = m_new > m_ref + kRescaleThreshold;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2(m_ref - m_new);  // 0 on the first tile of a segment
+          m_ref = m_new;
+          l *= alpha;
+        }
+        if (v > vbeg && __any_sync(0xffffffffu, resc)) {  // rescale the running O_t
 #pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[16];
+            ptx::tmem_ld16(tO + lane_off + c * 16, o);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            ptx::tmem_st16(tO + lane_off + c * 16, o);
+          }
+        }
+        // exponentials 32 keys at a time, stored at once as fp16 P into TMEM (column c
+        // holds keys 2c in the low half and 2c+1 in the high half)
+        // pairs of keys in packed fp32x2: one FMA and one add per two keys
+        const uint64_t c2 = ptx::pack_f32x2(kScaleLog2, kScaleLog2);
+        const uint64_t nm2 = ptx::pack_f32x2(-m_ref, -m_ref);
+        uint64_t lq[2] = {ptx::pack_f32x2(0.f, 0.f), ptx::pack_f32x2(0.f, 0.f)};  // row sums
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint64_t s2 = ptx::pack_f32x2(__uint_as_float(sv[32 * c + 2 * i]),
+                                                __uint_as_float(sv[32 * c + 2 * i + 1]));
+            float a0, a1;
+            ptx::unpack_f32x2(ptx::fma_f32x2(s2, c2, nm2), a0, a1);
+            const float p0 = ex2(a0), p1 = ex2(a1);
+            lq[i & 1] = ptx::add_f32x2(lq[i & 1], ptx::pack_f32x2(p0, p1));
+            pk[i] = pack_f16x2(p0, p1);
+          }
+          ptx::tmem_st16(tP + lane_off + 16 * c, pk);
+        }
+        {
+          float x0, x1, y0, y1;
+          ptx::unpack_f32x2(lq[0], x0, x1);
+          ptx::unpack_f32x2(lq[1], y0, y1);
+          l += (x0 + x1) + (y0 + y1);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->p_full[t]);
+      }
+      if (!ok) break;
+      // ---- end of the segment: O_t complete once its last P V has finished
+      if (!wait_or_abort(&bars->o_done[t], n & 1, a, bars)) { ok = false; break; }
+      ptx::tc_fence_after();
+      const UnitPos up = unit_pos(sg.u, a);
+      const float inv = 1.f / l;
+      if (sg.j0 == 0 && sg.len == a.nkt) {  // whole unit: normalised bf16 output
+        const int row_in_patch = up.q0 + t * QT + r;
+        const bool valid = row_in_patch < a.Lp;
+        __nv_bfloat16* dst = a.o + ((long long)up.b * a.L + up.patch0 + row_in_patch) *
+                                       (long long)(a.heads * D) + up.h * D;
+#pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[16];
           ptx::tmem_ld16(tO + lane_off + c * 16, o);
           ptx::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          ptx::tmem_st16(tO + lane_off + c * 16, o);
+          if (valid) store_bf16x16(dst + c * 16, o, inv);
         }
-      }
-      // exponentials 32 keys at a time, stored at once as fp16 P into TMEM (column c
-      // holds keys 2c in the low half and 2c+1 in the high half)
-      // pairs of keys in packed fp32x2: one FMA and one add per two keys
-      const uint64_t c2 = ptx::pack_f32x2(kScaleLog2, kScaleLog2);
-      const uint64_t nm2 = ptx::pack_f32x2(-m_ref, -m_ref);
-      uint64_t lq[2] = {ptx::pack_f32x2(0.f, 0.f), ptx::pack_f32x2(0.f, 0.f)};  // row sums
+      } else {  // one piece of a cut unit: O/l in fp16, m and l in fp32
+        const int rec = tail_seen ? a.G + (sg.u - a.W * a.G) : (int)blockIdx.x;
+        uint8_t* base = a.part + (size_t)rec * REC_BYTES;
+        uint4* dst = reinterpret_cast<uint4*>(base + ((size_t)(t * QT + r) * D) * 2);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint64_t sv = ptx::pack_f32x2(__uint_as_float(s[32 * c + 2 * i]),
-                                              __uint_as_float(s[32 * c + 2 * i + 1]));
-          float a0, a1;
-          ptx::unpack_f32x2(ptx::fma_f32x2(sv, c2, nm2), a0, a1);
-          const float p0 = ex2(a0), p1 = ex2(a1);
-          lq[i & 1] = ptx::add_f32x2(lq[i & 1], ptx::pack_f32x2(p0, p1));
-          __half2 hv = __floats2half2_rn(p0, p1);
-          pk[i] = *reinterpret_cast<uint32_t*>(&hv);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[16];
+          ptx::tmem_ld16(tO + lane_off + c * 16, o);
+          ptx::tmem_ld_wait();
+          store_f16x16(dst + 2 * c, o, inv);
         }
-        ptx::tmem_st16(tP + lane_off + 16 * c, pk);
+        reinterpret_cast<float*>(base + REC_M)[t * QT + r] = m_ref;
+        reinterpret_cast<float*>(base + REC_L)[t * QT + r] = l;
       }
-      {
-        float x0, x1, y0, y1;
-        ptx::unpack_f32x2(lq[0], x0, x1);
-        ptx::unpack_f32x2(lq[1], y0, y1);
-        l += (x0 + x1) + (y0 + y1);
-      }
-      ptx::tmem_st_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars->p_full[t]);
-    }
-    if (ok && wait_or_abort(&bars->o_done[t], 0, a, bars)) {
-      ptx::tc_fence_after();
-      const int row_in_patch = (2 * pair + t) * QT + r;
-      const bool valid = row_in_patch < a.Lp;
-      const float inv = 1.f / l;
-      __nv_bfloat16* dst =
-          a.o + ((long long)b * a.L + patch0 + row_in_patch) * (long long)(a.heads * D) + h * D;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[16];
-        ptx::tmem_ld16(tO + lane_off + c * 16, o);
-        ptx::tmem_ld_wait();
-        if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 16);
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            d4[i] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * i]) * inv,
-                                           __uint_as_float(o[8 * i + 1]) * inv),
-                               pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv,
-                                           __uint_as_float(o[8 * i + 3]) * inv),
-                               pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv,
-                                           __uint_as_float(o[8 * i + 5]) * inv),
-                               pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv,
-                                           __uint_as_float(o[8 * i + 7]) * inv));
-          }
-        }
-      }
+      if (sg.tail) tail_seen = true;
     }
   }
   ptx::tc_fence_before();
@@ -406,6 +570,79 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
+}
+
+// Merges the pieces of each cut tail unit (one CTA per tail unit; units not cut
+// return at once).  Thread = (query tile, row).  With pieces i = (m_i, l_i, O_i/l_i):
+// M = max m_i, w_i = l_i 2^(m_i - M), o = sum_i w_i (O_i/l_i) / sum_i w_i, summed in
+// the order of the CTAs.
+constexpr int kMaxPieces = 256;
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+  __shared__ int recs[kMaxPieces];
+  __shared__ int warp_count[8];
+  const int ut = blockIdx.x;
+  const long long s_a = (long long)ut * a.nkt, s_b = s_a + a.nkt - 1;
+  const int ca = tail_cta(s_a, a), cb = tail_cta(s_b, a);
+  if (ca == cb) return;
+  // the unit's records in CTA order (CTAs whose run is empty hold none): thread i looks
+  // at CTA ca + i, a ballot per warp gives each record its place in the list
+  const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
+  const int c = ca + i;
+  const bool has = c <= cb && tail_bound(c, a) != tail_bound(c + 1, a);
+  const unsigned ball = __ballot_sync(0xffffffffu, has);
+  if (lane == 0) warp_count[warp] = __popc(ball);
+  __syncthreads();
+  int pos = __popc(ball & ((1u << lane) - 1u)), np = 0;
+  for (int w = 0; w < 8; ++w) {
+    if (w < warp) pos += warp_count[w];
+    np += warp_count[w];
+  }
+  if (has) recs[pos] = (c == ca && tail_bound(c, a) != s_a) ? a.G + ut : c;
+  __syncthreads();
+  const int t = i >> 7, r = i & 127;
+  auto rec_f = [&](int k, int off) {
+    return reinterpret_cast<const float*>(a.part + (size_t)recs[k] * REC_BYTES + off)[t * QT + r];
+  };
+  float M = -INFINITY;
+#pragma unroll 4
+  for (int k = 0; k < np; ++k) M = fmaxf(M, rec_f(k, REC_M));
+  float acc[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) acc[d] = 0.f;
+  float wsum = 0.f;
+#pragma unroll 2
+  for (int k = 0; k < np; ++k) {
+    const float w = rec_f(k, REC_L) * exp2f(rec_f(k, REC_M) - M);
+    wsum += w;
+    const uint4* src = reinterpret_cast<const uint4*>(a.part + (size_t)recs[k] * REC_BYTES +
+                                                      ((size_t)(t * QT + r) * D) * 2);
+    uint4 u[D / 8];
+#pragma unroll
+    for (int q = 0; q < D / 8; ++q) u[q] = src[q];
+#pragma unroll
+    for (int q = 0; q < D / 8; ++q) {
+      const uint32_t hw[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[e]));
+        acc[8 * q + 2 * e] = fmaf(w, f.x, acc[8 * q + 2 * e]);
+        acc[8 * q + 2 * e + 1] = fmaf(w, f.y, acc[8 * q + 2 * e + 1]);
+      }
+    }
+  }
+  const UnitPos up = unit_pos(a.W * a.G + ut, a);
+  const int row_in_patch = up.q0 + t * QT + r;
+  if (row_in_patch >= a.Lp) return;
+  __nv_bfloat16* dst =
+      a.o + ((long long)up.b * a.L + up.patch0 + row_in_patch) * (long long)(a.heads * D) + up.h * D;
+  const float inv = 1.f / wsum;
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < D / 8; ++q)
+    d4[q] = make_uint4(pack_bf16x2(acc[8 * q] * inv, acc[8 * q + 1] * inv),
+                       pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
+                       pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv),
+                       pack_bf16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
 }
 
 bool make_map3(CUtensorMap* m, const void* base, int L, int B, int C, int box_rows) {
@@ -431,33 +668,77 @@ int set_attn_smem() {
   return rc;
 }
 
-}  // namespace
-
-int launch_tc_attention(const void* q, const void* kf, const void* vf, const void* ks,
-                        const void* vs, void* o, int B, int L, int heads, int P, int* status,
-                        long long wait_limit, cudaStream_t s) {
+// Schedule of one launch; false if the shape is not supported.
+bool plan(int B, int L, int heads, int P, bool split, AttnArgs* a) {
+  if (B <= 0 || L <= 0 || heads <= 0 || P <= 0 || L % P) return false;
   const int Lp = L / P;
-  if (L % P || Lp % 8) return DPP_ERR_SHAPE;
+  if (Lp % 8) return false;
   int g = 128;
   while (Lp % g) g >>= 1;
+  *a = AttnArgs{};
+  a->L = L; a->heads = heads; a->P = P; a->Lp = Lp; a->g = g;
+  a->n_pairs = ((Lp + QT - 1) / QT + 1) / 2;
+  a->nkt = (L + KT - 1) / KT;
+  const long long U = (long long)B * heads * P * a->n_pairs;
+  if (U * a->nkt > (1ll << 31) - 1) return false;
+  a->U = (int)U;
+  // at most kMaxPieces CTAs, so that a cut unit has at most that many pieces
+  const int sms = dpp_host::sm_count() < kMaxPieces ? dpp_host::sm_count() : kMaxPieces;
+  if (split) {
+    const long long T = U * a->nkt;
+    a->G = (int)(T < sms ? T : sms);
+    a->W = a->U / a->G;
+    // The last full round joins the leftover units in the shared tail: each CTA's
+    // tail run is then longer than a unit, so a cut unit has at most two pieces
+    // (one short merge per unit instead of a long chain).
+    if (a->U % a->G && a->W > 0) --a->W;
+    a->tailT = (long long)(a->U - a->W * a->G) * a->nkt;
+    a->split = a->U % a->G != 0;
+    if (!a->split) {
+      a->W = 0;
+      a->tailT = 0;
+    }
+  } else {
+    a->G = (int)(U < sms ? U : sms);
+  }
+  return true;
+}
+
+}  // namespace
+
+size_t tc_attention_partial_bytes(int B, int L, int heads, int P) {
+  AttnArgs a;
+  if (!plan(B, L, heads, P, true, &a) || !a.split) return 0;
+  return (size_t)(a.G + (a.U - a.W * a.G)) * REC_BYTES;
+}
+
+int tc_attention_kernel_count(int B, int L, int heads, int P, bool split) {
+  AttnArgs a;
+  if (!plan(B, L, heads, P, split, &a)) return 0;
+  return a.split ? 2 : 1;
+}
+
+int launch_tc_attention(const void* q, const void* kf, const void* vf, const void* ks,
+                        const void* vs, void* o, int B, int L, int heads, int P, void* partials,
+                        size_t partial_bytes, int* status, long long wait_limit, cudaStream_t s) {
+  AttnArgs a;
+  if (!plan(B, L, heads, P, partials != nullptr, &a)) return DPP_ERR_SHAPE;
+  if (a.split && partial_bytes < (size_t)(a.G + (a.U - a.W * a.G)) * REC_BYTES)
+    return DPP_ERR_ARG;
   const int C = heads * D;
   int rc = set_attn_smem();
   if (rc) return rc;
   CUtensorMap mq, mkf, mks, mvf, mvs;
-  if (!make_map3(&mq, q, L, B, C, QT) || !make_map3(&mkf, kf, L, B, C, g) ||
-      !make_map3(&mks, ks, L, B, C, g) || !make_map3(&mvf, vf, L, B, C, g) ||
-      !make_map3(&mvs, vs, L, B, C, g))
+  if (!make_map3(&mq, q, L, B, C, QT) || !make_map3(&mkf, kf, L, B, C, a.g) ||
+      !make_map3(&mks, ks, L, B, C, a.g) || !make_map3(&mvf, vf, L, B, C, a.g) ||
+      !make_map3(&mvs, vs, L, B, C, a.g))
     return DPP_ERR_CUDA;
-  AttnArgs a{};
-  a.L = L; a.heads = heads; a.P = P; a.Lp = Lp; a.g = g;
-  a.n_qt = (Lp + QT - 1) / QT;
-  a.n_pairs = (a.n_qt + 1) / 2;
-  a.nkt = (L + KT - 1) / KT;
   a.o = static_cast<__nv_bfloat16*>(o);
+  a.part = static_cast<uint8_t*>(partials);
   a.status = status;
   a.wait_limit = wait_limit;
-  dim3 grid(a.n_pairs * P, heads, B);
-  tc_attn_kernel<<<grid, ATTN_THREADS, ATTN_SMEM, s>>>(mq, mkf, mks, mvf, mvs, a);
+  tc_attn_kernel<<<a.G, ATTN_THREADS, ATTN_SMEM, s>>>(mq, mkf, mks, mvf, mvs, a);
+  if (a.split) attn_combine_kernel<<<a.U - a.W * a.G, 256, 0, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
 

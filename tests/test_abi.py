@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import stale_activations_gb300 as dpp
 from stale_activations_gb300 import build as dbuild
@@ -56,8 +57,14 @@ def test_workspace_layout_sizes(lib):
     lo = dpp.workspace_layout(prm)
     act = 2 * 64 * 64 * 640 * 2
     assert lo.total >= 6 * act
-    offs = [lo.status, lo.gn_partial, lo.gn_fresh, lo.y, lo.h, lo.q, lo.k, lo.v, lo.o]
+    offs = [lo.status, lo.gn_partial, lo.gn_fresh, lo.y, lo.h, lo.q, lo.k, lo.v, lo.o,
+            lo.attn_partial]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    # 320 attention units on (without a GPU, the library assumes) 152 SMs: one round of
+    # 152 whole units, the other 168 shared; partial records: 152 + 168 of 34816 bytes
+    part = dpp.attention_partials_size(2, 4096, 10, 4)
+    assert part == (152 + 168) * 34816 or torch.cuda.is_available()
+    assert lo.attn_partial_bytes == part and lo.total >= lo.attn_partial + part
     n, nb = dpp.message_sizes(prm)
     blc = 2 * 4096 * 640
     assert n == 2 * blc + 2 * 3 * 2 * 64 * 640
@@ -96,6 +103,16 @@ def test_host_checks_without_launch(lib):
     assert lib.stale_kv_attention(a, a, a, a, a, a, 1, 1000, 2, 64, 3, dpp.BF16, None, None) == 2
     assert lib.stale_kv_attention(a, a, a, a, a, vp(8), 1, 1024, 2, 64, 2, dpp.BF16, None,
                                   None) == 3
+    # split schedule: a missing or short partials buffer is refused before any launch
+    need = lib.dpp_attention_partials_size(1, 1024, 2, 64, 4, dpp.BF16)
+    assert need > 0
+    assert lib.stale_kv_attention_split(a, a, a, a, a, a, 1, 1024, 2, 64, 4, dpp.BF16, None, 0,
+                                        None, None) == 9
+    assert lib.stale_kv_attention_split(a, a, a, a, a, a, 1, 1024, 2, 64, 4, dpp.BF16, a,
+                                        need - 1, None, None) == 9
+    assert lib.stale_kv_attention_split(a, a, a, a, a, a, 1, 1024, 2, 64, 4, dpp.BF16, vp(264),
+                                        need, None, None) == 3
+    assert lib.dpp_attention_partials_size(1, 1000, 2, 64, 3, dpp.BF16) == 0  # invalid shape
     prm = _params()
     w = dpp.LayerWeights()
     st = dpp.LayerState()

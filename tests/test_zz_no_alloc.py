@@ -3,7 +3,7 @@ device memory when they run a layer (a plugin whose host framework owns every
 byte of device memory through its own allocator, a latency-critical loop where
 cudaMalloc's implicit synchronisation is not allowed).
 
-It takes its workspace from a fixed 64 MiB device array inside the library, so
+It takes its workspace from a fixed 80 MiB device array inside the library, so
 its results must match patch_layer_step with a caller-allocated workspace, call
 after call.  This file is collected last on purpose.
 """
@@ -25,7 +25,7 @@ def _fresh_state_pair(prm):
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
-    cfg = synth.SDXL1024_MID  # the bench workload: about 60 MiB of workspace
+    cfg = synth.SDXL1024_MID  # the bench workload: about 71 MiB of workspace
     prm = dpp.make_params(cfg.B, cfg.H, cfg.W, cfg.C, cfg.P, cfg.G, cfg.heads, dpp.BF16,
                           refresh=True, eps=cfg.eps)
     wts = {k: v.cuda() for k, v in synth.layer_weights(cfg, seed=5, affine=True).items()}
@@ -49,7 +49,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
 def test_noalloc_rejects_layers_beyond_the_scratch():
     lib = dpp.load(build_if_missing=True)
     prm = dpp.make_params(2, 128, 128, 640, 4, 32, 10, dpp.BF16)  # ~240 MiB of workspace
-    assert dpp.workspace_size(prm) > 64 * 1024 * 1024
+    assert dpp.workspace_size(prm) > 80 * 1024 * 1024
     rc = lib.patch_layer_step_noalloc(ctypes.byref(prm), ctypes.byref(dpp.LayerWeights()),
                                       ctypes.byref(dpp.LayerState()), ctypes.c_void_p(256),
                                       ctypes.c_void_p(256), dpp.STALE, None)
