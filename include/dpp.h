@@ -98,8 +98,8 @@ int refresh_residual(const void* fresh, void* stale, int8_t* codes, float* scale
  * for rows r0-1 and r1, and 0 outside the image (rows < 0, >= H; cols < 0, >= W).
  * y_fresh, y_stale: [B,H,W,Cin]; w: [Cout,3,3,Cin]; out: [B,H,W,Cout]; all `dtype`.
  * With y_stale == y_fresh the result is the unbanded convolution.
- * Requires H % P == 0.  DPP_BF16 also requires Cin % 64 == 0, Cout % 128 == 0,
- * W % 128 == 0 or 128 % W == 0, and (H/P)*W % 128 == 0.
+ * Requires H % P == 0.  DPP_BF16 also requires Cin % 64 == 0, Cout a multiple of
+ * 128 or of 160, W % 128 == 0 or 128 % W == 0, and (H/P)*W % 128 == 0.
  * dev_status: device int (may be NULL) that receives a give-up code.
  */
 int halo_conv3x3(const void* y_fresh, const void* y_stale, const void* w, void* out,

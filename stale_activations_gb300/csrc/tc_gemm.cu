@@ -1,13 +1,13 @@
 // tcgen05 GEMM engine for the bf16 path: the Q/K/V and output projections, and
 // the halo conv3x3 as an implicit GEMM (M = B*H*W pixels, N = Cout, K = 9*Cin).
 //
-// Persistent: one CTA per SM walks output tiles of 128 x BN (BN = 256, 160 or
-// 128, the largest that divides N).  Warp 0 streams 64-wide K slices of A and B
-// into a shared-memory ring with TMA (128-byte swizzle); warp 1 issues
-// tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM accumulators and releases
-// each stage with tcgen05.commit; warps 2-5 drain the other accumulator
-// (tcgen05.ld -> bf16 -> global), so a tile's epilogue overlaps the next tile's
-// main loop.
+// Persistent: one CTA per SM walks output tiles of 128 x BN (BN = 320, 256, 160
+// or 128, chosen per shape by pick_bn).  Warp 0 streams 64-wide K slices of A and
+// B into a shared-memory ring with TMA (128-byte swizzle); warp 1 issues
+// tcgen05.mma (M=128, K=16; one MMA of N=BN, or two of N=BN/2 for BN=320) and
+// releases each stage with tcgen05.commit; warps 2-5 drain the accumulator
+// (tcgen05.ld -> bf16 -> global).  With two TMEM accumulators (BN <= 256) a
+// tile's epilogue overlaps the next tile's main loop.
 //
 // Halo conv staging ("Benchmarking DistVAE", Glossary: the halo rows a sharded
 // convolution needs; "OTIL for SDXL on 4x L40S", item 3: the conv halo buffers
@@ -30,14 +30,21 @@ namespace {
 constexpr int BM = 128, BK = 64;
 constexpr int GEMM_THREADS = 192;
 
+constexpr int kMaxDynSmem = 227 * 1024;
+
 template <int BN>
 struct Cfg {
+  static constexpr int MMA_N = BN > 256 ? BN / 2 : BN;  // N of one MMA (<= 256)
+  static constexpr int NMMA = BN / MMA_N;               // MMAs per K step
+  static constexpr int NACC = 2 * BN <= 512 ? 2 : 1;    // TMEM accumulators
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-  static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
+  static constexpr int STAGES = (kMaxDynSmem - 1024 /*align*/ - 256 /*barriers*/) / STAGE_BYTES;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr uint32_t TMEM_COLS = NACC * BN <= 256 ? 256 : 512;
+  static_assert(BN % MMA_N == 0 && MMA_N % 16 == 0 && MMA_N <= 256, "MMA shape");
+  static_assert(SMEM <= kMaxDynSmem && STAGES >= 2, "shared memory");
 };
 
 struct GemmArgs {
@@ -63,8 +70,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;   // [2] MMA -> epilogue
-  uint64_t* acc_empty = acc_full + 2;    // [2] epilogue -> MMA (4 warps)
+  uint64_t* acc_full = empty + STAGES;   // [NACC] MMA -> epilogue
+  uint64_t* acc_empty = acc_full + 2;    // [NACC] epilogue -> MMA (4 warps)
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -77,7 +84,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NACC; ++b) {
       ptx::mbar_init(&acc_full[b], 1);
       ptx::mbar_init(&acc_empty[b], 4);
     }
@@ -147,7 +154,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           } else {
             ptx::tma_load_2d(a_dst, &tmA, &full[s], kb * BK, (int)m0);
           }
-          ptx::tma_load_2d(b_dst, &tmB, &full[s], kb * BK, n0);
+#pragma unroll
+          for (int h = 0; h < C::NMMA; ++h)
+            ptx::tma_load_2d(b_dst + h * C::MMA_N * 128, &tmB, &full[s], kb * BK,
+                             n0 + h * C::MMA_N);
         }
       }
       if (*abort_flag) {  // wait for own copies still in flight before the CTA may exit
@@ -160,13 +170,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_f16(BM, BN, 1, 0, 0);
+      constexpr uint32_t idesc = ptx::idesc_f16(BM, C::MMA_N, 1, 0, 0);
       bool any = false, ok = true;
       long long g = 0;
       int it = 0;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
-        const int ab = it & 1;
-        if (!ptx::mbar_wait(&acc_empty[ab], ((it >> 1) & 1) ^ 1, args.wait_limit, abort_flag)) {
+        const int ab = it % C::NACC;
+        if (!ptx::mbar_wait(&acc_empty[ab], ((it / C::NACC) & 1) ^ 1, args.wait_limit,
+                            abort_flag)) {
           set_status(args.status, DPP_ERR_TIMEOUT);
           *abort_flag = 1;
           break;
@@ -187,8 +198,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const uint32_t b_addr = a_addr + C::A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            ptx::mma_ss(d_tmem, ptx::sw128_desc(a_addr + k * 32, 16, 1024),
-                        ptx::sw128_desc(b_addr + k * 32, 16, 1024), idesc, (kb | k) ? 1u : 0u);
+#pragma unroll
+            for (int h = 0; h < C::NMMA; ++h)
+              ptx::mma_ss(d_tmem + h * C::MMA_N, ptx::sw128_desc(a_addr + k * 32, 16, 1024),
+                          ptx::sw128_desc(b_addr + h * C::MMA_N * 128 + k * 32, 16, 1024), idesc,
+                          (kb | k) ? 1u : 0u);
           any = true;
           ptx::mma_commit(&empty[s]);
         }
@@ -204,8 +218,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
     int it = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
-      const int ab = it & 1;
-      if (!ptx::mbar_wait(&acc_full[ab], (it >> 1) & 1, args.wait_limit, abort_flag)) {
+      const int ab = it % C::NACC;
+      if (!ptx::mbar_wait(&acc_full[ab], (it / C::NACC) & 1, args.wait_limit, abort_flag)) {
         set_status(args.status, DPP_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
@@ -216,7 +230,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int n0 = nt * BN;
       const int which = n0 / args.ncols;
       const int col0 = n0 - which * args.ncols;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.out[which]) + row * args.ncols + col0;
+      // select, not index: a run-time index into the parameter struct would copy it
+      // to local memory
+      void* const obase = which == 0 ? args.out[0] : which == 1 ? args.out[1] : args.out[2];
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(obase) + row * args.ncols + col0;
       const uint32_t t_base = tmem + ab * BN + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
@@ -294,12 +311,22 @@ int prepare() {
   return rc;
 }
 
-int pick_bn(int N, int ncols) {
-  // the tile must not straddle two of the split outputs
+// Tile width for an M x N x (nkb * 64) GEMM.  Measured on the GB300 at the layer's
+// sizes, the time per K slice is nearly the same for 36 KB and 56 KB stages (the
+// ring's latency, not its bytes, sets it), so the 128 x 320 tile (two MMAs per K
+// step, one accumulator) does twice the work per slice: it halved the SDXL-1024
+// conv (K = 5760, 90 slices).  With one accumulator its epilogue (~3 us) is not
+// overlapped, which costs more than it saves for the K = 640 projections (10
+// slices), so it is taken only for long K loops; otherwise the widest of 256 / 160
+// / 128 that divides N, with two accumulators.
+int pick_bn(int N, int ncols, int nkb) {
+  if (nkb >= 32 && N % 320 == 0 && ncols % 320 == 0) return 320;
   for (int bn : {256, 160, 128})
-    if (N % bn == 0 && ncols % bn == 0) return bn;
+    if (N % bn == 0 && ncols % bn == 0) return bn;  // no tile straddles two split outputs
   return 0;
 }
+
+constexpr int mma_n(int bn) { return bn > 256 ? bn / 2 : bn; }
 
 template <bool CONV, int BN>
 int launch(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, GemmArgs g,
@@ -317,6 +344,7 @@ template <bool CONV>
 int dispatch(int bn, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
              const GemmArgs& g, cudaStream_t s) {
   switch (bn) {
+    case 320: return launch<CONV, 320>(ta, ta2, tb, g, s);
     case 256: return launch<CONV, 256>(ta, ta2, tb, g, s);
     case 160: return launch<CONV, 160>(ta, ta2, tb, g, s);
     case 128: return launch<CONV, 128>(ta, ta2, tb, g, s);
@@ -331,7 +359,7 @@ bool tc_linear_supported(long long M, int C) {
 }
 
 bool tc_conv_supported(int B, int H, int W, int Cin, int Cout, int P) {
-  if (Cin % BK || Cout % 128) return false;
+  if (Cin % BK || Cin <= 0 || Cout <= 0 || !pick_bn(Cout, Cout, 9 * Cin / BK)) return false;
   if (!(W % 128 == 0 || (128 % W == 0 && W >= 8))) return false;
   if (((long long)(H / P) * W) % BM) return false;
   (void)B;
@@ -342,13 +370,13 @@ int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2,
                      int N, int K, int* status, long long wait_limit, cudaStream_t s) {
   if (M % BM || N % 128 || K % BK) return DPP_ERR_SHAPE;
   const int ncols = o1 ? N / 3 : N;
-  const int bn = pick_bn(N, ncols);
+  const int bn = pick_bn(N, ncols, K / BK);
   if (!bn) return DPP_ERR_SHAPE;
   CUtensorMap ta, tb;
   const uint64_t da[2] = {(uint64_t)K, (uint64_t)M}, sa[1] = {(uint64_t)K * 2};
   const uint32_t ba[2] = {BK, BM};
   const uint64_t db[2] = {(uint64_t)K, (uint64_t)N}, sb[1] = {(uint64_t)K * 2};
-  const uint32_t bb[2] = {BK, (uint32_t)bn};
+  const uint32_t bb[2] = {BK, (uint32_t)mma_n(bn)};
   if (!make_map(&ta, a, 2, da, sa, ba) || !make_map(&tb, w, 2, db, sb, bb)) return DPP_ERR_CUDA;
   GemmArgs g{};
   g.M = M; g.N = N; g.K = K; g.nkb = K / BK;
@@ -363,7 +391,7 @@ int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2,
 int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,
                    int Cin, int Cout, int P, int* status, long long wait_limit, cudaStream_t s) {
   if (!tc_conv_supported(B, H, W, Cin, Cout, P)) return DPP_ERR_SHAPE;
-  const int bn = pick_bn(Cout, Cout);
+  const int bn = pick_bn(Cout, Cout, 9 * Cin / BK);
   if (!bn) return DPP_ERR_SHAPE;
   const int box_px = W < 128 ? W : 128;
   CUtensorMap tf, ts, tw;
@@ -372,7 +400,7 @@ int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int
   const uint32_t by[4] = {BK, (uint32_t)box_px, 1, 1};
   const int K = 9 * Cin;
   const uint64_t dw[2] = {(uint64_t)K, (uint64_t)Cout}, sw[1] = {(uint64_t)K * 2};
-  const uint32_t bw[2] = {BK, (uint32_t)bn};
+  const uint32_t bw[2] = {BK, (uint32_t)mma_n(bn)};
   if (!make_map(&tf, yf, 4, dy, sy, by) || !make_map(&ts, ys, 4, dy, sy, by) ||
       !make_map(&tw, w, 2, dw, sw, bw))
     return DPP_ERR_CUDA;

@@ -28,6 +28,8 @@ def _conv_gpu(yf, ys, w, P):
     ("bf16", 1, 8, 256, 64, 128, 2),      # half a row per tile
     ("bf16", 1, 16, 32, 64, 256, 4),      # 4 rows per tile
     ("bf16", 1, 16, 128, 192, 128, 8),    # one row per tile, 1-row bands (both halos stale)
+    ("bf16", 1, 16, 64, 256, 320, 2),     # 36 K slices: 128 x 320 tiles (two MMAs per step)
+    ("bf16", 1, 160, 128, 256, 320, 4),   # 160 such tiles: some CTAs reuse one accumulator
     ("f32", 1, 32, 32, 64, 64, 2),
     ("f32", 1, 6, 5, 3, 7, 3),            # ragged sizes on the SIMT path
 ])
