@@ -261,20 +261,32 @@ def run_gpu(args):
             tdist.barrier()
         torch.cuda.synchronize()
 
+    # The step time comes from one start/end event pair per step: events recorded
+    # between the stages would keep each kernel from overlapping its predecessor's
+    # tail (the kernels are launched as programmatic dependents).  A second pass
+    # with per-stage events gives the breakdown.
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
     with NvmlClockSampler(lrank) as clocks:
         barrier()
         t0 = time.perf_counter()
         for i in range(K):
             flush.fill_(1)
-            step(events[i])
+            step_ev[i][0].record(stream)
+            step()
+            step_ev[i][1].record(stream)
         barrier()
         wall = time.perf_counter() - t0
+        for i in range(K):
+            flush.fill_(1)
+            step(events[i])
+        barrier()
     st = dpp.read_device_status(wsb)
     if st != 0:
         raise RuntimeError(f"device status {st} in the timed region")
     stage_ms = [[events[i][s].elapsed_time(events[i][s + 1]) for s in range(nst - 1)]
                 for i in range(K)]
-    step_ms = [events[i][0].elapsed_time(events[i][nst - 1]) for i in range(K)]
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
     tot_ms = reduce_max(sum(step_ms), dev)
     ms_per_step = tot_ms / K
     value = whole_job_rate(K, ws_n, tot_ms)
@@ -346,6 +358,8 @@ def run_gpu(args):
         "roofline": roofline, "kernels": kernels, "e2e": e2e,
         "gpu_launches": dpp.layer_kernel_count(prm, dpp.STALE) * K,
         "wall_s_timed_region": wall,
+        "ms_per_step_with_stage_events": statistics.mean(
+            events[i][0].elapsed_time(events[i][nst - 1]) for i in range(K)),
     }
     line["clocks"] = clocks.summary()
     if not args.no_secondary:

@@ -279,8 +279,10 @@ int dpp_layer_kernel_count(const dpp_layer_params* p, int mode) {
   if (p->dtype == DPP_BF16)  // + the merge of the split attention schedule
     n += dpp::tc_attention_kernel_count(p->B, p->H * p->W, p->heads, p->P, true) - 1;
   if (mode == DPP_STALE && p->refresh) {
+    // a launch per full table of segments, and always a last one (it also copies
+    // the GroupNorm sums)
     const long long nseg = 2 + (long long)p->B * (p->P - 1);
-    n += (int)cdiv(nseg, dpp::kMaxRefreshSegs);
+    n += (int)(nseg / dpp::kMaxRefreshSegs) + 1;
   }
   return n;
 }
@@ -408,8 +410,11 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
                2ll * p.W * p.C);
       if (rc) return rc;
     }
-  if (tab.nseg > 0 && (rc = dpp::launch_refresh(tab, p.dtype, s))) return rc;
-  DPP_CUDA_CHECK(cudaMemcpyAsync(st->gn_stats, gn_fresh, gn_bytes, cudaMemcpyDeviceToDevice, s));
+  // the last launch also copies the fresh GroupNorm sums into the state
+  tab.copy_n = (int)(gn_bytes / sizeof(float));
+  tab.copy_src = gn_fresh;
+  tab.copy_dst = st->gn_stats;
+  if ((rc = dpp::launch_refresh(tab, p.dtype, s))) return rc;
   return mark(6);
 }
 

@@ -1,5 +1,6 @@
 // Shared device/host helpers of the displaced-patch layer library (sm_103a).
 #pragma once
+#include <utility>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -68,6 +69,25 @@ namespace dpp_host {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 long long wait_limit_from_env();  // DPP_DEBUG_WAIT_LIMIT, else the default
 int sm_count();                   // SMs of the current device (cached per device)
+
+// Launches kernel<<<grid, block, smem, s>>>(args...) with programmatic stream
+// serialization (the kernel calls ptx::grid_dep_wait before its first dependent
+// memory access).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace dpp_host
 

@@ -12,6 +12,7 @@
 //   mu = S1/N, var = max(S2/N - mu^2, 0), y = (x - mu) * rstd * gamma + beta.
 // Both are HBM-bound streams: stats reads 1 element, apply reads 1 and writes 1.
 #include "groupnorm.cuh"
+#include "ptx.cuh"
 
 namespace dpp {
 
@@ -22,6 +23,8 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const T* __restrict__ x,
   constexpr int VEC = Vec<T>::N;
   extern __shared__ float red[];  // [2][PIX][C]
   const int chunk = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   if (status_to_zero && chunk == 0 && p == 0 && b == 0 && threadIdx.x == 0) *status_to_zero = 0;
   const int NV = g.C / VEC;
   const int PIX = 256 / NV;
@@ -92,6 +95,8 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
   float* s_tot = sm + 3 * g.C;  // [P][G][2] fresh sums of every patch (sync) or own
   const int chunk = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   // fresh sums over chunks, for own patch (and every patch at the synchronous step);
   // eight independent partial sums so that the chunk loads are in flight together
   for (int idx = tid; idx < g.P * g.G * 2; idx += blockDim.x) {
@@ -193,20 +198,26 @@ int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, 
   const int PIX = 256 / NV;
   const size_t red_bytes = 2ull * PIX * g.C * sizeof(float);
   const size_t app_bytes = (3ull * g.C + 2ull * g.P * g.G) * sizeof(float);
+  using dpp_host::launch_pdl;
+  cudaError_t e;
   if (dtype == DPP_BF16) {
     auto* xs = static_cast<const __nv_bfloat16*>(x);
-    gn_stats_kernel<__nv_bfloat16><<<grid, 256, red_bytes, stream>>>(xs, partial, g,
-                                                                     status_to_zero);
-    gn_apply_kernel<__nv_bfloat16><<<grid, 256, app_bytes, stream>>>(
-        xs, static_cast<__nv_bfloat16*>(y), partial, stale_stats, fresh_out, gamma, beta, g, eps,
-        sync);
+    e = launch_pdl(gn_stats_kernel<__nv_bfloat16>, grid, dim3(256), red_bytes, stream, xs, partial,
+                   g, status_to_zero);
+    if (e == cudaSuccess)
+      e = launch_pdl(gn_apply_kernel<__nv_bfloat16>, grid, dim3(256), app_bytes, stream, xs,
+                     static_cast<__nv_bfloat16*>(y), (const float*)partial, stale_stats, fresh_out,
+                     gamma, beta, g, eps, sync);
   } else {
     auto* xs = static_cast<const float*>(x);
-    gn_stats_kernel<float><<<grid, 256, red_bytes, stream>>>(xs, partial, g, status_to_zero);
-    gn_apply_kernel<float><<<grid, 256, app_bytes, stream>>>(
-        xs, static_cast<float*>(y), partial, stale_stats, fresh_out, gamma, beta, g, eps, sync);
+    e = launch_pdl(gn_stats_kernel<float>, grid, dim3(256), red_bytes, stream, xs, partial, g,
+                   status_to_zero);
+    if (e == cudaSuccess)
+      e = launch_pdl(gn_apply_kernel<float>, grid, dim3(256), app_bytes, stream, xs,
+                     static_cast<float*>(y), (const float*)partial, stale_stats, fresh_out, gamma,
+                     beta, g, eps, sync);
   }
-  return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
 
 }  // namespace dpp

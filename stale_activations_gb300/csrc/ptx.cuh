@@ -260,5 +260,17 @@ __device__ __forceinline__ uint32_t elect_one() {
   return pred;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream is finishing:
+// everything before grid_dep_wait() overlaps it, so that part must not touch
+// memory the previous kernels write or read.  grid_dep_wait() returns once the
+// previous kernel has completed and its writes are visible (at once when there is
+// no such dependency).  grid_dep_launch() lets the next kernel's CTAs be scheduled
+// (they run their own prologue, then wait likewise).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace ptx
 }  // namespace dpp

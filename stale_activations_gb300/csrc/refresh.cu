@@ -11,6 +11,7 @@
 // traffic per element: read fresh and stale, write stale and the int8 code, plus
 // 4 bytes of scale per 128.
 #include "refresh.cuh"
+#include "ptx.cuh"
 
 namespace dpp {
 
@@ -48,9 +49,9 @@ __device__ __forceinline__ void store8<float>(float* p, const float (&f)[8]) {
 
 // One 128-element block, done by the 16 lanes of a half warp (`hmask` names them):
 // elements strided by 16 so that any length nb <= 128 is covered.  Used for ragged
-// last blocks and misaligned segments only.
+// last blocks and misaligned segments only (the scalar pass after the streaming loop).
 template <typename T>
-__device__ __noinline__ void refresh_block_scalar(const T* fr, T* st, int8_t* cd, float* scale,
+__device__ __forceinline__ void refresh_block_scalar(const T* fr, T* st, int8_t* cd, float* scale,
                                                   int nb, int sub, unsigned hmask) {
   float d[8], sv[8];
   float a = 0.0f;
@@ -100,34 +101,30 @@ __device__ __forceinline__ void unpack8<float>(const uint4 (&u)[2], float (&f)[8
   for (int i = 0; i < 4; ++i) { f[i] = a[i]; f[4 + i] = b[i]; }
 }
 
-// Looks up block gb; issues the loads of a full aligned block (returned in v), or
-// refreshes a ragged/misaligned block at once.
+// Looks up block gb and, if it is a full block of an aligned segment, issues its
+// loads (returned in v); other blocks are left to the scalar pass.
 template <typename T>
 __device__ __forceinline__ void start_block(const RefreshTable& tab, long long gb, long long total,
-                                            int& seg, int sub, unsigned hmask, VecBlock& v) {
+                                            int& seg, int sub, VecBlock& v) {
   v.live = false;
   if (gb >= total) return;
   while (gb >= tab.blk_start[seg + 1]) ++seg;  // gb only grows: segments in order
   const RefreshSeg& sg = tab.seg[seg];
   const long long j = gb - tab.blk_start[seg];
   const long long e0 = j * 128;
-  const int nb = (int)min(128ll, sg.n - e0);
+  if (!sg.vec_ok || sg.n - e0 < 128) return;
   const T* fr = reinterpret_cast<const T*>(sg.fresh) + e0;
   T* st = reinterpret_cast<T*>(sg.stale) + e0;
-  if (nb == 128 && sg.vec_ok) {
-    constexpr int NV = 8 / Vec<T>::N;  // 16-byte vectors per lane: 1 (bf16) or 2 (fp32)
+  constexpr int NV = 8 / Vec<T>::N;  // 16-byte vectors per lane: 1 (bf16) or 2 (fp32)
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      v.fr[k] = __ldcs(reinterpret_cast<const uint4*>(fr + sub * 8) + k);
-      v.st[k] = __ldcs(reinterpret_cast<const uint4*>(st + sub * 8) + k);
-    }
-    v.stale = st + sub * 8;
-    v.codes = sg.codes + e0 + sub * 8;
-    v.scale = sg.scales + j;
-    v.live = true;
-  } else {
-    refresh_block_scalar<T>(fr, st, sg.codes + e0, sg.scales + j, nb, sub, hmask);
+  for (int k = 0; k < NV; ++k) {
+    v.fr[k] = __ldcs(reinterpret_cast<const uint4*>(fr + sub * 8) + k);
+    v.st[k] = __ldcs(reinterpret_cast<const uint4*>(st + sub * 8) + k);
   }
+  v.stale = st + sub * 8;
+  v.codes = sg.codes + e0 + sub * 8;
+  v.scale = sg.scales + j;
+  v.live = true;
 }
 
 template <typename T>
@@ -158,7 +155,9 @@ __device__ __forceinline__ void finish_block(const VecBlock& v, int sub, unsigne
 }
 
 // Each half warp takes two blocks per pass, issuing all four 128-bit loads before
-// finishing either block, to keep more bytes in flight per thread.
+// finishing either block, to keep more bytes in flight per thread.  Blocks that are
+// ragged (the last of a segment) or in a misaligned segment are refreshed by a
+// second, scalar pass, so that the streaming loop holds no call.
 template <typename T>
 __global__ void __launch_bounds__(256, 4) refresh_kernel(const __grid_constant__ RefreshTable tab) {
   const int lane = threadIdx.x & 31;
@@ -168,29 +167,45 @@ __global__ void __launch_bounds__(256, 4) refresh_kernel(const __grid_constant__
                           (lane >> 4);
   const long long stride = (long long)gridDim.x * (blockDim.x >> 5) * 2;
   const long long total = tab.blk_start[tab.nseg];
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < tab.copy_n; i += blockDim.x) tab.copy_dst[i] = tab.copy_src[i];
   int seg = 0;
   for (long long gb = group; gb < total; gb += 2 * stride) {
     VecBlock v0, v1;
-    start_block<T>(tab, gb, total, seg, sub, hmask, v0);
-    start_block<T>(tab, gb + stride, total, seg, sub, hmask, v1);
+    start_block<T>(tab, gb, total, seg, sub, v0);
+    start_block<T>(tab, gb + stride, total, seg, sub, v1);
     if (v0.live) finish_block<T>(v0, sub, hmask);
     if (v1.live) finish_block<T>(v1, sub, hmask);
+  }
+  // scalar pass: every block of a misaligned segment, the ragged last block of others
+  for (int k = 0; k < tab.nseg; ++k) {
+    const RefreshSeg& sg = tab.seg[k];
+    const long long nblk = tab.blk_start[k + 1] - tab.blk_start[k];
+    for (long long j = (sg.vec_ok ? sg.n / 128 : 0) + group; j < nblk; j += stride) {
+      const long long e0 = j * 128;
+      refresh_block_scalar<T>(reinterpret_cast<const T*>(sg.fresh) + e0,
+                              reinterpret_cast<T*>(sg.stale) + e0, sg.codes + e0, sg.scales + j,
+                              (int)min(128ll, sg.n - e0), sub, hmask);
+    }
   }
 }
 
 int launch_refresh(const RefreshTable& tab, int dtype, cudaStream_t stream) {
   const long long total = tab.blk_start[tab.nseg];
-  if (total == 0) return DPP_OK;
+  if (total == 0 && tab.copy_n == 0) return DPP_OK;
   const int threads = 256;
   const long long groups_per_cta = threads / 32 * 2 * 2;  // two blocks per group and pass
   long long want = (total + groups_per_cta - 1) / groups_per_cta;
   const long long cap = (long long)dpp_host::sm_count() * 4;  // 4 resident CTAs of 256 per SM
-  const int grid = (int)(want < cap ? want : cap);
-  if (dtype == DPP_BF16)
-    refresh_kernel<__nv_bfloat16><<<grid, threads, 0, stream>>>(tab);
-  else
-    refresh_kernel<float><<<grid, threads, 0, stream>>>(tab);
-  return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+  const int grid = (int)(want < 1 ? 1 : want < cap ? want : cap);  // >= 1 for the side copy
+  const cudaError_t e =
+      dtype == DPP_BF16
+          ? dpp_host::launch_pdl(refresh_kernel<__nv_bfloat16>, dim3(grid), dim3(threads), 0,
+                                 stream, tab)
+          : dpp_host::launch_pdl(refresh_kernel<float>, dim3(grid), dim3(threads), 0, stream, tab);
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
 
 }  // namespace dpp

@@ -20,6 +20,10 @@ struct RefreshTable {
   RefreshSeg seg[kMaxRefreshSegs];
   long long blk_start[kMaxRefreshSegs + 1];  // prefix sums of ceil(n/128)
   int nseg;
+  // an exact fp32 copy done on the side by CTA 0 (the layer's GroupNorm sums), or none
+  int copy_n;
+  const float* copy_src;
+  float* copy_dst;
 };
 
 // Launches one refresh over all segments of `tab` (blk_start filled by caller).

@@ -265,6 +265,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
   const Sched sc = make_sched(a);
+  // the set-up above overlaps the previous kernel; its outputs are read from here on
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
 
   if (warp >= 8) {
     // Register split (launch: 384 threads x 168): this warpgroup drops to 80 per
@@ -580,6 +583,8 @@ constexpr int kMaxPieces = 256;
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
   __shared__ int recs[kMaxPieces];
   __shared__ int warp_count[8];
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int ut = blockIdx.x;
   const long long s_a = (long long)ut * a.nkt, s_b = s_a + a.nkt - 1;
   const int ca = tail_cta(s_a, a), cb = tail_cta(s_b, a);
@@ -737,9 +742,11 @@ int launch_tc_attention(const void* q, const void* kf, const void* vf, const voi
   a.part = static_cast<uint8_t*>(partials);
   a.status = status;
   a.wait_limit = wait_limit;
-  tc_attn_kernel<<<a.G, ATTN_THREADS, ATTN_SMEM, s>>>(mq, mkf, mks, mvf, mvs, a);
-  if (a.split) attn_combine_kernel<<<a.U - a.W * a.G, 256, 0, s>>>(a);
-  return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+  cudaError_t e = dpp_host::launch_pdl(tc_attn_kernel, dim3(a.G), dim3(ATTN_THREADS), ATTN_SMEM,
+                                       s, mq, mkf, mks, mvf, mvs, a);
+  if (e == cudaSuccess && a.split)
+    e = dpp_host::launch_pdl(attn_combine_kernel, dim3(a.U - a.W * a.G), dim3(256), 0, s, a);
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
 
 }  // namespace dpp

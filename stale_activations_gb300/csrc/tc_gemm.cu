@@ -105,6 +105,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the set-up above overlaps the previous kernel; its outputs are read from here on
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -336,8 +339,9 @@ int launch(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
   g.n_tiles = g.N / BN;
   const long long ntiles = (long long)g.m_tiles * g.n_tiles;
   const int grid = (int)(ntiles < dpp_host::sm_count() ? ntiles : dpp_host::sm_count());
-  tc_gemm_kernel<CONV, BN><<<grid, GEMM_THREADS, Cfg<BN>::SMEM, s>>>(ta, ta2, tb, g);
-  return cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+  const cudaError_t e = dpp_host::launch_pdl(tc_gemm_kernel<CONV, BN>, dim3(grid),
+                                             dim3(GEMM_THREADS), Cfg<BN>::SMEM, s, ta, ta2, tb, g);
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
 
 template <bool CONV>
