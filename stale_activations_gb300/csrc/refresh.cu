@@ -22,18 +22,6 @@ __device__ __forceinline__ int quantise(float d, float s) {
   return max(-127, min(127, q));
 }
 
-// Same result as quantise(d, s), cheaper: with r = rn(1/s) the product t = rn(d*r)
-// is within 2e-5 of rn(d/s) (|d/s| <= 127.0001 and three roundings of relative
-// size 2^-24 each), so both round to the same integer unless t lies within 1e-4 of
-// a half-integer; only then is the IEEE quotient formed.  Needs s >= FLT_MIN so
-// that r is finite.
-__device__ __forceinline__ int quantise_fast(float d, float s, float r) {
-  const float t = d * r;
-  float rt = rintf(t);
-  if (0.5f - fabsf(t - rt) < 1e-4f) rt = rintf(__fdiv_rn(d, s));
-  return max(-127, min(127, (int)rt));
-}
-
 template <typename T>
 __device__ __forceinline__ void store8(T* p, const float (&f)[8]);
 template <>
@@ -127,6 +115,12 @@ __device__ __forceinline__ void start_block(const RefreshTable& tab, long long g
   v.live = true;
 }
 
+// Rounding without conversion instructions: for |t| < 2^22 the fp32 sum t + 1.5 * 2^23
+// (round to nearest, ties to even) is exactly 1.5 * 2^23 + rint(t) with rint's ties to
+// even (the constant is even), so subtracting it back gives rint(t) as a float and the
+// low byte of the sum's bits is rint(t) as a two's-complement int8.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+
 template <typename T>
 __device__ __forceinline__ void finish_block(const VecBlock& v, int sub, unsigned hmask) {
   float f[8], sv[8], d[8];
@@ -139,16 +133,32 @@ __device__ __forceinline__ void finish_block(const VecBlock& v, int sub, unsigne
   for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(hmask, a, o));
   const float s = __fdiv_rn(a, 127.0f);
   if (sub == 0) *v.scale = s;
-  const bool fast = s >= 1.17549435e-38f;  // FLT_MIN: 1/s is finite (s == 0 is not fast)
+  // With r = rn(1/s), t = rn(d*r) lies within 2e-5 of rn(d/s) (|d/s| <= 127.0001 and
+  // three roundings of relative size 2^-24), so both round to the same integer unless
+  // t is within 1e-4 of a half-integer; only then is the IEEE quotient formed.  A zero
+  // or subnormal s (1/s not finite) takes the IEEE rule for every element.
+  const bool fast = s >= 1.17549435e-38f;  // FLT_MIN
   const float rc = fast ? __frcp_rn(s) : 0.0f;
   float nv[8];
   uint32_t c0 = 0, c1 = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int q = fast ? quantise_fast(d[i], s, rc) : quantise(d[i], s);
-    nv[i] = __fmaf_rn((float)q, s, sv[i]);
-    const uint32_t b = (uint32_t)(q & 0xFF);
-    if (i < 4) c0 |= b << (8 * i); else c1 |= b << (8 * (i - 4));
+    float tm;
+    if (fast) {
+      const float t = d[i] * rc;
+      tm = t + kRoundMagic;
+      if (0.5f - fabsf(t - (tm - kRoundMagic)) < 1e-4f) tm = __fdiv_rn(d[i], s) + kRoundMagic;
+    } else {
+      tm = (float)quantise(d[i], s) + kRoundMagic;
+    }
+    tm = fminf(fmaxf(tm, kRoundMagic - 127.0f), kRoundMagic + 127.0f);  // clamp to +-127
+    nv[i] = __fmaf_rn(tm - kRoundMagic, s, sv[i]);
+    // the code byte (low byte of tm's bits) into byte i % 4 of c0 / c1
+    constexpr uint32_t kSel[4] = {0x3214u, 0x3240u, 0x3410u, 0x4210u};
+    if (i < 4)
+      c0 = __byte_perm(c0, __float_as_uint(tm), kSel[i]);
+    else
+      c1 = __byte_perm(c1, __float_as_uint(tm), kSel[i - 4]);
   }
   store8<T>(static_cast<T*>(v.stale), nv);
   __stcs(reinterpret_cast<uint2*>(v.codes), make_uint2(c0, c1));
