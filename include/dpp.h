@@ -135,9 +135,10 @@ int stale_kv_attention(const void* q, const void* k_fresh, const void* v_fresh,
  * the last round leaves SMs idle.  Here those last units are cut into runs of
  * 128-key tiles shared evenly by all CTAs; each piece leaves a partial result
  * (O/l rounded to fp16, the running maximum m and sum l in fp32) in `partials`,
- * and a second kernel merges the pieces of each unit in a fixed order
- * (deterministic).  The merge reads O/l in fp16, whose rounding (2^-11 relative)
- * stays well below that of the bf16 output.
+ * and whichever piece of a unit finishes last merges them all in a fixed order
+ * (deterministic; the call zeroes the counters it uses for this at the start of the
+ * buffer).  The merge reads O/l in fp16, whose rounding (2^-11 relative) stays well
+ * below that of the bf16 output.
  * partials: caller-owned device buffer, 16-byte aligned, of at least
  * dpp_attention_partials_size() bytes; that size depends on the current device's
  * SM count, so query it on the device that runs the call.  It may be NULL when

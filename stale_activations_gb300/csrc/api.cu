@@ -139,10 +139,10 @@ int run_linear(const void* a, const void* w, void* o0, void* o1, void* o2, long 
 
 int run_attention(const void* q, const void* kf, const void* vf, const void* ks, const void* vs,
                   void* o, int B, int L, int heads, int P, int dtype, void* part,
-                  size_t part_bytes, int* st, cudaStream_t s) {
+                  size_t part_bytes, bool counters_zeroed, int* st, cudaStream_t s) {
   if (dtype == DPP_BF16)
-    return dpp::launch_tc_attention(q, kf, vf, ks, vs, o, B, L, heads, P, part, part_bytes, st,
-                                    dpp_host::wait_limit_from_env(), s);
+    return dpp::launch_tc_attention(q, kf, vf, ks, vs, o, B, L, heads, P, part, part_bytes,
+                                    counters_zeroed, st, dpp_host::wait_limit_from_env(), s);
   return dpp::launch_simt_attention(q, kf, vf, ks, vs, o, B, L, heads, P, dtype, s);
 }
 
@@ -223,7 +223,7 @@ int stale_kv_attention(const void* q, const void* k_fresh, const void* v_fresh,
       !aligned16(v_stale) || !aligned16(o))
     return DPP_ERR_ALIGN;
   return run_attention(q, k_fresh, v_fresh, k_stale, v_stale, o, B, L, heads, P, dtype, nullptr,
-                       0, dev_status, static_cast<cudaStream_t>(stream));
+                       0, false, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 size_t dpp_attention_partials_size(int B, int L, int heads, int head_dim, int P, int dtype) {
@@ -247,7 +247,7 @@ int stale_kv_attention_split(const void* q, const void* k_fresh, const void* v_f
   if (need && (!partials || partials_bytes < need)) return DPP_ERR_ARG;
   // with `need` 0 the units divide evenly and both schedules are the same
   return run_attention(q, k_fresh, v_fresh, k_stale, v_stale, o, B, L, heads, P, dtype,
-                       need ? partials : nullptr, partials_bytes, dev_status,
+                       need ? partials : nullptr, partials_bytes, false, dev_status,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -276,8 +276,6 @@ int64_t dpp_message_blocks(const dpp_layer_params* p) {
 int dpp_layer_kernel_count(const dpp_layer_params* p, int mode) {
   if (check_layer(p)) return -1;
   int n = 2 /* gn */ + 1 /* conv */ + 1 /* qkv */ + 1 /* attention */ + 1 /* out proj */;
-  if (p->dtype == DPP_BF16)  // + the merge of the split attention schedule
-    n += dpp::tc_attention_kernel_count(p->B, p->H * p->W, p->heads, p->P, true) - 1;
   if (mode == DPP_STALE && p->refresh) {
     // a launch per full table of segments, and always a last one (it also copies
     // the GroupNorm sums)
@@ -340,8 +338,13 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
   if ((rc = mark(0))) return rc;
   // a1 + a2: fresh sums of every patch, spliced GroupNorm
   const dpp::GnDims g = dpp::make_gn_dims(p.B, p.H, p.W, p.C, p.P, p.G);
+  // the first kernel also zeroes the status word and the attention's piece counters
+  const int ncnt = p.dtype == DPP_BF16 && lo.attn_partial_bytes
+                       ? dpp::tc_attention_counters(p.B, L, p.heads, p.P)
+                       : 0;
   rc = dpp::launch_gn(x, y, gn_partial, sync ? nullptr : st->gn_stats, gn_fresh, wts->gamma,
-                      wts->beta, g, p.eps, sync ? 1 : 0, p.dtype, status, s);
+                      wts->beta, g, p.eps, sync ? 1 : 0, p.dtype, status,
+                      reinterpret_cast<int*>(ws + lo.attn_partial), ncnt, s);
   if (rc || (rc = mark(1))) return rc;
   // a3: halo conv, halo rows from the stale conv input (fresh at the synchronous step)
   rc = run_conv(y, sync ? y : st->y_stale, wts->w_conv, h, p.B, p.H, p.W, p.C, p.C, p.P, p.dtype,
@@ -353,7 +356,7 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
   // a5: stale-KV attention
   rc = run_attention(q, k, v, sync ? k : st->k_stale, sync ? v : st->v_stale, o, p.B, L, p.heads,
                      p.P, p.dtype, lo.attn_partial_bytes ? ws + lo.attn_partial : nullptr,
-                     lo.attn_partial_bytes, status, s);
+                     lo.attn_partial_bytes, true /* zeroed by gn_stats */, status, s);
   if (rc || (rc = mark(4))) return rc;
   // a6: output projection
   rc = run_linear(o, wts->w_o, out, nullptr, nullptr, M, p.C, p.C, p.dtype, status, s);

@@ -19,13 +19,17 @@ namespace dpp {
 template <typename T>
 __global__ void __launch_bounds__(256) gn_stats_kernel(const T* __restrict__ x,
                                                        float* __restrict__ partial, GnDims g,
-                                                       int* status_to_zero) {
+                                                       int* status_to_zero, int* zero_ints,
+                                                       int nzero) {
   constexpr int VEC = Vec<T>::N;
   extern __shared__ float red[];  // [2][PIX][C]
   const int chunk = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  if (status_to_zero && chunk == 0 && p == 0 && b == 0 && threadIdx.x == 0) *status_to_zero = 0;
+  if (chunk == 0 && p == 0 && b == 0) {
+    if (status_to_zero && threadIdx.x == 0) *status_to_zero = 0;
+    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero_ints[i] = 0;
+  }
   const int NV = g.C / VEC;
   const int PIX = 256 / NV;
   const int tid = threadIdx.x;
@@ -191,7 +195,7 @@ size_t gn_partial_bytes(const GnDims& g) {
 
 int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, float* fresh_out,
               const float* gamma, const float* beta, const GnDims& g, float eps, int sync,
-              int dtype, int* status_to_zero, cudaStream_t stream) {
+              int dtype, int* status_to_zero, int* zero_ints, int nzero, cudaStream_t stream) {
   dim3 grid(g.nchunk, g.P, g.B);
   const int VEC = dtype == DPP_BF16 ? 8 : 4;
   const int NV = g.C / VEC;
@@ -203,7 +207,7 @@ int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, 
   if (dtype == DPP_BF16) {
     auto* xs = static_cast<const __nv_bfloat16*>(x);
     e = launch_pdl(gn_stats_kernel<__nv_bfloat16>, grid, dim3(256), red_bytes, stream, xs, partial,
-                   g, status_to_zero);
+                   g, status_to_zero, zero_ints, nzero);
     if (e == cudaSuccess)
       e = launch_pdl(gn_apply_kernel<__nv_bfloat16>, grid, dim3(256), app_bytes, stream, xs,
                      static_cast<__nv_bfloat16*>(y), (const float*)partial, stale_stats, fresh_out,
@@ -211,7 +215,7 @@ int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, 
   } else {
     auto* xs = static_cast<const float*>(x);
     e = launch_pdl(gn_stats_kernel<float>, grid, dim3(256), red_bytes, stream, xs, partial, g,
-                   status_to_zero);
+                   status_to_zero, zero_ints, nzero);
     if (e == cudaSuccess)
       e = launch_pdl(gn_apply_kernel<float>, grid, dim3(256), app_bytes, stream, xs,
                      static_cast<float*>(y), (const float*)partial, stale_stats, fresh_out, gamma,

@@ -15,9 +15,10 @@ size_t gn_partial_bytes(const GnDims& g);
 
 // Launches the stats and apply kernels.  stale_stats may be NULL when sync != 0.
 // fresh_out (may be NULL) receives the [B,P,G,2] fresh sums.  The stats kernel
-// zeroes *status_to_zero first (if non-NULL).
+// zeroes *status_to_zero first (if non-NULL), and the nzero ints at zero_ints (the next
+// kernels' counters).
 int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, float* fresh_out,
               const float* gamma, const float* beta, const GnDims& g, float eps, int sync,
-              int dtype, int* status_to_zero, cudaStream_t stream);
+              int dtype, int* status_to_zero, int* zero_ints, int nzero, cudaStream_t stream);
 
 }  // namespace dpp

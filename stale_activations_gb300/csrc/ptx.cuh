@@ -260,6 +260,11 @@ __device__ __forceinline__ uint32_t elect_one() {
   return pred;
 }
 
+// Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Programmatic dependent launch.  A kernel launched with programmatic stream
 // serialization may start while the previous kernel in the stream is finishing:
 // everything before grid_dep_wait() overlaps it, so that part must not touch

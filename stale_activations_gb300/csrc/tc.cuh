@@ -19,13 +19,16 @@ int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int
 
 // Stale-KV flash attention (see stale_kv_attention in dpp.h), head_dim 64.  With
 // `partials` non-NULL the units that do not divide evenly over the CTAs are shared key
-// tile by key tile and merged by a second kernel; partial_bytes must then be at least
-// tc_attention_partial_bytes() (0 when the units divide evenly).
+// tile by key tile and merged in the kernel; partial_bytes must then be at least
+// tc_attention_partial_bytes() (0 when the units divide evenly).  The buffer starts
+// with tc_attention_counters() ints that must be zero when the kernel starts: the
+// launch zeroes them unless counters_zeroed says an earlier kernel of the stream did
+// (the kernel leaves them zero).
 int launch_tc_attention(const void* q, const void* kf, const void* vf, const void* ks,
                         const void* vs, void* o, int B, int L, int heads, int P, void* partials,
-                        size_t partial_bytes, int* status, long long wait_limit, cudaStream_t s);
+                        size_t partial_bytes, bool counters_zeroed, int* status,
+                        long long wait_limit, cudaStream_t s);
 size_t tc_attention_partial_bytes(int B, int L, int heads, int P);
-// Kernels launch_tc_attention launches (1, or 2 with the split schedule).
-int tc_attention_kernel_count(int B, int L, int heads, int P, bool split);
+int tc_attention_counters(int B, int L, int heads, int P);
 
 }  // namespace dpp

@@ -13,8 +13,9 @@
 // U mod G units are shared by all CTAs key tile by key tile ("split" schedule):
 // each CTA takes an equal contiguous run of their (unit, key tile) steps, a unit
 // cut between CTAs leaves one partial result per piece (O/l in fp16, the running
-// maximum m and sum l in fp32), and attn_combine_kernel merges the pieces of each
-// cut unit in CTA order (deterministic).  A CTA's steps run through one pipeline:
+// maximum m and sum l in fp32); the warpgroup that finishes a unit's last piece
+// (an atomic count per unit and query tile) merges all of them in CTA order, so the
+// result does not depend on which piece finished last.  A CTA's steps run through one pipeline:
 // the next unit's Q is loaded into the second Q buffer while the current unit
 // finishes, and its first S = Q K^T is issued right after the last P V.
 // Per CTA, 12 warps:
@@ -81,6 +82,7 @@ constexpr int REC_BYTES = REC_L + 2 * QT * 4;
 
 struct AttnArgs {
   int L, heads, P, Lp, g, n_pairs, nkt;
+  int* cnt;         // split: [tail unit][query tile] pieces finished (zero before the call)
   int U;            // units (batch, head, patch, pair of query tiles), pair fastest
   int G;            // CTAs
   int W;            // split: whole units per CTA (c, c+G, ...); 0 otherwise
@@ -98,6 +100,8 @@ struct Bars {
   uint64_t s_full[2], p_full[2], o_done[2], drain;
   uint32_t tmem_slot;
   int abort_flag;
+  int merge_from[2];  // per query tile: first CTA of the unit to merge, or -1
+  int merge_to[2];
 };
 static_assert(sizeof(Bars) <= 512, "barrier area");
 
@@ -217,6 +221,63 @@ __device__ __forceinline__ void store_f16x16(uint4* d4, const uint32_t (&o)[16],
         pack_f16x2(__uint_as_float(o[8 * i + 2]) * s, __uint_as_float(o[8 * i + 3]) * s),
         pack_f16x2(__uint_as_float(o[8 * i + 4]) * s, __uint_as_float(o[8 * i + 5]) * s),
         pack_f16x2(__uint_as_float(o[8 * i + 6]) * s, __uint_as_float(o[8 * i + 7]) * s));
+}
+
+// Merges the pieces of tail unit ut for row r of query tile t: records of CTAs
+// ca..cb (those with a non-empty run), in that order.  With pieces i = (m_i, l_i,
+// O_i/l_i): M = max m_i, w_i = l_i 2^(m_i - M), o = sum_i w_i (O_i/l_i) / sum_i w_i.
+// The records were written by other SMs: read through L2 (ld.global.cg).
+__device__ __forceinline__ void merge_rows(const AttnArgs& a, int ut, int t, int r, int ca, int cb,
+                                           const UnitPos& up) {
+  const long long s_a = (long long)ut * a.nkt;
+  auto record = [&](int c, long long b0) -> const uint8_t* {
+    // a CTA's first tail segment, or the last one of the CTA that started before the unit
+    return a.part + (size_t)((c == ca && b0 != s_a) ? a.G + ut : c) * REC_BYTES;
+  };
+  float M = -INFINITY;
+  for (int c = ca; c <= cb; ++c) {
+    const long long b0 = tail_bound(c, a);
+    if (b0 == tail_bound(c + 1, a)) continue;  // empty run
+    M = fmaxf(M, __ldcg(reinterpret_cast<const float*>(record(c, b0) + REC_M) + t * QT + r));
+  }
+  float acc[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) acc[d] = 0.f;
+  float wsum = 0.f;
+  for (int c = ca; c <= cb; ++c) {
+    const long long b0 = tail_bound(c, a);
+    if (b0 == tail_bound(c + 1, a)) continue;
+    const uint8_t* base = record(c, b0);
+    const float m = __ldcg(reinterpret_cast<const float*>(base + REC_M) + t * QT + r);
+    const float w = __ldcg(reinterpret_cast<const float*>(base + REC_L) + t * QT + r) * exp2f(m - M);
+    wsum += w;
+    const uint4* src = reinterpret_cast<const uint4*>(base + ((size_t)(t * QT + r) * D) * 2);
+    uint4 u[D / 8];
+#pragma unroll
+    for (int q = 0; q < D / 8; ++q) u[q] = __ldcg(src + q);
+#pragma unroll
+    for (int q = 0; q < D / 8; ++q) {
+      const uint32_t hw[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[e]));
+        acc[8 * q + 2 * e] = fmaf(w, f.x, acc[8 * q + 2 * e]);
+        acc[8 * q + 2 * e + 1] = fmaf(w, f.y, acc[8 * q + 2 * e + 1]);
+      }
+    }
+  }
+  const int row_in_patch = up.q0 + t * QT + r;
+  if (row_in_patch >= a.Lp) return;
+  __nv_bfloat16* dst =
+      a.o + ((long long)up.b * a.L + up.patch0 + row_in_patch) * (long long)(a.heads * D) + up.h * D;
+  const float inv = 1.f / wsum;
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < D / 8; ++q)
+    d4[q] = make_uint4(pack_bf16x2(acc[8 * q] * inv, acc[8 * q + 1] * inv),
+                       pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
+                       pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv),
+                       pack_bf16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
 }
 
 __global__ void __launch_bounds__(ATTN_THREADS, 1)
@@ -551,7 +612,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           if (valid) store_bf16x16(dst + c * 16, o, inv);
         }
       } else {  // one piece of a cut unit: O/l in fp16, m and l in fp32
-        const int rec = tail_seen ? a.G + (sg.u - a.W * a.G) : (int)blockIdx.x;
+        const int ut = sg.u - a.W * a.G;
+        const int rec = tail_seen ? a.G + ut : (int)blockIdx.x;
         uint8_t* base = a.part + (size_t)rec * REC_BYTES;
         uint4* dst = reinterpret_cast<uint4*>(base + ((size_t)(t * QT + r) * D) * 2);
 #pragma unroll
@@ -563,6 +625,25 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         }
         reinterpret_cast<float*>(base + REC_M)[t * QT + r] = m_ref;
         reinterpret_cast<float*>(base + REC_L)[t * QT + r] = l;
+        // The last piece of the unit to finish (for this query tile) merges them all.
+        __threadfence();
+        ptx::named_bar_sync(1 + t, 128);
+        if (quarter == 0 && lane == 0) {
+          const long long s_a = (long long)ut * a.nkt;
+          const int ca = tail_cta(s_a, a), cb = tail_cta(s_a + a.nkt - 1, a);
+          int np = 0;
+          for (int c = ca; c <= cb; ++c) np += tail_bound(c, a) != tail_bound(c + 1, a);
+          const bool last = atomicAdd(&a.cnt[2 * ut + t], 1) == np - 1;
+          if (last) atomicExch(&a.cnt[2 * ut + t], 0);  // all arrived: ready for the next call
+          bars->merge_from[t] = last ? ca : -1;
+          bars->merge_to[t] = cb;
+        }
+        ptx::named_bar_sync(1 + t, 128);
+        const int ca = bars->merge_from[t], cb = bars->merge_to[t];
+        if (ca >= 0) {
+          __threadfence();
+          merge_rows(a, ut, t, r, ca, cb, up);
+        }
       }
       if (sg.tail) tail_seen = true;
     }
@@ -573,81 +654,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
-}
-
-// Merges the pieces of each cut tail unit (one CTA per tail unit; units not cut
-// return at once).  Thread = (query tile, row).  With pieces i = (m_i, l_i, O_i/l_i):
-// M = max m_i, w_i = l_i 2^(m_i - M), o = sum_i w_i (O_i/l_i) / sum_i w_i, summed in
-// the order of the CTAs.
-constexpr int kMaxPieces = 256;
-__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
-  __shared__ int recs[kMaxPieces];
-  __shared__ int warp_count[8];
-  ptx::grid_dep_wait();
-  ptx::grid_dep_launch();
-  const int ut = blockIdx.x;
-  const long long s_a = (long long)ut * a.nkt, s_b = s_a + a.nkt - 1;
-  const int ca = tail_cta(s_a, a), cb = tail_cta(s_b, a);
-  if (ca == cb) return;
-  // the unit's records in CTA order (CTAs whose run is empty hold none): thread i looks
-  // at CTA ca + i, a ballot per warp gives each record its place in the list
-  const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
-  const int c = ca + i;
-  const bool has = c <= cb && tail_bound(c, a) != tail_bound(c + 1, a);
-  const unsigned ball = __ballot_sync(0xffffffffu, has);
-  if (lane == 0) warp_count[warp] = __popc(ball);
-  __syncthreads();
-  int pos = __popc(ball & ((1u << lane) - 1u)), np = 0;
-  for (int w = 0; w < 8; ++w) {
-    if (w < warp) pos += warp_count[w];
-    np += warp_count[w];
-  }
-  if (has) recs[pos] = (c == ca && tail_bound(c, a) != s_a) ? a.G + ut : c;
-  __syncthreads();
-  const int t = i >> 7, r = i & 127;
-  auto rec_f = [&](int k, int off) {
-    return reinterpret_cast<const float*>(a.part + (size_t)recs[k] * REC_BYTES + off)[t * QT + r];
-  };
-  float M = -INFINITY;
-#pragma unroll 4
-  for (int k = 0; k < np; ++k) M = fmaxf(M, rec_f(k, REC_M));
-  float acc[D];
-#pragma unroll
-  for (int d = 0; d < D; ++d) acc[d] = 0.f;
-  float wsum = 0.f;
-#pragma unroll 2
-  for (int k = 0; k < np; ++k) {
-    const float w = rec_f(k, REC_L) * exp2f(rec_f(k, REC_M) - M);
-    wsum += w;
-    const uint4* src = reinterpret_cast<const uint4*>(a.part + (size_t)recs[k] * REC_BYTES +
-                                                      ((size_t)(t * QT + r) * D) * 2);
-    uint4 u[D / 8];
-#pragma unroll
-    for (int q = 0; q < D / 8; ++q) u[q] = src[q];
-#pragma unroll
-    for (int q = 0; q < D / 8; ++q) {
-      const uint32_t hw[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[e]));
-        acc[8 * q + 2 * e] = fmaf(w, f.x, acc[8 * q + 2 * e]);
-        acc[8 * q + 2 * e + 1] = fmaf(w, f.y, acc[8 * q + 2 * e + 1]);
-      }
-    }
-  }
-  const UnitPos up = unit_pos(a.W * a.G + ut, a);
-  const int row_in_patch = up.q0 + t * QT + r;
-  if (row_in_patch >= a.Lp) return;
-  __nv_bfloat16* dst =
-      a.o + ((long long)up.b * a.L + up.patch0 + row_in_patch) * (long long)(a.heads * D) + up.h * D;
-  const float inv = 1.f / wsum;
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < D / 8; ++q)
-    d4[q] = make_uint4(pack_bf16x2(acc[8 * q] * inv, acc[8 * q + 1] * inv),
-                       pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
-                       pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv),
-                       pack_bf16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
 }
 
 bool make_map3(CUtensorMap* m, const void* base, int L, int B, int C, int box_rows) {
@@ -687,8 +693,7 @@ bool plan(int B, int L, int heads, int P, bool split, AttnArgs* a) {
   const long long U = (long long)B * heads * P * a->n_pairs;
   if (U * a->nkt > (1ll << 31) - 1) return false;
   a->U = (int)U;
-  // at most kMaxPieces CTAs, so that a cut unit has at most that many pieces
-  const int sms = dpp_host::sm_count() < kMaxPieces ? dpp_host::sm_count() : kMaxPieces;
+  const int sms = dpp_host::sm_count();
   if (split) {
     const long long T = U * a->nkt;
     a->G = (int)(T < sms ? T : sms);
@@ -711,24 +716,30 @@ bool plan(int B, int L, int heads, int P, bool split, AttnArgs* a) {
 
 }  // namespace
 
+// The partials buffer: the per-(tail unit, query tile) counters, then the records.
+static size_t counter_bytes(const AttnArgs& a) {
+  return ((size_t)2 * (a.U - a.W * a.G) * sizeof(int) + 255) / 256 * 256;
+}
+
 size_t tc_attention_partial_bytes(int B, int L, int heads, int P) {
   AttnArgs a;
   if (!plan(B, L, heads, P, true, &a) || !a.split) return 0;
-  return (size_t)(a.G + (a.U - a.W * a.G)) * REC_BYTES;
+  return counter_bytes(a) + (size_t)(a.G + (a.U - a.W * a.G)) * REC_BYTES;
 }
 
-int tc_attention_kernel_count(int B, int L, int heads, int P, bool split) {
+int tc_attention_counters(int B, int L, int heads, int P) {
   AttnArgs a;
-  if (!plan(B, L, heads, P, split, &a)) return 0;
-  return a.split ? 2 : 1;
+  if (!plan(B, L, heads, P, true, &a) || !a.split) return 0;
+  return 2 * (a.U - a.W * a.G);
 }
 
 int launch_tc_attention(const void* q, const void* kf, const void* vf, const void* ks,
                         const void* vs, void* o, int B, int L, int heads, int P, void* partials,
-                        size_t partial_bytes, int* status, long long wait_limit, cudaStream_t s) {
+                        size_t partial_bytes, bool counters_zeroed, int* status,
+                        long long wait_limit, cudaStream_t s) {
   AttnArgs a;
   if (!plan(B, L, heads, P, partials != nullptr, &a)) return DPP_ERR_SHAPE;
-  if (a.split && partial_bytes < (size_t)(a.G + (a.U - a.W * a.G)) * REC_BYTES)
+  if (a.split && partial_bytes < counter_bytes(a) + (size_t)(a.G + (a.U - a.W * a.G)) * REC_BYTES)
     return DPP_ERR_ARG;
   const int C = heads * D;
   int rc = set_attn_smem();
@@ -739,13 +750,16 @@ int launch_tc_attention(const void* q, const void* kf, const void* vf, const voi
       !make_map3(&mvs, vs, L, B, C, a.g))
     return DPP_ERR_CUDA;
   a.o = static_cast<__nv_bfloat16*>(o);
-  a.part = static_cast<uint8_t*>(partials);
+  if (a.split) {
+    a.cnt = static_cast<int*>(partials);
+    a.part = static_cast<uint8_t*>(partials) + counter_bytes(a);
+    if (!counters_zeroed && cudaMemsetAsync(a.cnt, 0, counter_bytes(a), s) != cudaSuccess)
+      return DPP_ERR_CUDA;
+  }
   a.status = status;
   a.wait_limit = wait_limit;
-  cudaError_t e = dpp_host::launch_pdl(tc_attn_kernel, dim3(a.G), dim3(ATTN_THREADS), ATTN_SMEM,
-                                       s, mq, mkf, mks, mvf, mvs, a);
-  if (e == cudaSuccess && a.split)
-    e = dpp_host::launch_pdl(attn_combine_kernel, dim3(a.U - a.W * a.G), dim3(256), 0, s, a);
+  const cudaError_t e = dpp_host::launch_pdl(tc_attn_kernel, dim3(a.G), dim3(ATTN_THREADS),
+                                             ATTN_SMEM, s, mq, mkf, mks, mvf, mvs, a);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
 

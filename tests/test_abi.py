@@ -61,9 +61,10 @@ def test_workspace_layout_sizes(lib):
             lo.attn_partial]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     # 320 attention units on (without a GPU, the library assumes) 152 SMs: one round of
-    # 152 whole units, the other 168 shared; partial records: 152 + 168 of 34816 bytes
+    # 152 whole units, the other 168 shared; two counters per shared unit (1536 bytes
+    # with padding), then 152 + 168 partial records of 34816 bytes
     part = dpp.attention_partials_size(2, 4096, 10, 4)
-    assert part == (152 + 168) * 34816 or torch.cuda.is_available()
+    assert part == 1536 + (152 + 168) * 34816 or torch.cuda.is_available()
     assert lo.attn_partial_bytes == part and lo.total >= lo.attn_partial + part
     n, nb = dpp.message_sizes(prm)
     blc = 2 * 4096 * 640
