@@ -90,6 +90,18 @@ int refresh_residual(const void* fresh, void* stale, int8_t* codes, float* scale
                      int64_t n, int dtype, void* stream);
 
 /*
+ * apply_residual -- the receiver's half of refresh_residual: applies a message to a
+ * copy of the stale buffer, in place.  ("A way to reduce bandwidth requirement for
+ * xDiT": each receiver adds the dequantised residual to its own stale copy.)
+ * For each element i of block j: stale_i = store(fmaf(codes[i], scales[j], f32(stale_i))),
+ * the sender's last step exactly, so a copy that equalled the sender's stale buffer
+ * before refresh_residual equals it bit for bit afterwards.  Layout, alignment and
+ * n == 0 as in refresh_residual; codes/scales are read only.
+ */
+int apply_residual(const int8_t* codes, const float* scales, void* stale, int64_t n, int dtype,
+                   void* stream);
+
+/*
  * halo_conv3x3 -- 3x3 "same" convolution of each row band with stale halo rows.
  * ("Benchmarking DistVAE", Glossary: halo; "OTIL for SDXL on 4x L40S", item 3.)
  *
@@ -156,6 +168,18 @@ int stale_kv_attention_split(const void* q, const void* k_fresh, const void* v_f
 
 /* ---------------------------------------------------------------- layer step */
 
+/* Where patch p's GroupNorm statistics come from at a DPP_STALE step (a DPP_SYNC step
+ * always uses every patch's fresh sums):
+ *   DPP_GN_SPLICED   its own fresh sums + the other patches' sums of the previous step
+ *                    (the stale global statistics; "OTIL for SDXL on 4x L40S", Periodic
+ *                    layer-context refresh);
+ *   DPP_GN_SYNC      every patch's fresh sums while the conv and the attention stay
+ *                    stale (same page, "GroupNorm sync without the rest");
+ *   DPP_GN_PREVIOUS  every patch's sums of the previous step, its own included. */
+#define DPP_GN_SPLICED 0
+#define DPP_GN_SYNC 1
+#define DPP_GN_PREVIOUS 2
+
 typedef struct dpp_layer_params {
   int B, H, W, C;  /* feature map [B,H,W,C] */
   int P;           /* row patches (virtual ranks); H % P == 0 */
@@ -165,6 +189,7 @@ typedef struct dpp_layer_params {
   int dtype;       /* DPP_F32 or DPP_BF16 */
   int refresh;     /* DPP_STALE only: 1 = refresh the state, 0 = leave it (no_sync) */
   float eps;       /* GroupNorm epsilon */
+  int gn_mode;     /* DPP_GN_SPLICED (0), DPP_GN_SYNC or DPP_GN_PREVIOUS */
 } dpp_layer_params;
 
 typedef struct dpp_layer_weights {
@@ -246,6 +271,21 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
 /* Synchronizes `stream` and returns the workspace's device status word
  * (DPP_OK, DPP_ERR_TIMEOUT, ...), or DPP_ERR_CUDA if the copy fails. */
 int dpp_read_device_status(const void* workspace, void* stream);
+
+/*
+ * dpp_apply_layer_message -- brings another rank's copy of the layer state up to date
+ * from the message of one DPP_STALE patch_layer_step with refresh (no counterpart
+ * on the pages as a call: it is the receiving end of the exchange that "A way to
+ * reduce bandwidth requirement for xDiT" describes, emulated on one device).
+ * codes, scales: the message in message order (dpp_message_elems / _blocks: K, V,
+ * then for each batch the P-1 halo ranges of y); gn_sums: the sender's fresh GroupNorm
+ * sums [B,P,G,2] fp32 (its state's gn_stats after the step), copied exactly.
+ * copy: the rank's gn_stats, y_stale, k_stale, v_stale (its codes/scales are not
+ * used).  A copy equal to the sender's state before the step equals it after.
+ */
+int dpp_apply_layer_message(const dpp_layer_params* prm, const int8_t* codes,
+                            const float* scales, const float* gn_sums,
+                            const dpp_layer_state* copy, void* stream);
 
 /*
  * patch_layer_step_noalloc -- patch_layer_step without a caller workspace.

@@ -10,7 +10,7 @@ Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 absolute end-to-end image quality of the method (seams, FID) is "parity
 unpinned": it needs trained weights and datasets that are not available.
 """
-from .layer import (SYNC, STALE, round_bf16, to_storage, patch_rows, gn_partial_stats,  # noqa: F401
+from .layer import (SYNC, STALE, GN_SPLICED, GN_SYNC, GN_PREVIOUS, round_bf16, to_storage, patch_rows, gn_partial_stats,  # noqa: F401
                     gn_apply_spliced, halo_conv3x3, linear, stale_kv_attention,
                     refresh_residual, apply_residual, halo_segments, layer_forward, layer_state_update,
                     patch_layer_step, empty_state)

@@ -40,6 +40,12 @@ import numpy as np
 SYNC = 0
 STALE = 1
 
+# Where a patch's GroupNorm statistics come from at a stale step.
+GN_SPLICED = 0   # own patch fresh, other patches from the previous step (the default)
+GN_SYNC = 1      # every patch fresh: "GroupNorm sync without the rest" ("OTIL for SDXL
+                 # on 4x L40S", What is implemented where), conv and attention stay stale
+GN_PREVIOUS = 2  # every patch from the previous step (the whole previous-step statistics)
+
 
 # ---------------------------------------------------------------- storage rounding
 def round_bf16(x) -> np.ndarray:
@@ -95,13 +101,16 @@ def gn_partial_stats(x: np.ndarray, P: int, G: int) -> np.ndarray:
 
 
 def gn_apply_spliced(x: np.ndarray, fresh: np.ndarray, stale: np.ndarray, gamma, beta,
-                     G: int, eps: float, dtype: str) -> np.ndarray:
+                     G: int, eps: float, dtype: str, gn_mode: int = GN_SPLICED) -> np.ndarray:
     """GroupNorm of each patch with statistics spliced from fresh and stale sums.
 
-    Patch p uses its own fresh sums plus every other patch's stale sums (the
-    stale global statistics of DistriFusion's GroupNorm; "OTIL for SDXL on 4x
-    L40S", Periodic layer-context refresh).  mu = S1/N, var = max(S2/N - mu^2, 0),
-    y = (x - mu) / sqrt(var + eps) * gamma_c + beta_c, N = H*W*C/G.
+    GN_SPLICED: patch p uses its own fresh sums plus every other patch's stale sums
+    (the stale global statistics of DistriFusion's GroupNorm; "OTIL for SDXL on 4x
+    L40S", Periodic layer-context refresh).  GN_SYNC: every patch's fresh sums
+    (same page, GroupNorm sync without the rest).  GN_PREVIOUS: every patch's
+    stale sums.  Own patch first, then the others in order.
+    mu = S1/N, var = max(S2/N - mu^2, 0), y = (x - mu) / sqrt(var + eps) * gamma_c
+    + beta_c, N = H*W*C/G.
     """
     B, H, W, C = x.shape
     P = fresh.shape[1]
@@ -110,11 +119,13 @@ def gn_apply_spliced(x: np.ndarray, fresh: np.ndarray, stale: np.ndarray, gamma,
     gamma = np.asarray(gamma, dtype=np.float64)
     beta = np.asarray(beta, dtype=np.float64)
     y = np.empty_like(x)
+    other = fresh if gn_mode == GN_SYNC else stale
+    own = stale if gn_mode == GN_PREVIOUS else fresh
     for p in range(P):
-        tot = fresh[:, p].copy()                              # [B, G, 2]
+        tot = own[:, p].copy()                                # [B, G, 2]
         for q in range(P):
             if q != p:
-                tot += stale[:, q]
+                tot += other[:, q]
         mu = tot[..., 0] / N
         var = np.maximum(tot[..., 1] / N - mu * mu, 0.0)
         rstd = 1.0 / np.sqrt(var + eps)
@@ -249,7 +260,7 @@ def halo_segments(H: int, W: int, C: int, P: int):
 
 # ---------------------------------------------------------------- whole layer
 def layer_forward(x, state, wts, P: int, G: int, heads: int, eps: float, dtype: str,
-                  mode: int, rows=None):
+                  mode: int, rows=None, gn_mode: int = GN_SPLICED):
     """Steps a1-a6 for all P virtual ranks; returns a dict of every stored tensor.
 
     SYNC (the warm-up / refresh step, "DistriFusion", How It Works; "OTIL for
@@ -261,7 +272,8 @@ def layer_forward(x, state, wts, P: int, G: int, heads: int, eps: float, dtype: 
     x = np.asarray(x, np.float64)
     fresh_stats = gn_partial_stats(x, P, G)
     stale_stats = fresh_stats if mode == SYNC else np.asarray(state["gn_stats"], np.float64)
-    y = gn_apply_spliced(x, fresh_stats, stale_stats, wts["gamma"], wts["beta"], G, eps, dtype)
+    y = gn_apply_spliced(x, fresh_stats, stale_stats, wts["gamma"], wts["beta"], G, eps, dtype,
+                         gn_mode)
     y_st = y if mode == SYNC else state["y_stale"]
     h = halo_conv3x3(y, y_st, wts["w_conv"], P, dtype)
     hf = h.reshape(B, L, C)
@@ -322,9 +334,9 @@ def layer_state_update(fwd: dict, state: dict, P: int, dtype: str, mode: int, re
 
 
 def patch_layer_step(x, state, wts, P: int, G: int, heads: int, eps: float, dtype: str,
-                     mode: int, refresh: bool = True):
+                     mode: int, refresh: bool = True, gn_mode: int = GN_SPLICED):
     """One layer pass of all P virtual ranks followed by the state update."""
-    fwd = layer_forward(x, state, wts, P, G, heads, eps, dtype, mode)
+    fwd = layer_forward(x, state, wts, P, G, heads, eps, dtype, mode, gn_mode=gn_mode)
     new_state, codes, scales = layer_state_update(fwd, state, P, dtype, mode, refresh)
     return fwd, new_state, codes, scales
 

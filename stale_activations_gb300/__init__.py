@@ -36,7 +36,7 @@ class DppError(RuntimeError):
 class LayerParams(ctypes.Structure):
     _fields_ = [("B", _c_int), ("H", _c_int), ("W", _c_int), ("C", _c_int), ("P", _c_int),
                 ("G", _c_int), ("heads", _c_int), ("head_dim", _c_int), ("dtype", _c_int),
-                ("refresh", _c_int), ("eps", ctypes.c_float)]
+                ("refresh", _c_int), ("eps", ctypes.c_float), ("gn_mode", _c_int)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -58,7 +58,7 @@ class WorkspaceLayout(ctypes.Structure):
 _lib = None
 EXPORTS = ("dpp_status_string", "dpp_version", "refresh_residual", "halo_conv3x3",
            "stale_kv_attention", "stale_kv_attention_split", "dpp_attention_partials_size",
-           "dpp_workspace_query", "dpp_workspace_size", "dpp_message_elems",
+           "apply_residual", "dpp_apply_layer_message", "dpp_workspace_query", "dpp_workspace_size", "dpp_message_elems",
            "dpp_message_blocks", "patch_layer_step", "patch_layer_step_timed",
            "dpp_read_device_status", "dpp_layer_kernel_count", "patch_layer_step_noalloc")
 
@@ -80,6 +80,11 @@ def load(build_if_missing: bool = False):
     lib.dpp_version.restype = _c_int
     lib.refresh_residual.restype = _c_int
     lib.refresh_residual.argtypes = [_c_void, _c_void, _c_void, _c_void, I64, _c_int, _c_void]
+    lib.apply_residual.restype = _c_int
+    lib.apply_residual.argtypes = [_c_void, _c_void, _c_void, I64, _c_int, _c_void]
+    lib.dpp_apply_layer_message.restype = _c_int
+    lib.dpp_apply_layer_message.argtypes = [P(LayerParams), _c_void, _c_void, _c_void,
+                                            P(LayerState), _c_void]
     lib.halo_conv3x3.restype = _c_int
     lib.halo_conv3x3.argtypes = [_c_void] * 4 + [_c_int] * 7 + [_c_void, _c_void]
     lib.stale_kv_attention.restype = _c_int
@@ -158,6 +163,24 @@ def refresh_residual(fresh, stale, codes, scales, stream=None):
            "refresh_residual")
 
 
+def apply_residual(codes, scales, stale, stream=None):
+    """The receiver's half of refresh_residual: stale <- store(fmaf(code, scale, stale))."""
+    lib = load()
+    _check(lib.apply_residual(_ptr(codes), _ptr(scales), _ptr(stale), stale.numel(),
+                              dtype_code(stale), _stream(stream)), "apply_residual")
+
+
+def apply_layer_message(prm: "LayerParams", codes, scales, gn_sums, copy: dict, stream=None):
+    """Applies one stale step's message (codes, scales, the sender's GroupNorm sums) to
+    another rank's copy of the layer state (a dict like alloc_layer's)."""
+    st = LayerState()
+    for k in ("gn_stats", "y_stale", "k_stale", "v_stale"):
+        setattr(st, k, _ptr(copy[k]))
+    _check(load().dpp_apply_layer_message(ctypes.byref(prm), _ptr(codes), _ptr(scales),
+                                          _ptr(gn_sums), ctypes.byref(st), _stream(stream)),
+           "dpp_apply_layer_message")
+
+
 def halo_conv3x3(y_fresh, y_stale, w, out, P: int, dev_status=None, stream=None):
     lib = load()
     B, H, W, Cin = y_fresh.shape
@@ -196,8 +219,13 @@ def stale_kv_attention_split(q, k_fresh, v_fresh, k_stale, v_stale, o, heads: in
            "stale_kv_attention_split")
 
 
-def make_params(B, H, W, C, P, G, heads, dtype, refresh=True, eps=1e-5, head_dim=64):
-    return LayerParams(B, H, W, C, P, G, heads, head_dim, dtype, 1 if refresh else 0, eps)
+GN_SPLICED, GN_SYNC, GN_PREVIOUS = 0, 1, 2
+
+
+def make_params(B, H, W, C, P, G, heads, dtype, refresh=True, eps=1e-5, head_dim=64,
+                gn_mode=GN_SPLICED):
+    return LayerParams(B, H, W, C, P, G, heads, head_dim, dtype, 1 if refresh else 0, eps,
+                       gn_mode)
 
 
 def workspace_layout(prm: LayerParams) -> WorkspaceLayout:

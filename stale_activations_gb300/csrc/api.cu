@@ -82,6 +82,7 @@ int check_layer(const dpp_layer_params* p) {
   const int vec = p->dtype == DPP_BF16 ? 8 : 4;
   if (p->C % vec || p->C / vec > 256) return DPP_ERR_SHAPE;
   if (p->refresh != 0 && p->refresh != 1) return DPP_ERR_ARG;
+  if (p->gn_mode < DPP_GN_SPLICED || p->gn_mode > DPP_GN_PREVIOUS) return DPP_ERR_ARG;
   if (!(p->eps >= 0.f)) return DPP_ERR_ARG;
   rc = check_conv(p->B, p->H, p->W, p->C, p->C, p->P, p->dtype);
   if (rc) return rc;
@@ -196,6 +197,22 @@ int refresh_residual(const void* fresh, void* stale, int8_t* codes, float* scale
     return DPP_ERR_ALIGN;
   dpp::RefreshSeg sg{fresh, stale, codes, scales, (long long)n, 1, 0};
   return refresh_segments(&sg, 1, dtype, static_cast<cudaStream_t>(stream));
+}
+
+int apply_residual(const int8_t* codes, const float* scales, void* stale, int64_t n, int dtype,
+                   void* stream) {
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  if (n < 0) return DPP_ERR_SHAPE;
+  if (n == 0) return DPP_OK;
+  if (!codes || !scales || !stale) return DPP_ERR_NULL;
+  if (!aligned16(codes) || !aligned16(stale) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return DPP_ERR_ALIGN;
+  dpp::ApplyTable tab{};
+  tab.nseg = 1;
+  tab.seg[0] = dpp::ApplySeg{codes, scales, stale, (long long)n, 1, 0};
+  tab.blk_start[1] = cdiv(n, 128);
+  return dpp::launch_apply(tab, dtype, static_cast<cudaStream_t>(stream));
 }
 
 int halo_conv3x3(const void* y_fresh, const void* y_stale, const void* w, void* out, int B, int H,
@@ -343,7 +360,7 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
                        ? dpp::tc_attention_counters(p.B, L, p.heads, p.P)
                        : 0;
   rc = dpp::launch_gn(x, y, gn_partial, sync ? nullptr : st->gn_stats, gn_fresh, wts->gamma,
-                      wts->beta, g, p.eps, sync ? 1 : 0, p.dtype, status,
+                      wts->beta, g, p.eps, sync ? DPP_GN_SYNC : p.gn_mode, p.dtype, status,
                       reinterpret_cast<int*>(ws + lo.attn_partial), ncnt, s);
   if (rc || (rc = mark(1))) return rc;
   // a3: halo conv, halo rows from the stale conv input (fresh at the synchronous step)
@@ -419,6 +436,50 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
   tab.copy_dst = st->gn_stats;
   if ((rc = dpp::launch_refresh(tab, p.dtype, s))) return rc;
   return mark(6);
+}
+
+int dpp_apply_layer_message(const dpp_layer_params* prm, const int8_t* codes,
+                            const float* scales, const float* gn_sums,
+                            const dpp_layer_state* copy, void* stream) {
+  int rc = check_layer(prm);
+  if (rc) return rc;
+  if (!codes || !scales || !gn_sums || !copy || !copy->gn_stats || !copy->y_stale ||
+      !copy->k_stale || !copy->v_stale)
+    return DPP_ERR_NULL;
+  const dpp_layer_params& p = *prm;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t es = esize(p.dtype);
+  const long long blc = (long long)p.B * p.H * p.W * p.C;
+  const size_t halo_bytes = 2ull * p.W * p.C * es;
+  const size_t band_bytes = (size_t)(p.H / p.P) * p.W * p.C * es;
+  const size_t img_bytes = (size_t)p.H * p.W * p.C * es;
+  dpp::ApplyTable tab{};
+  long long coff = 0, soff = 0;
+  auto add = [&](void* stl, long long n) -> int {
+    const bool ok = aligned16(stl) && aligned16(codes + coff);
+    tab.seg[tab.nseg] = dpp::ApplySeg{codes + coff, scales + soff, stl, n, ok ? 1 : 0, 0};
+    tab.blk_start[tab.nseg + 1] = tab.blk_start[tab.nseg] + cdiv(n, 128);
+    ++tab.nseg;
+    coff += n;
+    soff += cdiv(n, 128);
+    if (tab.nseg == dpp::kMaxRefreshSegs) {
+      const int r = dpp::launch_apply(tab, p.dtype, s);
+      tab.nseg = 0;
+      return r;
+    }
+    return DPP_OK;
+  };
+  if ((rc = add(copy->k_stale, blc)) || (rc = add(copy->v_stale, blc))) return rc;
+  for (int b = 0; b < p.B; ++b)
+    for (int pp = 1; pp < p.P; ++pp) {
+      const size_t off = b * img_bytes + pp * band_bytes - halo_bytes / 2;
+      if ((rc = add(static_cast<char*>(copy->y_stale) + off, 2ll * p.W * p.C))) return rc;
+    }
+  // the last launch also copies the GroupNorm sums
+  tab.copy_n = p.B * p.P * p.G * 2;
+  tab.copy_src = gn_sums;
+  tab.copy_dst = copy->gn_stats;
+  return dpp::launch_apply(tab, p.dtype, s);
 }
 
 int dpp_read_device_status(const void* workspace, void* stream) {

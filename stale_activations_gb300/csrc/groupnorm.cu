@@ -8,7 +8,8 @@
 //   per-channel sums are reduced across the block in shared memory and then
 //   folded into groups in a fixed order (deterministic, no atomics).
 // gn_apply: patch p's statistics = its own fresh sums (summed over chunks) +
-//   the other patches' stale sums (fresh ones at the synchronous step);
+//   the other patches' stale sums (fresh ones at the synchronous step and under
+//   DPP_GN_SYNC; under DPP_GN_PREVIOUS its own sums are the stale ones too);
 //   mu = S1/N, var = max(S2/N - mu^2, 0), y = (x - mu) * rstd * gamma + beta.
 // Both are HBM-bound streams: stats reads 1 element, apply reads 1 and writes 1.
 #include "groupnorm.cuh"
@@ -90,23 +91,24 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
                                                        float* __restrict__ fresh_out,
                                                        const float* __restrict__ gamma,
                                                        const float* __restrict__ beta, GnDims g,
-                                                       float eps, int sync) {
+                                                       float eps, int mode) {
   constexpr int VEC = Vec<T>::N;
   extern __shared__ float sm[];  // mean[C], scale[C], beta[C], group sums [P][G][2]
+  const bool all_fresh = mode == DPP_GN_SYNC;
   float* s_mu = sm;
   float* s_sc = sm + g.C;
   float* s_be = sm + 2 * g.C;
-  float* s_tot = sm + 3 * g.C;  // [P][G][2] fresh sums of every patch (sync) or own
+  float* s_tot = sm + 3 * g.C;  // [P][G][2]: own patch fresh, others fresh or stale
   const int chunk = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  // fresh sums over chunks, for own patch (and every patch at the synchronous step);
+  // fresh sums over chunks, for own patch (and every patch when all are fresh);
   // eight independent partial sums so that the chunk loads are in flight together
   for (int idx = tid; idx < g.P * g.G * 2; idx += blockDim.x) {
     const int q = idx / (g.G * 2), r = idx % (g.G * 2);
     float v = 0.f;
-    if (sync || q == p) {
+    if (all_fresh || q == p) {
       const float* src = partial + (((long long)b * g.P + q) * g.nchunk) * g.G * 2 + r;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       int c = 0;
@@ -128,9 +130,12 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
   }
   const int cg = g.C / g.G;
   const double invN = 1.0 / ((double)g.H * g.W * cg);
+  // own patch first (its previous-step sums under DPP_GN_PREVIOUS), then the others
+  const float* own = mode == DPP_GN_PREVIOUS ? stale_stats + ((long long)b * g.P + p) * g.G * 2
+                                             : s_tot + p * g.G * 2;
   for (int c = tid; c < g.C; c += blockDim.x) {
     const int gi = c / cg;
-    float S1 = s_tot[p * g.G * 2 + gi * 2], S2 = s_tot[p * g.G * 2 + gi * 2 + 1];
+    float S1 = own[gi * 2], S2 = own[gi * 2 + 1];
     for (int q = 0; q < g.P; ++q)
       if (q != p) { S1 += s_tot[q * g.G * 2 + gi * 2]; S2 += s_tot[q * g.G * 2 + gi * 2 + 1]; }
     const float mu = (float)(S1 * invN);
@@ -194,7 +199,7 @@ size_t gn_partial_bytes(const GnDims& g) {
 }
 
 int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, float* fresh_out,
-              const float* gamma, const float* beta, const GnDims& g, float eps, int sync,
+              const float* gamma, const float* beta, const GnDims& g, float eps, int mode,
               int dtype, int* status_to_zero, int* zero_ints, int nzero, cudaStream_t stream) {
   dim3 grid(g.nchunk, g.P, g.B);
   const int VEC = dtype == DPP_BF16 ? 8 : 4;
@@ -211,7 +216,7 @@ int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, 
     if (e == cudaSuccess)
       e = launch_pdl(gn_apply_kernel<__nv_bfloat16>, grid, dim3(256), app_bytes, stream, xs,
                      static_cast<__nv_bfloat16*>(y), (const float*)partial, stale_stats, fresh_out,
-                     gamma, beta, g, eps, sync);
+                     gamma, beta, g, eps, mode);
   } else {
     auto* xs = static_cast<const float*>(x);
     e = launch_pdl(gn_stats_kernel<float>, grid, dim3(256), red_bytes, stream, xs, partial, g,
@@ -219,7 +224,7 @@ int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, 
     if (e == cudaSuccess)
       e = launch_pdl(gn_apply_kernel<float>, grid, dim3(256), app_bytes, stream, xs,
                      static_cast<float*>(y), (const float*)partial, stale_stats, fresh_out, gamma,
-                     beta, g, eps, sync);
+                     beta, g, eps, mode);
   }
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }

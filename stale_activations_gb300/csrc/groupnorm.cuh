@@ -13,12 +13,14 @@ struct GnDims {
 GnDims make_gn_dims(int B, int H, int W, int C, int P, int G);
 size_t gn_partial_bytes(const GnDims& g);
 
-// Launches the stats and apply kernels.  stale_stats may be NULL when sync != 0.
+// Launches the stats and apply kernels.  mode: DPP_GN_SPLICED, DPP_GN_SYNC (every patch
+// fresh; the synchronous step) or DPP_GN_PREVIOUS; stale_stats may be NULL under
+// DPP_GN_SYNC.
 // fresh_out (may be NULL) receives the [B,P,G,2] fresh sums.  The stats kernel
 // zeroes *status_to_zero first (if non-NULL), and the nzero ints at zero_ints (the next
 // kernels' counters).
 int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, float* fresh_out,
-              const float* gamma, const float* beta, const GnDims& g, float eps, int sync,
+              const float* gamma, const float* beta, const GnDims& g, float eps, int mode,
               int dtype, int* status_to_zero, int* zero_ints, int nzero, cudaStream_t stream);
 
 }  // namespace dpp

@@ -218,4 +218,77 @@ int launch_refresh(const RefreshTable& tab, int dtype, cudaStream_t stream) {
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ receiver side
+// One 128-element block per half warp, 8 elements per lane (codes as one 8-byte load),
+// stale streamed in and out.  The code byte becomes an exact float without a
+// conversion: the bits of 1.5 * 2^23 plus q (|q| <= 127) are the float 1.5 * 2^23 + q.
+template <typename T>
+__device__ __forceinline__ void apply8(const int8_t* cd, float s, T* st) {
+  const uint2 c = *reinterpret_cast<const uint2*>(cd);
+  float sv[8], nv[8];
+  if constexpr (sizeof(T) == 2) {
+    unpack16(__ldcs(reinterpret_cast<const uint4*>(st)), sv);
+  } else {
+    float a[4], b[4];
+    unpack16(__ldcs(reinterpret_cast<const uint4*>(st)), a);
+    unpack16(__ldcs(reinterpret_cast<const uint4*>(st) + 1), b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { sv[i] = a[i]; sv[4 + i] = b[i]; }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int q = (int)(int8_t)((i < 4 ? c.x : c.y) >> (8 * (i & 3)));
+    const float qf = __int_as_float(0x4B400000 + q) - kRoundMagic;
+    nv[i] = __fmaf_rn(qf, s, sv[i]);
+  }
+  store8<T>(st, nv);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) apply_kernel(const __grid_constant__ ApplyTable tab) {
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 15;
+  const long long group = (long long)(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 2 +
+                          (lane >> 4);
+  const long long stride = (long long)gridDim.x * (blockDim.x >> 5) * 2;
+  const long long total = tab.blk_start[tab.nseg];
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < tab.copy_n; i += blockDim.x) tab.copy_dst[i] = tab.copy_src[i];
+  int seg = 0;
+  for (long long gb = group; gb < total; gb += stride) {
+    while (gb >= tab.blk_start[seg + 1]) ++seg;
+    const ApplySeg& sg = tab.seg[seg];
+    const long long j = gb - tab.blk_start[seg];
+    const long long e0 = j * 128;
+    const int nb = (int)min(128ll, sg.n - e0);
+    const float s = sg.scales[j];
+    T* st = static_cast<T*>(sg.stale) + e0;
+    const int8_t* cd = sg.codes + e0;
+    if (nb == 128 && sg.vec_ok) {
+      apply8<T>(cd + sub * 8, s, st + sub * 8);
+    } else {  // ragged or misaligned: element by element, strided by 16
+      for (int e = sub; e < nb; e += 16)
+        st[e] = from_f32<T>(__fmaf_rn((float)cd[e], s, to_f32(st[e])));
+    }
+  }
+}
+
+int launch_apply(const ApplyTable& tab, int dtype, cudaStream_t stream) {
+  const long long total = tab.blk_start[tab.nseg];
+  if (total == 0 && tab.copy_n == 0) return DPP_OK;
+  const int threads = 256;
+  const long long groups_per_cta = threads / 32 * 2 * 4;  // ~4 blocks per half warp
+  long long want = (total + groups_per_cta - 1) / groups_per_cta;
+  const long long cap = (long long)dpp_host::sm_count() * 8;
+  const int grid = (int)(want < 1 ? 1 : want < cap ? want : cap);
+  const cudaError_t e =
+      dtype == DPP_BF16
+          ? dpp_host::launch_pdl(apply_kernel<__nv_bfloat16>, dim3(grid), dim3(threads), 0, stream,
+                                 tab)
+          : dpp_host::launch_pdl(apply_kernel<float>, dim3(grid), dim3(threads), 0, stream, tab);
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
+}
+
 }  // namespace dpp

@@ -73,7 +73,8 @@ def test_workspace_layout_sizes(lib):
 
 
 @pytest.mark.parametrize("kw", [dict(H=63), dict(P=3), dict(C=600, heads=10), dict(G=7),
-                                dict(heads=5), dict(dtype=7), dict(W=48)])
+                                dict(heads=5), dict(dtype=7), dict(W=48), dict(gn_mode=3),
+                                dict(gn_mode=-1)])
 def test_invalid_params_rejected(lib, kw):
     prm = _params(**kw)
     assert lib.dpp_workspace_size(ctypes.byref(prm)) == 0
@@ -96,6 +97,12 @@ def test_host_checks_without_launch(lib):
     assert lib.refresh_residual(vp(16), vp(16), vp(16), vp(16), 5, 9, None) == 4
     assert lib.refresh_residual(vp(16), vp(16), vp(16), vp(16), -1, dpp.BF16, None) == 2
     assert lib.refresh_residual(vp(16), vp(24), vp(16), vp(16), 5, dpp.BF16, None) == 3
+    # the receiver's half: same argument rules
+    assert lib.apply_residual(None, None, None, 0, dpp.BF16, None) == 0
+    assert lib.apply_residual(None, vp(16), vp(16), 5, dpp.BF16, None) == 1
+    assert lib.apply_residual(vp(16), vp(16), vp(16), 5, 9, None) == 4
+    assert lib.apply_residual(vp(16), vp(16), vp(24), 5, dpp.BF16, None) == 3
+    assert lib.apply_residual(vp(16), vp(18), vp(16), 5, dpp.BF16, None) == 3
     assert lib.halo_conv3x3(None, None, None, None, 1, 8, 8, 64, 128, 2, dpp.BF16, None, None) == 1
     a = vp(256)
     assert lib.halo_conv3x3(a, a, a, a, 1, 9, 64, 64, 128, 2, dpp.BF16, None, None) == 2

@@ -162,3 +162,97 @@ def test_layer_no_sync_leaves_state():
     torch.cuda.synchronize()
     for k in before:
         assert torch.equal(before[k], state[k]), k
+
+
+@pytest.mark.parametrize("gn_mode", [dpp.GN_SYNC, dpp.GN_PREVIOUS])
+@pytest.mark.parametrize("name", ["tiny_f32", "small_bf16"])
+def test_layer_gn_modes(name, gn_mode):
+    """The GroupNorm statistics variants at a stale step: DPP_GN_SYNC (every patch
+    fresh, conv and attention still stale) and DPP_GN_PREVIOUS (every patch from the
+    previous step).  The GroupNorm stage on the GPU's own bytes, then end to end."""
+    cfg = CFGS[name]
+    tol = TOL_BF16 if cfg.dtype == "bf16" else TOL_F32
+    wts, wn, x, _, _, ostate = _setup(cfg)
+    prm = dpp.make_params(cfg.B, cfg.H, cfg.W, cfg.C, cfg.P, cfg.G, cfg.heads,
+                          dpp.BF16 if cfg.dtype == "bf16" else dpp.F32, eps=cfg.eps,
+                          gn_mode=gn_mode)
+    state, ws = _gpu_state_from(ostate, cfg, prm)
+    out = torch.empty(cfg.B, cfg.H, cfg.W, cfg.C, dtype=x.dtype, device="cuda")
+    dpp.patch_layer_step(prm, {k: t.cuda() for k, t in wts.items()}, state, x.cuda(), out,
+                         dpp.STALE, ws)
+    assert dpp.read_device_status(ws) == 0
+    v = {k: np64(t) for k, t in dpp.workspace_views(prm, ws).items()}
+    fresh = oracle.gn_partial_stats(np64(x), cfg.P, cfg.G)
+    y = oracle.gn_apply_spliced(np64(x), fresh, ostate["gn_stats"], wn["gamma"], wn["beta"],
+                                cfg.G, cfg.eps, cfg.dtype, gn_mode)
+    assert rel_err(v["y"], y) < tol
+    # the state keeps this step's own fresh sums whatever the mode
+    np.testing.assert_array_equal(np64(state["gn_stats"]), v["gn_fresh"])
+    fwd = oracle.layer_forward(np64(x), ostate, wn, cfg.P, cfg.G, cfg.heads, cfg.eps, cfg.dtype,
+                               oracle.STALE, gn_mode=gn_mode)
+    assert rel_err(np64(out), fwd["out"]) < (TOL_CHAIN_BF16 if cfg.dtype == "bf16" else TOL_F32)
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "small_bf16"])
+def test_layer_periodic_refresh_sequence(name):
+    """Periodic layer-context refresh ("OTIL for SDXL on 4x L40S"): a synchronous step
+    every third step, stale steps with the compressed refresh in between.  At every
+    step the output matches the oracle run on the same state, and the new state is
+    bit-exactly the oracle's state update fed this step's GPU tensors (a fresh K that
+    differs by one rounding may legitimately change a code)."""
+    cfg = CFGS[name]
+    wts, wn, _, _, _, _ = _setup(cfg)
+    prm = _params(cfg)
+    state, ws = dpp.alloc_layer(prm)
+    wd = {k: t.cuda() for k, t in wts.items()}
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    tol = TOL_CHAIN_BF16 if cfg.dtype == "bf16" else TOL_F32
+    names = ("gn_stats", "y_stale", "k_stale", "v_stale")
+    for i, mode in enumerate([dpp.SYNC, dpp.STALE, dpp.STALE, dpp.SYNC, dpp.STALE]):
+        x, _ = synth.layer_inputs(cfg, seed=10 + i)
+        ost = {k: np64(state[k]).reshape(oracle.empty_state(cfg.B, cfg.H, cfg.W, cfg.C, cfg.P,
+                                                             cfg.G)[k].shape) for k in names}
+        out = torch.empty(cfg.B, cfg.H, cfg.W, cfg.C, dtype=dt, device="cuda")
+        dpp.patch_layer_step(prm, wd, state, x.cuda(), out, mode, ws)
+        assert dpp.read_device_status(ws) == 0
+        omode = oracle.SYNC if mode == dpp.SYNC else oracle.STALE
+        fwd = oracle.layer_forward(np64(x), ost, wn, cfg.P, cfg.G, cfg.heads, cfg.eps, cfg.dtype,
+                                   omode)
+        assert rel_err(np64(out), fwd["out"]) < tol, (i, mode)
+        v = {k: np64(t) for k, t in dpp.workspace_views(prm, ws).items()}
+        gpu_fwd = dict(gn_fresh=v["gn_fresh"], y=v["y"], k=v["k"], v=v["v"])
+        new, _, _ = oracle.layer_state_update(gpu_fwd, ost, cfg.P, cfg.dtype, omode, True)
+        for k in names:
+            np.testing.assert_array_equal(np64(state[k]).reshape(new[k].shape),
+                                          np64(torch.from_numpy(new[k]).to(torch.float32))
+                                          if k == "gn_stats" else new[k], err_msg=f"{i} {k}")
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "small_bf16"])
+def test_layer_message_keeps_rank_copies_identical(name):
+    """The exchange of the multi-GPU method on one device: besides the sender's state,
+    P-1 other ranks each hold their own copy of it and receive only the messages
+    (codes, scales and the GroupNorm sums) of each stale step.  After a synchronous
+    step and three stale steps every copy equals the sender's state bit for bit."""
+    cfg = CFGS[name]
+    wts, _, _, _, _, _ = _setup(cfg)
+    prm = _params(cfg)
+    state, ws = dpp.alloc_layer(prm)
+    wd = {k: t.cuda() for k, t in wts.items()}
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    out = torch.empty(cfg.B, cfg.H, cfg.W, cfg.C, dtype=dt, device="cuda")
+    x, _ = synth.layer_inputs(cfg, seed=20)
+    dpp.patch_layer_step(prm, wd, state, x.cuda(), out, dpp.SYNC, ws)
+    copies = [{k: state[k].clone() for k in ("gn_stats", "y_stale", "k_stale", "v_stale")}
+              for _ in range(cfg.P - 1)]
+    for i in range(3):
+        x, _ = synth.layer_inputs(cfg, seed=21 + i)
+        dpp.patch_layer_step(prm, wd, state, x.cuda(), out, dpp.STALE, ws)
+        assert dpp.read_device_status(ws) == 0
+        for c in copies:
+            dpp.apply_layer_message(prm, state["codes"], state["scales"], state["gn_stats"], c)
+        torch.cuda.synchronize()
+        for r, c in enumerate(copies):
+            for k in c:
+                assert torch.equal(c[k], state[k]), (i, r, k)
+    assert state["k_stale"].float().abs().sum().item() > 0  # a non-trivial state

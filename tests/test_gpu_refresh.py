@@ -84,3 +84,16 @@ def test_refresh_rejects_misaligned():
     with pytest.raises(dpp.DppError) as e:
         dpp.refresh_residual(x[1:513], x[1:513], c[:512], sc[:4])
     assert e.value.code == 3
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("n", [1, 127, 129, 1000, 128 * 997 + 77])
+def test_apply_residual_matches_oracle_bitexact(dtype, n):
+    """The receiver's half: the oracle's message (codes, scales) applied on the GPU to a
+    copy of the old stale buffer gives the oracle's refreshed buffer, bit for bit."""
+    fresh, stale = synth.refresh_inputs(n, dtype, seed=n + 3)
+    en, ec, es = oracle.refresh_residual(np64(fresh), np64(stale), dtype)
+    copy = stale.clone().cuda()
+    dpp.apply_residual(torch.from_numpy(ec).cuda(), torch.from_numpy(es).cuda(), copy)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(np64(copy), en)

@@ -87,6 +87,45 @@ def test_gn_stale_uses_only_other_patches():
     assert np.abs(y1[:, :2] - y2[:, :2]).max() > 1e-3               # others changed
 
 
+@pytest.mark.parametrize("P", [2, 4])
+def test_gn_sync_mode_ignores_stale_and_equals_torch(P):
+    """GN_SYNC (GroupNorm sync without the rest): every patch uses every patch's fresh
+    sums, so any stale state gives textbook GroupNorm of the whole map."""
+    B, H, W, C, G = 2, 16, 8, 24, 4
+    x = RNG.standard_normal((B, H, W, C)) * 2 + 0.5
+    gamma, beta = RNG.standard_normal(C), RNG.standard_normal(C)
+    s = oracle.gn_partial_stats(x, P, G)
+    junk = RNG.standard_normal(s.shape) * 100.0
+    y = oracle.gn_apply_spliced(x, s, junk, gamma, beta, G, 1e-5, "f64", oracle.GN_SYNC)
+    xt = torch.from_numpy(x).permute(0, 3, 1, 2)
+    ref = torch.nn.functional.group_norm(xt, G, torch.from_numpy(gamma), torch.from_numpy(beta),
+                                         eps=1e-5).permute(0, 2, 3, 1).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-10)
+
+
+def test_gn_previous_mode_uses_only_the_stale_statistics():
+    """GN_PREVIOUS: every patch is normalised with the previous step's statistics alone.
+    With the stale sums of another map x2 the output is (x - mean(x2)) / sqrt(var(x2) +
+    eps) per group, the biased mean and variance of x2 taken directly (numpy)."""
+    B, H, W, C, G, P = 2, 8, 4, 12, 3, 4
+    x = RNG.standard_normal((B, H, W, C))
+    x2 = RNG.standard_normal((B, H, W, C)) * 1.5 - 0.25
+    f = oracle.gn_partial_stats(x, P, G)
+    st = oracle.gn_partial_stats(x2, P, G)
+    y = oracle.gn_apply_spliced(x, f, st, np.ones(C), np.zeros(C), G, 1e-5, "f64",
+                                oracle.GN_PREVIOUS)
+    g2 = x2.reshape(B, H, W, G, C // G)
+    mu = g2.mean(axis=(1, 2, 4))
+    var = g2.var(axis=(1, 2, 4))
+    ref = ((x.reshape(B, H, W, G, C // G) - mu[:, None, None, :, None]) /
+           np.sqrt(var[:, None, None, :, None] + 1e-5)).reshape(B, H, W, C)
+    np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-10)
+    # the fresh sums do not enter at all
+    y2 = oracle.gn_apply_spliced(x, f * 3.0 + 1.0, st, np.ones(C), np.zeros(C), G, 1e-5, "f64",
+                                 oracle.GN_PREVIOUS)
+    np.testing.assert_array_equal(y, y2)
+
+
 # ------------------------------------------------------------------ halo conv
 @pytest.mark.parametrize("P", [1, 2, 4])
 def test_conv_unbanded_matches_torch_conv2d(P):
@@ -353,13 +392,32 @@ def test_layer_stale_P1_equals_sync():
     np.testing.assert_array_equal(a["out"], b["out"])
 
 
-def test_layer_stale_with_synced_state_equals_sync():
+@pytest.mark.parametrize("gn_mode", [0, 1, 2])
+def test_layer_stale_with_synced_state_equals_sync(gn_mode):
     B, H, W, C, G, heads, P = 2, 16, 4, 16, 4, 2, 4
     x, wts = _layer_case(B, H, W, C, G, heads)
     st0 = oracle.empty_state(B, H, W, C, P, G)
     fwd, st, _, _ = oracle.patch_layer_step(x, st0, wts, P, G, heads, 1e-5, "f32", oracle.SYNC)
-    again = oracle.layer_forward(x, st, wts, P, G, heads, 1e-5, "f32", oracle.STALE)
+    again = oracle.layer_forward(x, st, wts, P, G, heads, 1e-5, "f32", oracle.STALE,
+                                 gn_mode=gn_mode)
     np.testing.assert_allclose(again["out"], fwd["out"], rtol=1e-6, atol=1e-7)
+
+
+def test_layer_gn_sync_mode_keeps_conv_and_attention_stale():
+    """GN_SYNC changes only the GroupNorm: its y equals the SYNC step's y on the same x
+    while the attention still reads the stale K/V (so out differs from SYNC's)."""
+    B, H, W, C, G, heads, P = 1, 8, 4, 16, 4, 2, 2
+    x, wts = _layer_case(B, H, W, C, G, heads)
+    st0 = oracle.empty_state(B, H, W, C, P, G)
+    x_prev = x + 0.5 * RNG.standard_normal(x.shape)
+    _, st, _, _ = oracle.patch_layer_step(x_prev, st0, wts, P, G, heads, 1e-5, "f32", oracle.SYNC)
+    sync = oracle.layer_forward(x, st, wts, P, G, heads, 1e-5, "f32", oracle.SYNC)
+    gs = oracle.layer_forward(x, st, wts, P, G, heads, 1e-5, "f32", oracle.STALE,
+                              gn_mode=oracle.GN_SYNC)
+    np.testing.assert_array_equal(gs["y"], sync["y"])
+    # the conv still takes its halo rows from the old state, the attention its K/V
+    assert np.linalg.norm(gs["h"] - sync["h"]) > 1e-3 * np.linalg.norm(sync["h"])
+    assert not np.array_equal(gs["out"], sync["out"])
 
 
 def test_layer_stale_state_changes_only_remote_dependence():
