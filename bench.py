@@ -34,8 +34,8 @@ if ROOT not in sys.path:
 
 METRIC = "patch-layer steps/s; attention TFLOP/s & refresh GB/s as % of GB300 roofline"
 # dram__bytes_read.sum + dram__bytes_write.sum of one SDXL-1024 attention launch from an
-# ncu capture of the current kernel version (None until one is taken)
-ATTN_TRAFFIC_BYTES = None
+# ncu capture of the current kernel version (profiles/tc_attn_kernel_sdxl.md)
+ATTN_TRAFFIC_BYTES = 52.515072e6 + 1.034496e6
 WORKLOAD = "sdxl1024_mid_b2_64x64_c640_p4_bf16"
 
 
@@ -321,8 +321,8 @@ def run_gpu(args):
     roofline = {"kernel": "stale_kv_attention (tc_attn_kernel)", "bound": "tensor",
                 "achieved": attn_tfs, "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
                 "frac": attn_tfs / peaks["bf16_sus"], "traffic": ATTN_TRAFFIC_BYTES,
-                "traffic_note": "dram read+write bytes per launch (ncu); algorithmic 62.9e6; "
-                                "achieved includes the merge kernel of the split schedule",
+                "traffic_note": "dram read+write bytes per launch (ncu); algorithmic 62.9e6 "
+                                "(O writes stay in L2)",
                 "peak_kind": f"bf16 dense sustained, {peaks['src']}",
                 "algorithmic": f"4*B*heads*L^2*d = {attn_flop:.4g} FLOP per launch"}
 
