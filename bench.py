@@ -415,7 +415,8 @@ def run_gpu(args):
         line["secondary"] = {"attention_sdxl3840": measure_attention_3840(dev, peaks),
                              "refresh_sweep": measure_refresh_sweep(dev, peaks),
                              "layer_2x256x256x640_p8": measure_large_layer(dev, peaks),
-                             "halo_conv_vae": measure_vae_conv(dev, peaks)}
+                             "halo_conv_vae": measure_vae_conv(dev, peaks),
+                             "otil_exchange_2x4x128x128_p4": measure_otil(dev)}
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
     if ws_n > 1:
@@ -547,6 +548,38 @@ def measure_vae_conv(dev, peaks, iters=5):
     return {"ms_mean": statistics.mean(ms), "ms_min": min(ms), "TFLOP/s": tfs,
             "frac_of_sustained_bf16": tfs / peaks["bf16_sus"], "flop_per_launch": flop,
             "launches": iters}
+
+
+def measure_otil(dev, iters=20):
+    """The OTIL exchange alone at the pages' noise-prediction shape: [2, 4, 128, 128]
+    bf16, P = 4 ranks, 8 x 32 sub-blocks (K = 16 per band), k = 4 sent per rank and
+    step: one dpp_otil_step (score, select, pack, copy to the other ranks) per launch."""
+    import torch
+
+    import stale_activations_gb300 as dpp
+    B, C, H, W, P, bh, bw, k = 2, 4, 128, 128, 4, 8, 32, 4
+    prm = dpp.otil_params(B, C, H, W, P, bh, bw, k, dpp.BF16)
+    g = torch.Generator(device=dev).manual_seed(5)
+    xs = [torch.randn(B, C, H, W, generator=g, device=dev).to(torch.bfloat16) for _ in range(4)]
+    st = dpp.otil_alloc(prm, xs[0], device=dev)
+    for i in range(3):
+        dpp.otil_step(prm, xs[i % 4], st)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
+    torch.cuda.synchronize()
+    ev[0].record()
+    for i in range(iters):
+        dpp.otil_step(prm, xs[i % 4], st)
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(iters)]
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record()
+    dpp.otil_finalize(prm, xs[0], st, reset=True)
+    f1.record()
+    torch.cuda.synchronize()
+    return {"ms_per_step": statistics.median(ms), "finalize_ms": f0.elapsed_time(f1),
+            "sent_bytes_per_step": P * k * B * C * bh * bw * 2,
+            "note": "back-to-back exchange steps (launch-bound at this size)"}
 
 
 def measure_large_layer(dev, peaks, iters=3):

@@ -314,6 +314,44 @@ int patch_layer_step_noalloc(const dpp_layer_params* prm, const dpp_layer_weight
                              const dpp_layer_state* st, const void* x, void* out, int mode,
                              void* stream);
 
+/* ---------------------------------------------------------------- OTIL exchange */
+
+/*
+ * OTIL selective latent transmit ("OTIL for SDXL on 4x L40S", What is implemented
+ * where / Self-tests), P virtual ranks on one device.  The latent (the noise prediction,
+ * "Read this before interpreting the numbers", item 3) is [B, C, H, W]; rank p owns
+ * rows [p*H/P, (p+1)*H/P) and views[p] is its copy of the whole latent.  A sub-block is
+ * a bh x bw tile of a band over all B and C, numbered row-major over the band
+ * (K = (H/P/bh) * (W/bw) per band).
+ *
+ * dpp_otil_step: every rank p scores its K sub-blocks -- d = 1 - cos(fresh block, the
+ * peers' copy of it), cos = 0 if a norm is 0, plus 10 if the block was not sent since
+ * the last reset -- sends the k highest (ties to the lower index): sel[p][0..k) in
+ * index order, msg[p][j] = the fresh block sel[p][j] ([B, C, bh, bw] each), flags set;
+ * every other rank copies the blocks into its view, rank p's own band of views[p]
+ * becomes fresh.  Copies only (never a blend).  The scores are fp32 sums over the block.
+ * dpp_otil_finalize: every view := fresh (the exact gather); reset != 0 also clears the
+ * flags (the synchronous step).
+ * fresh: [B,C,H,W] `dtype` holding every rank's fresh band; views: [P][B,C,H,W];
+ * visited: [P][K] uint8 (zero before the first step); sel: [P][k] int32; msg:
+ * [P][k][B][C][bh][bw] `dtype`.  Requires P >= 2, H % P == 0, (H/P) % bh == 0,
+ * W % bw == 0, K <= 4096, 1 <= k <= min(K, 256).
+ */
+typedef struct dpp_otil_params {
+  int B, C, H, W;  /* latent [B,C,H,W] */
+  int P;           /* ranks (row bands) */
+  int bh, bw;      /* sub-block rows and columns */
+  int k;           /* sub-blocks each rank sends per step */
+  int dtype;       /* DPP_BF16 or DPP_F32 */
+} dpp_otil_params;
+
+/* K (sub-blocks per band) for these params, or -1 if they are invalid. */
+int dpp_otil_blocks(const dpp_otil_params* prm);
+int dpp_otil_step(const dpp_otil_params* prm, const void* fresh, void* views, uint8_t* visited,
+                  int32_t* sel, void* msg, void* stream);
+int dpp_otil_finalize(const dpp_otil_params* prm, const void* fresh, void* views,
+                      uint8_t* visited, int reset, void* stream);
+
 /* Number of kernels one patch_layer_step launches for these params and mode. */
 int dpp_layer_kernel_count(const dpp_layer_params* prm, int mode);
 

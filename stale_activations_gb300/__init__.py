@@ -55,12 +55,17 @@ class WorkspaceLayout(ctypes.Structure):
                  "attn_partial_bytes", "total")]
 
 
+class OtilParams(ctypes.Structure):
+    _fields_ = [(n, _c_int) for n in ("B", "C", "H", "W", "P", "bh", "bw", "k", "dtype")]
+
+
 _lib = None
 EXPORTS = ("dpp_status_string", "dpp_version", "refresh_residual", "halo_conv3x3",
            "stale_kv_attention", "stale_kv_attention_split", "dpp_attention_partials_size",
            "apply_residual", "dpp_apply_layer_message", "dpp_workspace_query", "dpp_workspace_size", "dpp_message_elems",
            "dpp_message_blocks", "patch_layer_step", "patch_layer_step_timed",
-           "dpp_read_device_status", "dpp_layer_kernel_count", "patch_layer_step_noalloc")
+           "dpp_read_device_status", "dpp_layer_kernel_count", "patch_layer_step_noalloc",
+           "dpp_otil_blocks", "dpp_otil_step", "dpp_otil_finalize")
 
 
 def load(build_if_missing: bool = False):
@@ -113,6 +118,12 @@ def load(build_if_missing: bool = False):
                                              _c_void, _c_void, _c_int, _c_void]
     lib.dpp_read_device_status.restype = _c_int
     lib.dpp_read_device_status.argtypes = [_c_void, _c_void]
+    lib.dpp_otil_blocks.restype = _c_int
+    lib.dpp_otil_blocks.argtypes = [P(OtilParams)]
+    lib.dpp_otil_step.restype = _c_int
+    lib.dpp_otil_step.argtypes = [P(OtilParams)] + [_c_void] * 6
+    lib.dpp_otil_finalize.restype = _c_int
+    lib.dpp_otil_finalize.argtypes = [P(OtilParams), _c_void, _c_void, _c_void, _c_int, _c_void]
     lib.dpp_layer_kernel_count.restype = _c_int
     lib.dpp_layer_kernel_count.argtypes = [P(LayerParams), _c_int]
     _lib = lib
@@ -336,3 +347,39 @@ def workspace_views(prm: LayerParams, ws):
         out[name] = view(getattr(lo, name), n, dt, (B, H * W, C))
     assert es in (2, 4)
     return out
+
+
+# ------------------------------------------------------------------ OTIL exchange
+def otil_params(B, C, H, W, P, bh, bw, k, dtype=BF16) -> OtilParams:
+    return OtilParams(B, C, H, W, P, bh, bw, k, dtype)
+
+
+def otil_blocks(prm: OtilParams) -> int:
+    """Sub-blocks per band (K), or -1 for invalid params."""
+    return load().dpp_otil_blocks(ctypes.byref(prm))
+
+
+def otil_alloc(prm: OtilParams, fresh0, device="cuda"):
+    """The exchange state: every rank's view initialised to fresh0 [B,C,H,W], cleared
+    flags, and the selection / message outputs."""
+    K = otil_blocks(prm)
+    if K < 0:
+        raise DppError(2, "invalid OTIL params")
+    dt = fresh0.dtype
+    views = fresh0.to(device).unsqueeze(0).repeat(prm.P, 1, 1, 1, 1).contiguous()
+    visited = torch.zeros(prm.P, K, dtype=torch.uint8, device=device)
+    sel = torch.zeros(prm.P, prm.k, dtype=torch.int32, device=device)
+    msg = torch.zeros(prm.P, prm.k, prm.B, prm.C, prm.bh, prm.bw, dtype=dt, device=device)
+    return dict(views=views, visited=visited, sel=sel, msg=msg)
+
+
+def otil_step(prm: OtilParams, fresh, st: dict, stream=None):
+    _check(load().dpp_otil_step(ctypes.byref(prm), _ptr(fresh), _ptr(st["views"]),
+                                _ptr(st["visited"]), _ptr(st["sel"]), _ptr(st["msg"]),
+                                _stream(stream)), "dpp_otil_step")
+
+
+def otil_finalize(prm: OtilParams, fresh, st: dict, reset: bool = False, stream=None):
+    _check(load().dpp_otil_finalize(ctypes.byref(prm), _ptr(fresh), _ptr(st["views"]),
+                                    _ptr(st["visited"]), 1 if reset else 0, _stream(stream)),
+           "dpp_otil_finalize")

@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "groupnorm.cuh"
+#include "otil.cuh"
 #include "refresh.cuh"
 #include "simt.cuh"
 #include "tc.cuh"
@@ -480,6 +481,33 @@ int dpp_apply_layer_message(const dpp_layer_params* prm, const int8_t* codes,
   tab.copy_src = gn_sums;
   tab.copy_dst = copy->gn_stats;
   return dpp::launch_apply(tab, p.dtype, s);
+}
+
+int dpp_otil_blocks(const dpp_otil_params* prm) { return dpp::otil_blocks(prm); }
+
+int dpp_otil_step(const dpp_otil_params* prm, const void* fresh, void* views, uint8_t* visited,
+                  int32_t* sel, void* msg, void* stream) {
+  const int rc = dpp::otil_check(prm);
+  if (rc) return rc;
+  if (!fresh || !views || !visited || !sel || !msg) return DPP_ERR_NULL;
+  const size_t es = esize(prm->dtype);
+  if (reinterpret_cast<uintptr_t>(fresh) % es || reinterpret_cast<uintptr_t>(views) % es ||
+      reinterpret_cast<uintptr_t>(msg) % es || reinterpret_cast<uintptr_t>(sel) % 4)
+    return DPP_ERR_ALIGN;
+  return dpp::launch_otil_step(*prm, fresh, views, visited, sel, msg,
+                               static_cast<cudaStream_t>(stream));
+}
+
+int dpp_otil_finalize(const dpp_otil_params* prm, const void* fresh, void* views,
+                      uint8_t* visited, int reset, void* stream) {
+  const int rc = dpp::otil_check(prm);
+  if (rc) return rc;
+  if (!fresh || !views || !visited) return DPP_ERR_NULL;
+  const size_t es = esize(prm->dtype);
+  if (reinterpret_cast<uintptr_t>(fresh) % es || reinterpret_cast<uintptr_t>(views) % es)
+    return DPP_ERR_ALIGN;
+  return dpp::launch_otil_finalize(*prm, fresh, views, visited, reset ? 1 : 0,
+                                   static_cast<cudaStream_t>(stream));
 }
 
 int dpp_read_device_status(const void* workspace, void* stream) {

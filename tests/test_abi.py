@@ -126,3 +126,18 @@ def test_host_checks_without_launch(lib):
     st = dpp.LayerState()
     assert lib.patch_layer_step(ctypes.byref(prm), ctypes.byref(w), ctypes.byref(st), a, a, 0, a,
                                 None) == 1
+
+
+def test_otil_host_checks(lib):
+    ok = dpp.otil_params(2, 4, 128, 128, 4, 8, 32, 4)
+    assert dpp.otil_blocks(ok) == (32 // 8) * (128 // 32)
+    for kw in (dict(P=1), dict(H=130), dict(bh=5), dict(bw=48), dict(k=0), dict(k=17),
+               dict(dtype=7)):
+        base = dict(B=2, C=4, H=128, W=128, P=4, bh=8, bw=32, k=4, dtype=dpp.BF16)
+        base.update(kw)
+        bad = dpp.otil_params(**base)
+        assert dpp.otil_blocks(bad) == -1
+        assert lib.dpp_otil_step(ctypes.byref(bad), None, None, None, None, None, None) != 0
+    a = ctypes.c_void_p(256)
+    assert lib.dpp_otil_step(ctypes.byref(ok), None, a, a, a, a, None) == 1
+    assert lib.dpp_otil_step(ctypes.byref(ok), ctypes.c_void_p(257), a, a, a, a, None) == 3
