@@ -203,7 +203,7 @@ def whole_job_rate(steps: int, world: int, max_total_ms: float) -> float:
     return world * steps / (max_total_ms / 1e3)
 
 
-def _layer_setup(dev):
+def _layer_setup(dev, fuse_gn=False):
     import torch
 
     import stale_activations_gb300 as dpp
@@ -212,7 +212,7 @@ def _layer_setup(dev):
     wts = synth.layer_weights(cfg, seed=0)
     x, x_prev = synth.layer_inputs(cfg, seed=0)
     prm = dpp.make_params(cfg.B, cfg.H, cfg.W, cfg.C, cfg.P, cfg.G, cfg.heads, dpp.BF16,
-                          refresh=True, eps=cfg.eps)
+                          refresh=True, eps=cfg.eps, fuse_gn=fuse_gn)
     state, ws = dpp.alloc_layer(prm, device=dev)
     wd = {k: v.to(dev) for k, v in wts.items()}
     xd, xpd = x.to(dev), x_prev.to(dev)
@@ -416,7 +416,8 @@ def run_gpu(args):
                              "refresh_sweep": measure_refresh_sweep(dev, peaks),
                              "layer_2x256x256x640_p8": measure_large_layer(dev, peaks),
                              "halo_conv_vae": measure_vae_conv(dev, peaks),
-                             "otil_exchange_2x4x128x128_p4": measure_otil(dev)}
+                             "otil_exchange_2x4x128x128_p4": measure_otil(dev),
+                             "layer_fused_gn": measure_fused_gn(dev)}
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
     if ws_n > 1:
@@ -580,6 +581,46 @@ def measure_otil(dev, iters=20):
     return {"ms_per_step": statistics.median(ms), "finalize_ms": f0.elapsed_time(f1),
             "sent_bytes_per_step": P * k * B * C * bh * bw * 2,
             "note": "back-to-back exchange steps (launch-bound at this size)"}
+
+
+def measure_fused_gn(dev, iters=20):
+    """The headline layer step with the GroupNorm apply fused into the conv's operand
+    path (fuse_gn = 1) against the separate apply, same workload and L2 flush."""
+    import torch
+
+    import stale_activations_gb300 as dpp
+    res = {}
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for fuse in (False, True):
+        cfg, prm, wd, state, ws, _, xd, out = _layer_setup(dev, fuse_gn=fuse)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(dpp.NUM_STAGE_EVENTS)]
+               for _ in range(iters)]
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(iters)]
+        for row in evs:
+            for e in row:
+                e.record()
+        for _ in range(3):
+            flush.fill_(1)
+            dpp.patch_layer_step(prm, wd, state, xd, out, dpp.STALE, ws)
+        for i in range(iters):
+            flush.fill_(1)
+            pairs[i][0].record()
+            dpp.patch_layer_step(prm, wd, state, xd, out, dpp.STALE, ws)
+            pairs[i][1].record()
+        for i in range(iters):
+            flush.fill_(1)
+            dpp.patch_layer_step(prm, wd, state, xd, out, dpp.STALE, ws, stage_events=evs[i])
+        torch.cuda.synchronize()
+        if dpp.read_device_status(ws) != 0:
+            raise RuntimeError("device status set in the fused-GroupNorm comparison")
+        res["fused" if fuse else "separate"] = {
+            "ms_per_step": statistics.median(a.elapsed_time(b) for a, b in pairs),
+            "stage_ms": {n: statistics.median(evs[i][k].elapsed_time(evs[i][k + 1])
+                                              for i in range(iters))
+                         for k, n in enumerate(dpp.STAGES)}}
+        del state, ws
+    return res
 
 
 def measure_large_layer(dev, peaks, iters=3):

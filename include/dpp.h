@@ -190,6 +190,11 @@ typedef struct dpp_layer_params {
   int refresh;     /* DPP_STALE only: 1 = refresh the state, 0 = leave it (no_sync) */
   float eps;       /* GroupNorm epsilon */
   int gn_mode;     /* DPP_GN_SPLICED (0), DPP_GN_SYNC or DPP_GN_PREVIOUS */
+  int fuse_gn;     /* DPP_BF16 only (0 for DPP_F32): 1 = the conv applies GroupNorm to its
+                      own band's rows of x as its input tiles land in shared memory, and
+                      the workspace's y holds only each band's first and last row (the
+                      rows the neighbours read as halos); 0 = a separate apply pass
+                      writes all of y (the faster choice on the SDXL-1024 layer) */
 } dpp_layer_params;
 
 typedef struct dpp_layer_weights {
@@ -216,7 +221,10 @@ typedef struct dpp_workspace_layout {
   size_t status;     /* int device status word (zeroed by each patch_layer_step) */
   size_t gn_partial; /* fp32 per-chunk GroupNorm partial sums */
   size_t gn_fresh;   /* [B,P,G,2] fp32 fresh sums of this step */
-  size_t y;          /* [B,H,W,C] GroupNorm output (conv input) */
+  size_t gn_params;  /* fuse_gn: [B,P,3,C] fp32 mean, rstd*gamma, beta of each band (the
+                        conv applies them to its band's rows of x); else an empty piece */
+  size_t y;          /* [B,H,W,C] GroupNorm output (conv input); with fuse_gn only the
+                        first and last row of each band */
   size_t h;          /* [B,H,W,C] conv output */
   size_t q, k, v;    /* [B,L,C] fresh projections */
   size_t o;          /* [B,L,C] attention output */

@@ -36,7 +36,8 @@ class DppError(RuntimeError):
 class LayerParams(ctypes.Structure):
     _fields_ = [("B", _c_int), ("H", _c_int), ("W", _c_int), ("C", _c_int), ("P", _c_int),
                 ("G", _c_int), ("heads", _c_int), ("head_dim", _c_int), ("dtype", _c_int),
-                ("refresh", _c_int), ("eps", ctypes.c_float), ("gn_mode", _c_int)]
+                ("refresh", _c_int), ("eps", ctypes.c_float), ("gn_mode", _c_int),
+                ("fuse_gn", _c_int)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -51,7 +52,7 @@ class LayerState(ctypes.Structure):
 
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("status", "gn_partial", "gn_fresh", "y", "h", "q", "k", "v", "o", "attn_partial",
+                ("status", "gn_partial", "gn_fresh", "gn_params", "y", "h", "q", "k", "v", "o", "attn_partial",
                  "attn_partial_bytes", "total")]
 
 
@@ -234,9 +235,9 @@ GN_SPLICED, GN_SYNC, GN_PREVIOUS = 0, 1, 2
 
 
 def make_params(B, H, W, C, P, G, heads, dtype, refresh=True, eps=1e-5, head_dim=64,
-                gn_mode=GN_SPLICED):
+                gn_mode=GN_SPLICED, fuse_gn=False):
     return LayerParams(B, H, W, C, P, G, heads, head_dim, dtype, 1 if refresh else 0, eps,
-                       gn_mode)
+                       gn_mode, 1 if fuse_gn else 0)
 
 
 def workspace_layout(prm: LayerParams) -> WorkspaceLayout:
@@ -343,6 +344,8 @@ def workspace_views(prm: LayerParams, ws):
 
     out = dict(gn_fresh=view(lo.gn_fresh, B * P * G * 2, torch.float32, (B, P, G, 2)),
                y=view(lo.y, n, dt, (B, H, W, C)), h=view(lo.h, n, dt, (B, H, W, C)))
+    if prm.fuse_gn:
+        out["gn_params"] = view(lo.gn_params, B * P * 3 * C, torch.float32, (B, P, 3, C))
     for name in ("q", "k", "v", "o"):
         out[name] = view(getattr(lo, name), n, dt, (B, H * W, C))
     assert es in (2, 4)

@@ -84,6 +84,7 @@ int check_layer(const dpp_layer_params* p) {
   if (p->C % vec || p->C / vec > 256) return DPP_ERR_SHAPE;
   if (p->refresh != 0 && p->refresh != 1) return DPP_ERR_ARG;
   if (p->gn_mode < DPP_GN_SPLICED || p->gn_mode > DPP_GN_PREVIOUS) return DPP_ERR_ARG;
+  if (p->fuse_gn != 0 && !(p->fuse_gn == 1 && p->dtype == DPP_BF16)) return DPP_ERR_ARG;
   if (!(p->eps >= 0.f)) return DPP_ERR_ARG;
   rc = check_conv(p->B, p->H, p->W, p->C, p->C, p->P, p->dtype);
   if (rc) return rc;
@@ -103,6 +104,9 @@ int layout(const dpp_layer_params* p, dpp_workspace_layout* o) {
   o->status = off; off = align256(off + 256);
   o->gn_partial = off; off = align256(off + dpp::gn_partial_bytes(g));
   o->gn_fresh = off; off = align256(off + (size_t)p->B * p->P * p->G * 2 * sizeof(float));
+  // per-channel GroupNorm parameters the conv applies to its input tiles (fuse_gn)
+  o->gn_params = off;
+  off = align256(off + (p->fuse_gn ? (size_t)p->B * p->P * 3 * p->C * sizeof(float) : 0));
   o->y = off; off = align256(off + act);
   o->h = off; off = align256(off + act);
   o->q = off; off = align256(off + act);
@@ -121,9 +125,9 @@ int layout(const dpp_layer_params* p, dpp_workspace_layout* o) {
 }
 
 int run_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,
-             int Cin, int Cout, int P, int dtype, int* st, cudaStream_t s) {
+             int Cin, int Cout, int P, int dtype, const float* gn_par, int* st, cudaStream_t s) {
   if (dtype == DPP_BF16)
-    return dpp::launch_tc_conv(yf, ys, w, out, B, H, W, Cin, Cout, P, st,
+    return dpp::launch_tc_conv(yf, ys, w, out, B, H, W, Cin, Cout, P, gn_par, st,
                                dpp_host::wait_limit_from_env(), s);
   return dpp::launch_simt_conv(yf, ys, w, out, B, H, W, Cin, Cout, P, dtype, s);
 }
@@ -225,7 +229,7 @@ int halo_conv3x3(const void* y_fresh, const void* y_stale, const void* w, void* 
   if (rc) return rc;
   if (!aligned16(y_fresh) || !aligned16(y_stale) || !aligned16(w) || !aligned16(out))
     return DPP_ERR_ALIGN;
-  return run_conv(y_fresh, y_stale, w, out, B, H, W, Cin, Cout, P, dtype, dev_status,
+  return run_conv(y_fresh, y_stale, w, out, B, H, W, Cin, Cout, P, dtype, nullptr, dev_status,
                   static_cast<cudaStream_t>(stream));
 }
 
@@ -360,13 +364,19 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
   const int ncnt = p.dtype == DPP_BF16 && lo.attn_partial_bytes
                        ? dpp::tc_attention_counters(p.B, L, p.heads, p.P)
                        : 0;
+  // fuse_gn: the apply writes only the rows other bands read as halos (and the state
+  // update reads), plus the per-channel parameters; the conv normalises its own band's
+  // rows of x as its tiles land in shared memory
+  const bool fused = p.fuse_gn != 0;
+  float* gn_params = fused ? reinterpret_cast<float*>(ws + lo.gn_params) : nullptr;
   rc = dpp::launch_gn(x, y, gn_partial, sync ? nullptr : st->gn_stats, gn_fresh, wts->gamma,
                       wts->beta, g, p.eps, sync ? DPP_GN_SYNC : p.gn_mode, p.dtype, status,
-                      reinterpret_cast<int*>(ws + lo.attn_partial), ncnt, s);
+                      reinterpret_cast<int*>(ws + lo.attn_partial), ncnt, gn_params,
+                      fused ? 1 : 0, s);
   if (rc || (rc = mark(1))) return rc;
   // a3: halo conv, halo rows from the stale conv input (fresh at the synchronous step)
-  rc = run_conv(y, sync ? y : st->y_stale, wts->w_conv, h, p.B, p.H, p.W, p.C, p.C, p.P, p.dtype,
-                status, s);
+  rc = run_conv(fused ? x : y, sync ? y : st->y_stale, wts->w_conv, h, p.B, p.H, p.W, p.C, p.C,
+                p.P, p.dtype, gn_params, status, s);
   if (rc || (rc = mark(2))) return rc;
   // a4: Q, K, V projections (one GEMM over the packed [3C, C] weight)
   rc = run_linear(h, wts->w_qkv, q, k, v, M, 3 * p.C, p.C, p.dtype, status, s);

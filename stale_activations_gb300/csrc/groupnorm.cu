@@ -17,6 +17,15 @@
 
 namespace dpp {
 
+// Threads that share one sum in a 256-thread block reducing `nsum` sums: the largest
+// power of two <= min(32, 256 / nsum), at least 1 (lanes of one warp, aligned).
+__device__ __forceinline__ int lanes_per_sum(int nsum) {
+  int t = nsum >= 256 ? 1 : 256 / nsum;
+  if (t > 32) t = 32;
+  while (t & (t - 1)) t &= t - 1;
+  return t;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) gn_stats_kernel(const T* __restrict__ x,
                                                        float* __restrict__ partial, GnDims g,
@@ -70,17 +79,30 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const T* __restrict__ x,
     for (int i = 0; i < VEC; ++i) { r1[i] = s1[i]; r2[i] = s2[i]; }
   }
   __syncthreads();
+  // fold channels into groups: tpg threads per group, each summing a fixed stride of the
+  // group's (pixel lane, channel) values, then a shuffle tree over the tpg lanes (a
+  // fixed order, so the sums are deterministic)
   const int cg = g.C / g.G;
-  for (int gi = tid; gi < g.G; gi += blockDim.x) {
+  const int tpg = lanes_per_sum(g.G);
+  const int n = PIX * cg;
+  for (int t0 = 0; t0 < g.G * tpg; t0 += blockDim.x) {
+    const int t = t0 + tid, gi = t / tpg, part = t % tpg;
     float a = 0.f, q = 0.f;
-    for (int k = 0; k < PIX; ++k)
-      for (int c = gi * cg; c < (gi + 1) * cg; ++c) {
+    if (gi < g.G)
+      for (int j = part; j < n; j += tpg) {
+        const int k = j / cg, c = gi * cg + (j - k * cg);
         a += red[(long long)k * g.C + c];
         q += red[(long long)PIX * g.C + (long long)k * g.C + c];
       }
-    float* out = partial + ((((long long)b * g.P + p) * g.nchunk + chunk) * g.G + gi) * 2;
-    out[0] = a;
-    out[1] = q;
+    for (int m = tpg >> 1; m > 0; m >>= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, m);
+      q += __shfl_xor_sync(0xffffffffu, q, m);
+    }
+    if (gi < g.G && part == 0) {
+      float* out = partial + ((((long long)b * g.P + p) * g.nchunk + chunk) * g.G + gi) * 2;
+      out[0] = a;
+      out[1] = q;
+    }
   }
 }
 
@@ -91,7 +113,9 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
                                                        float* __restrict__ fresh_out,
                                                        const float* __restrict__ gamma,
                                                        const float* __restrict__ beta, GnDims g,
-                                                       float eps, int mode) {
+                                                       float eps, int mode,
+                                                       float* __restrict__ params_out,
+                                                       int halo_only) {
   constexpr int VEC = Vec<T>::N;
   extern __shared__ float sm[];  // mean[C], scale[C], beta[C], group sums [P][G][2]
   const bool all_fresh = mode == DPP_GN_SYNC;
@@ -103,26 +127,35 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
   const int tid = threadIdx.x;
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  // fresh sums over chunks, for own patch (and every patch when all are fresh);
-  // eight independent partial sums so that the chunk loads are in flight together
-  for (int idx = tid; idx < g.P * g.G * 2; idx += blockDim.x) {
-    const int q = idx / (g.G * 2), r = idx % (g.G * 2);
+  // fresh sums over chunks, for own patch (and every patch when all are fresh): tps
+  // threads per sum, each a fixed stride of chunks with eight loads in flight, then a
+  // shuffle tree (fixed order); the other patches' sums come from the stale statistics
+  const int G2 = g.G * 2;
+  const int nq = all_fresh ? g.P : 1;
+  const int tps = lanes_per_sum(nq * G2);
+  for (int t0 = 0; t0 < nq * G2 * tps; t0 += blockDim.x) {
+    const int t = t0 + tid, si = t / tps, part = t % tps;
+    const int q = all_fresh ? si / G2 : p, r = si % G2;
     float v = 0.f;
-    if (all_fresh || q == p) {
-      const float* src = partial + (((long long)b * g.P + q) * g.nchunk) * g.G * 2 + r;
+    if (si < nq * G2) {
+      const float* src = partial + (((long long)b * g.P + q) * g.nchunk) * G2 + r;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      int c = 0;
-      for (; c + 8 <= g.nchunk; c += 8) {
+      int c = part;
+      for (; c + 7 * tps < g.nchunk; c += 8 * tps) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) acc[u] += src[(long long)(c + u) * g.G * 2];
+        for (int u = 0; u < 8; ++u) acc[u] += src[(long long)(c + u * tps) * G2];
       }
-      for (; c < g.nchunk; ++c) acc[c & 7] += src[(long long)c * g.G * 2];
+#pragma unroll
+      for (int u = 0; u < 7; ++u)
+        if (c + u * tps < g.nchunk) acc[u] += src[(long long)(c + u * tps) * G2];
       v = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-    } else {
-      v = stale_stats[((long long)b * g.P + q) * g.G * 2 + r];
     }
-    s_tot[idx] = v;
+    for (int m = tps >> 1; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    if (si < nq * G2 && part == 0) s_tot[q * G2 + r] = v;
   }
+  if (!all_fresh)
+    for (int idx = tid; idx < g.P * G2; idx += blockDim.x)
+      if (idx / G2 != p) s_tot[idx] = stale_stats[((long long)b * g.P) * G2 + idx];
   __syncthreads();
   if (chunk == 0 && fresh_out) {
     for (int r = tid; r < g.G * 2; r += blockDim.x)
@@ -144,6 +177,12 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
     s_mu[c] = mu;
     s_sc[c] = rstd * gamma[c];
     s_be[c] = beta[c];
+    if (params_out && chunk == 0) {  // the per-channel parameters, for a fused consumer
+      float* dst = params_out + ((long long)b * g.P + p) * 3 * g.C;
+      dst[c] = mu;
+      dst[g.C + c] = s_sc[c];
+      dst[2 * g.C + c] = s_be[c];
+    }
   }
   __syncthreads();
   // each thread keeps one 16-byte channel vector (and its GroupNorm parameters in
@@ -160,8 +199,13 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
     be[k] = s_be[v * VEC + k];
   }
   const long long band_pix = (long long)g.Hp * g.W;
-  const long long p0 = (long long)chunk * g.chunk_pix;
-  const long long p1 = min(band_pix, p0 + g.chunk_pix);
+  long long p0 = (long long)chunk * g.chunk_pix;
+  long long p1 = min(band_pix, p0 + g.chunk_pix);
+  if (halo_only) {  // block 0: the band's first row (p > 0), block 1: its last (p < P-1)
+    if ((chunk == 0 && p == 0) || (chunk == 1 && p == g.P - 1)) return;
+    p0 = chunk == 0 ? 0 : (long long)(g.Hp - 1) * g.W;
+    p1 = p0 + g.W;
+  }
   const long long base = (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C + v * VEC;
   auto apply_one = [&](const uint4& u, long long px) {
     float f[VEC];
@@ -200,8 +244,10 @@ size_t gn_partial_bytes(const GnDims& g) {
 
 int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, float* fresh_out,
               const float* gamma, const float* beta, const GnDims& g, float eps, int mode,
-              int dtype, int* status_to_zero, int* zero_ints, int nzero, cudaStream_t stream) {
+              int dtype, int* status_to_zero, int* zero_ints, int nzero, float* params_out,
+              int halo_only, cudaStream_t stream) {
   dim3 grid(g.nchunk, g.P, g.B);
+  const dim3 agrid = halo_only ? dim3(2, g.P, g.B) : grid;
   const int VEC = dtype == DPP_BF16 ? 8 : 4;
   const int NV = g.C / VEC;
   const int PIX = 256 / NV;
@@ -214,17 +260,17 @@ int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, 
     e = launch_pdl(gn_stats_kernel<__nv_bfloat16>, grid, dim3(256), red_bytes, stream, xs, partial,
                    g, status_to_zero, zero_ints, nzero);
     if (e == cudaSuccess)
-      e = launch_pdl(gn_apply_kernel<__nv_bfloat16>, grid, dim3(256), app_bytes, stream, xs,
+      e = launch_pdl(gn_apply_kernel<__nv_bfloat16>, agrid, dim3(256), app_bytes, stream, xs,
                      static_cast<__nv_bfloat16*>(y), (const float*)partial, stale_stats, fresh_out,
-                     gamma, beta, g, eps, mode);
+                     gamma, beta, g, eps, mode, params_out, halo_only);
   } else {
     auto* xs = static_cast<const float*>(x);
     e = launch_pdl(gn_stats_kernel<float>, grid, dim3(256), red_bytes, stream, xs, partial, g,
                    status_to_zero, zero_ints, nzero);
     if (e == cudaSuccess)
-      e = launch_pdl(gn_apply_kernel<float>, grid, dim3(256), app_bytes, stream, xs,
+      e = launch_pdl(gn_apply_kernel<float>, agrid, dim3(256), app_bytes, stream, xs,
                      static_cast<float*>(y), (const float*)partial, stale_stats, fresh_out, gamma,
-                     beta, g, eps, mode);
+                     beta, g, eps, mode, params_out, halo_only);
   }
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }

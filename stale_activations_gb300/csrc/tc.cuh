@@ -13,9 +13,12 @@ bool tc_linear_supported(long long M, int C);
 int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2, long long M,
                      int N, int K, int* status, long long wait_limit, cudaStream_t s);
 
-// Implicit-GEMM halo conv3x3 (see halo_conv3x3 in dpp.h).
+// Implicit-GEMM halo conv3x3 (see halo_conv3x3 in dpp.h).  With gn_par non-NULL, yf is
+// the raw GroupNorm input x and the kernel applies GroupNorm to its in-band rows on the
+// fly (gn_par: [B][P][3][Cin] fp32 mean, rstd * gamma, beta); ys is the stale y.
 int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,
-                   int Cin, int Cout, int P, int* status, long long wait_limit, cudaStream_t s);
+                   int Cin, int Cout, int P, const float* gn_par, int* status,
+                   long long wait_limit, cudaStream_t s);
 
 // Stale-KV flash attention (see stale_kv_attention in dpp.h), head_dim 64.  With
 // `partials` non-NULL the units that do not divide evenly over the CTAs are shared key

@@ -28,7 +28,9 @@ namespace dpp {
 namespace {
 
 constexpr int BM = 128, BK = 64;
-constexpr int GEMM_THREADS = 192;
+constexpr int GEMM_THREADS = 192;     // producer, MMA, 4 epilogue warps
+constexpr int GEMM_GN_THREADS = 320;  // + 4 warps applying GroupNorm to the A operand
+constexpr int kBarBytes = 512;        // barriers, flags and per-stage notes
 
 constexpr int kMaxDynSmem = 227 * 1024;
 
@@ -40,8 +42,8 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (kMaxDynSmem - 1024 /*align*/ - 256 /*barriers*/) / STAGE_BYTES;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int STAGES = (kMaxDynSmem - 1024 /*align*/ - kBarBytes) / STAGE_BYTES;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + kBarBytes;
   static constexpr uint32_t TMEM_COLS = NACC * BN <= 256 ? 256 : 512;
   static_assert(BN % MMA_N == 0 && MMA_N % 16 == 0 && MMA_N <= 256, "MMA shape");
   static_assert(SMEM <= kMaxDynSmem && STAGES >= 2, "shared memory");
@@ -57,10 +59,23 @@ struct GemmArgs {
   long long wait_limit;
   // implicit conv
   int H, W, Cin, Hp, cin_blocks, boxes, box_px;
+  // conv with GroupNorm applied to the in-band rows of A (raw x): [B][P][3][Cin] fp32
+  // (mean, rstd * gamma, beta per channel of each batch and patch)
+  const float* gn_par;
+  int P;
 };
 
-template <bool CONV, int BN>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+// What the producer fetched into a stage, for the GroupNorm warps: the boxes' first
+// column (c0 + dj) and which boxes hold in-band rows of x (bit per box).
+struct StageNote {
+  int col0, fresh;
+};
+
+// GNF (conv only): tmA maps the raw input x, tmA2 the stale GroupNorm output; warps
+// 6-9 turn each landed in-band box of x into y = (x - mean) * scale + beta in place
+// (the zero fill of out-of-image positions stays 0) before the MMA reads the stage.
+template <bool CONV, int BN, bool GNF>
+__global__ void __launch_bounds__(GNF ? GEMM_GN_THREADS : GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
   using C = Cfg<BN>;
@@ -73,8 +88,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* acc_full = empty + STAGES;   // [NACC] MMA -> epilogue
   uint64_t* acc_empty = acc_full + 2;    // [NACC] epilogue -> MMA (4 warps)
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* xform = drain + 1;           // [STAGES] GroupNorm warps -> MMA (GNF)
+  StageNote* note = reinterpret_cast<StageNote*>(xform + STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(note + STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  static_assert((2 * STAGES + 5 + STAGES) * 8 + STAGES * sizeof(StageNote) + 8 <= kBarBytes,
+                "barrier area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = args.m_tiles * args.n_tiles;
@@ -83,6 +102,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
+      if (GNF) ptx::mbar_init(&xform[s], 4);  // one arrival per GroupNorm warp
     }
     for (int b = 0; b < C::NACC; ++b) {
       ptx::mbar_init(&acc_full[b], 1);
@@ -142,6 +162,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           uint8_t* a_dst = smem + s * C::STAGE_BYTES;
           uint8_t* b_dst = a_dst + C::A_BYTES;
+          if (GNF) {  // the note first: the arrive below releases it to the waiters
+            const int tap = kb / args.cin_blocks;
+            const int di = tap / 3 - 1;
+            uint32_t fresh = 0;
+            for (int bx = 0; bx < args.boxes; ++bx) {
+              const int rk = r + bx, rr = rk + di;
+              if (rr >= 0 && rr < args.H && (rr / args.Hp) == (rk / args.Hp)) fresh |= 1u << bx;
+            }
+            note[s] = StageNote{c0 + tap % 3 - 1, (int)fresh};
+          }
           ptx::mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
           if (CONV) {
             const int tap = kb / args.cin_blocks;
@@ -190,7 +220,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int kb = 0; kb < args.nkb; ++kb, ++g) {
           const int s = (int)(g % STAGES);
           const uint32_t ph = (uint32_t)((g / STAGES) & 1);
-          if (!ptx::mbar_wait(&full[s], ph, args.wait_limit, abort_flag)) {
+          if (!ptx::mbar_wait(GNF ? &xform[s] : &full[s], ph, args.wait_limit, abort_flag)) {
             set_status(args.status, DPP_ERR_TIMEOUT);
             *abort_flag = 1;
             ok = false;
@@ -214,6 +244,84 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (*abort_flag && any) {  // let issued MMAs finish before TMEM is released
         ptx::mma_commit(drain);
         ptx::mbar_wait(drain, 0, kDrainWaitLimit, nullptr);
+      }
+    }
+  } else if (GNF && warp >= 6) {
+    // ------------------------------------------------ GroupNorm on A (warps 6..9)
+    // Per stage: the in-band boxes of raw x become y = (x - mean) * scale + beta, the
+    // apply of the separate GroupNorm kernel written out (same operations, same bf16
+    // rounding); boxes of stale y and the zero fill outside the image are left as they
+    // are.  The 128-byte swizzle puts logical 16-byte chunk (ch ^ (row & 7)) of a
+    // 128-byte row at physical chunk ch (box rows start on 1024-byte boundaries).
+    // Thread t handles 16-byte chunk (t & 7) of A rows (t >> 3) + 16 i, i = 0..7: every
+    // such row has the same (row & 7), so the thread's 8 channels are the same in all
+    // eight chunks and their parameters are loaded once per stage.
+    const int tid = threadIdx.x - 6 * 32;
+    const int ch = tid & 7, row_lo = tid >> 3;
+    const int c = (ch ^ (row_lo & 7)) << 3;  // first of the thread's 8 channels
+    const int box_lg = __ffs(args.box_px) - 1;  // box_px is a power of two
+    long long g = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      // the tile's batch and band, and its K-slice rotation, as the producer has them:
+      // the parameters of a stage are fetched before its data lands
+      const int mt = tile / args.n_tiles;
+      const long long m0 = (long long)mt * BM;
+      const long long hw = (long long)args.H * args.W;
+      const int tb = (int)(m0 / hw);
+      const int band = (int)((m0 - (long long)tb * hw) / args.W) / args.Hp;
+      const float* par_tile = args.gn_par + ((long long)tb * args.P + band) * 3 * args.Cin + c;
+      const int rot = (int)(mt % args.nkb);
+      for (int kq = 0; kq < args.nkb; ++kq, ++g) {
+        const int s = (int)(g % STAGES);
+        const uint32_t ph = (uint32_t)((g / STAGES) & 1);
+        const int kb = kq + rot < args.nkb ? kq + rot : kq + rot - args.nkb;
+        const float* par = par_tile + (kb % args.cin_blocks) * BK;
+        float mu[8], sc[8], be[8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float4 m = __ldg(reinterpret_cast<const float4*>(par) + h);
+          const float4 k = __ldg(reinterpret_cast<const float4*>(par + args.Cin) + h);
+          const float4 e = __ldg(reinterpret_cast<const float4*>(par + 2 * args.Cin) + h);
+          mu[4 * h] = m.x; mu[4 * h + 1] = m.y; mu[4 * h + 2] = m.z; mu[4 * h + 3] = m.w;
+          sc[4 * h] = k.x; sc[4 * h + 1] = k.y; sc[4 * h + 2] = k.z; sc[4 * h + 3] = k.w;
+          be[4 * h] = e.x; be[4 * h + 1] = e.y; be[4 * h + 2] = e.z; be[4 * h + 3] = e.w;
+        }
+        if (!ptx::mbar_wait(&full[s], ph, args.wait_limit, abort_flag)) {
+          set_status(args.status, DPP_ERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        const StageNote nt = note[s];
+        const uint32_t fresh = (uint32_t)nt.fresh;
+        if (fresh) {
+          uint8_t* a_st = smem + s * C::STAGE_BYTES + ch * 16;
+          uint4 v[8];
+          uint32_t take = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int row = row_lo + 16 * i;  // row of the 128-row A tile
+            const int bx = row >> box_lg;
+            const int col = nt.col0 + (row & (args.box_px - 1));
+            if (((fresh >> bx) & 1) && col >= 0 && col < args.W) {
+              take |= 1u << i;
+              v[i] = *reinterpret_cast<const uint4*>(a_st + row * 128);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (!((take >> i) & 1)) continue;
+            float f[8];
+            unpack16(v[i], f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] = fmaf(f[k] - mu[k], sc[k], be[k]);
+            *reinterpret_cast<uint4*>(a_st + (row_lo + 16 * i) * 128) = pack16(f);
+          }
+          ptx::fence_proxy_async_smem();  // generic writes -> the tensor core's reads
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&xform[s]);
       }
     }
   } else {
@@ -302,12 +410,13 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
   return r == CUDA_SUCCESS;
 }
 
-template <bool CONV, int BN>
+template <bool CONV, int BN, bool GNF>
 int prepare() {
   static std::once_flag once;
   static int rc = DPP_OK;
   std::call_once(once, [] {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<CONV, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_gemm_kernel<CONV, BN, GNF>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<BN>::SMEM) != cudaSuccess)
       rc = DPP_ERR_CUDA;
   });
@@ -331,27 +440,29 @@ int pick_bn(int N, int ncols, int nkb) {
 
 constexpr int mma_n(int bn) { return bn > 256 ? bn / 2 : bn; }
 
-template <bool CONV, int BN>
+template <bool CONV, int BN, bool GNF>
 int launch(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, GemmArgs g,
            cudaStream_t s) {
-  int rc = prepare<CONV, BN>();
+  int rc = prepare<CONV, BN, GNF>();
   if (rc) return rc;
   g.n_tiles = g.N / BN;
   const long long ntiles = (long long)g.m_tiles * g.n_tiles;
   const int grid = (int)(ntiles < dpp_host::sm_count() ? ntiles : dpp_host::sm_count());
-  const cudaError_t e = dpp_host::launch_pdl(tc_gemm_kernel<CONV, BN>, dim3(grid),
-                                             dim3(GEMM_THREADS), Cfg<BN>::SMEM, s, ta, ta2, tb, g);
+  const cudaError_t e =
+      dpp_host::launch_pdl(tc_gemm_kernel<CONV, BN, GNF>, dim3(grid),
+                           dim3(GNF ? GEMM_GN_THREADS : GEMM_THREADS), Cfg<BN>::SMEM, s, ta, ta2,
+                           tb, g);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
 
-template <bool CONV>
+template <bool CONV, bool GNF>
 int dispatch(int bn, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
              const GemmArgs& g, cudaStream_t s) {
   switch (bn) {
-    case 320: return launch<CONV, 320>(ta, ta2, tb, g, s);
-    case 256: return launch<CONV, 256>(ta, ta2, tb, g, s);
-    case 160: return launch<CONV, 160>(ta, ta2, tb, g, s);
-    case 128: return launch<CONV, 128>(ta, ta2, tb, g, s);
+    case 320: return launch<CONV, 320, GNF>(ta, ta2, tb, g, s);
+    case 256: return launch<CONV, 256, GNF>(ta, ta2, tb, g, s);
+    case 160: return launch<CONV, 160, GNF>(ta, ta2, tb, g, s);
+    case 128: return launch<CONV, 128, GNF>(ta, ta2, tb, g, s);
     default: return DPP_ERR_SHAPE;
   }
 }
@@ -389,11 +500,12 @@ int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2,
   g.ncols = ncols;
   g.status = status;
   g.wait_limit = wait_limit;
-  return dispatch<false>(bn, ta, ta, tb, g, s);
+  return dispatch<false, false>(bn, ta, ta, tb, g, s);
 }
 
 int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,
-                   int Cin, int Cout, int P, int* status, long long wait_limit, cudaStream_t s) {
+                   int Cin, int Cout, int P, const float* gn_par, int* status,
+                   long long wait_limit, cudaStream_t s) {
   if (!tc_conv_supported(B, H, W, Cin, Cout, P)) return DPP_ERR_SHAPE;
   const int bn = pick_bn(Cout, Cout, 9 * Cin / BK);
   if (!bn) return DPP_ERR_SHAPE;
@@ -417,7 +529,10 @@ int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int
   g.H = H; g.W = W; g.Cin = Cin; g.Hp = H / P; g.cin_blocks = Cin / BK;
   g.boxes = BM / box_px;
   g.box_px = box_px;
-  return dispatch<true>(bn, tf, ts, tw, g, s);
+  g.gn_par = gn_par;
+  g.P = P;
+  return gn_par ? dispatch<true, true>(bn, tf, ts, tw, g, s)
+                : dispatch<true, false>(bn, tf, ts, tw, g, s);
 }
 
 }  // namespace dpp

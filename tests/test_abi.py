@@ -47,9 +47,13 @@ def test_status_strings(lib):
 
 
 def _params(**kw):
+    raw = kw.pop("fuse_gn_raw", None)   # a value make_params would not produce
     base = dict(B=2, H=64, W=64, C=640, P=4, G=32, heads=10, dtype=dpp.BF16)
     base.update(kw)
-    return dpp.make_params(**base)
+    prm = dpp.make_params(**base)
+    if raw is not None:
+        prm.fuse_gn = raw
+    return prm
 
 
 def test_workspace_layout_sizes(lib):
@@ -57,9 +61,12 @@ def test_workspace_layout_sizes(lib):
     lo = dpp.workspace_layout(prm)
     act = 2 * 64 * 64 * 640 * 2
     assert lo.total >= 6 * act
-    offs = [lo.status, lo.gn_partial, lo.gn_fresh, lo.y, lo.h, lo.q, lo.k, lo.v, lo.o,
+    offs = [lo.status, lo.gn_partial, lo.gn_fresh, lo.gn_params, lo.y, lo.h, lo.q, lo.k, lo.v, lo.o,
             lo.attn_partial]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert lo.y == lo.gn_params                          # no parameters without fuse_gn
+    lf = dpp.workspace_layout(_params(fuse_gn=1))
+    assert lf.y - lf.gn_params >= 2 * 4 * 3 * 640 * 4   # [B, P, 3, C] fp32 parameters
     # 320 attention units on (without a GPU, the library assumes) 152 SMs: one round of
     # 152 whole units, the other 168 shared; two counters per shared unit (1536 bytes
     # with padding), then 152 + 168 partial records of 34816 bytes
@@ -74,7 +81,9 @@ def test_workspace_layout_sizes(lib):
 
 @pytest.mark.parametrize("kw", [dict(H=63), dict(P=3), dict(C=600, heads=10), dict(G=7),
                                 dict(heads=5), dict(dtype=7), dict(W=48), dict(gn_mode=3),
-                                dict(gn_mode=-1)])
+                                dict(gn_mode=-1), dict(fuse_gn_raw=2),
+                                dict(B=1, H=32, W=32, C=64, P=2, G=8, heads=1, dtype=dpp.F32,
+                                     fuse_gn=1)])
 def test_invalid_params_rejected(lib, kw):
     prm = _params(**kw)
     assert lib.dpp_workspace_size(ctypes.byref(prm)) == 0

@@ -40,10 +40,10 @@ def _gpu_state_from(ostate, cfg, prm, dev="cuda"):
     return state, ws
 
 
-def _params(cfg, refresh=True):
+def _params(cfg, refresh=True, fuse_gn=False, gn_mode=dpp.GN_SPLICED):
     return dpp.make_params(cfg.B, cfg.H, cfg.W, cfg.C, cfg.P, cfg.G, cfg.heads,
                            dpp.BF16 if cfg.dtype == "bf16" else dpp.F32, refresh=refresh,
-                           eps=cfg.eps)
+                           eps=cfg.eps, fuse_gn=fuse_gn, gn_mode=gn_mode)
 
 
 CFGS = {
@@ -51,15 +51,32 @@ CFGS = {
     "small_bf16": synth.LayerConfig("small", B=1, H=16, W=64, C=128, P=4, G=8, heads=2,
                                     head_dim=64, dtype="bf16"),
     "sdxl1024_mid": synth.SDXL1024_MID,
+    # tiles of eight 16-pixel rows, and of half a 256-pixel row (the conv's two box shapes
+    # at the image's left and right edges)
+    "narrow_bf16": synth.LayerConfig("narrow", B=2, H=32, W=16, C=128, P=4, G=8, heads=2,
+                                     head_dim=64, dtype="bf16"),
+    "wide_bf16": synth.LayerConfig("wide", B=1, H=8, W=256, C=128, P=2, G=8, heads=2,
+                                   head_dim=64, dtype="bf16"),
 }
 
 
-@pytest.mark.parametrize("name", list(CFGS))
-def test_layer_stale_step_stagewise_and_end_to_end(name):
+def _y_rows(cfg, fuse):
+    """Rows of the workspace's y the step writes: all of them, or with the fused GroupNorm
+    only each band's first and last row (the conv normalises its own band's rows of x)."""
+    if not fuse:
+        return np.arange(cfg.H)
+    Hp = cfg.H // cfg.P
+    return np.array(sorted({r for p in range(1, cfg.P) for r in (p * Hp - 1, p * Hp)}),
+                    dtype=np.int64)
+
+
+@pytest.mark.parametrize("name,fuse", [(n, False) for n in CFGS] +
+                         [(n, True) for n in CFGS if CFGS[n].dtype == "bf16"])
+def test_layer_stale_step_stagewise_and_end_to_end(name, fuse):
     cfg = CFGS[name]
     tol = TOL_BF16 if cfg.dtype == "bf16" else TOL_F32
     wts, wn, x, _, _, ostate = _setup(cfg)
-    prm = _params(cfg)
+    prm = _params(cfg, fuse_gn=fuse)
     state, ws = _gpu_state_from(ostate, cfg, prm)
     old = {k: v.clone() for k, v in state.items()}
     wd = {k: v.cuda() for k, v in wts.items()}
@@ -75,9 +92,23 @@ def test_layer_stale_step_stagewise_and_end_to_end(name):
     # a2: GroupNorm with spliced statistics
     y = oracle.gn_apply_spliced(np64(x), fresh, ostate["gn_stats"], wn["gamma"], wn["beta"], G,
                                 cfg.eps, dt)
-    assert rel_err(v["y"], y) < tol
-    # a3: halo conv on the GPU's y, halo rows from the state
-    h = oracle.halo_conv3x3(v["y"], ostate["y_stale"], wn["w_conv"], P, dt)
+    rows = _y_rows(cfg, fuse)
+    if len(rows):
+        assert rel_err(v["y"][:, rows], y[:, rows]) < tol
+    if fuse:
+        # the parameters the conv applies: (x - mean) * scale + beta of each band is the
+        # oracle's GroupNorm before rounding, and beta is passed through
+        par = v["gn_params"]                                    # [B, P, 3, C]
+        Hp = cfg.H // P
+        xb = np64(x).reshape(B, P, Hp, cfg.W, C)
+        yb = (xb - par[:, :, None, None, 0]) * par[:, :, None, None, 1] + par[:, :, None, None, 2]
+        ye = oracle.gn_apply_spliced(np64(x), fresh, ostate["gn_stats"], wn["gamma"], wn["beta"],
+                                     G, cfg.eps, "f64")
+        assert rel_err(yb.reshape(y.shape), ye) < 1e-5
+        np.testing.assert_array_equal(par[:, :, 2], np.broadcast_to(wn["beta"], (B, P, C)))
+    # a3: halo conv, halo rows from the state; on the GPU's y, or with the fused GroupNorm
+    # on the oracle's (the GPU's own band rows exist only inside the conv)
+    h = oracle.halo_conv3x3(y if fuse else v["y"], ostate["y_stale"], wn["w_conv"], P, dt)
     assert rel_err(v["h"], h) < tol
     # a4: projections of the GPU's h
     hf = v["h"].reshape(B, L, C)
@@ -107,11 +138,12 @@ def test_layer_stale_step_stagewise_and_end_to_end(name):
     assert e2e < (TOL_CHAIN_BF16 if dt == "bf16" else TOL_F32), e2e
 
 
-@pytest.mark.parametrize("name", ["tiny_f32", "small_bf16"])
-def test_layer_sync_step_and_state(name):
+@pytest.mark.parametrize("name,fuse", [("tiny_f32", False), ("small_bf16", False),
+                                      ("small_bf16", True)])
+def test_layer_sync_step_and_state(name, fuse):
     cfg = CFGS[name]
     wts, wn, _, x_prev, sync_fwd, ostate = _setup(cfg)
-    prm = _params(cfg)
+    prm = _params(cfg, fuse_gn=fuse)
     state, ws = dpp.alloc_layer(prm)
     state["k_stale"].fill_(7.0)
     wd = {k: t.cuda() for k, t in wts.items()}
@@ -131,7 +163,8 @@ def test_layer_sync_step_and_state(name):
         np.testing.assert_array_equal(np64(state["y_stale"])[:, rows], v["y"][:, rows])
 
 
-def test_layer_sync_equals_unpartitioned_on_gpu():
+@pytest.mark.parametrize("fuse", [False, True])
+def test_layer_sync_equals_unpartitioned_on_gpu(fuse):
     """At the synchronous step the P-patch layer equals the P = 1 layer."""
     base = CFGS["small_bf16"]
     outs = []
@@ -140,7 +173,7 @@ def test_layer_sync_equals_unpartitioned_on_gpu():
                                 heads=base.heads, head_dim=64, dtype="bf16")
         wts = synth.layer_weights(cfg, seed=1, affine=True)
         x, _ = synth.layer_inputs(cfg, seed=1)
-        prm = _params(cfg)
+        prm = _params(cfg, fuse_gn=fuse)
         state, ws = dpp.alloc_layer(prm)
         out = torch.empty(cfg.B, cfg.H, cfg.W, cfg.C, dtype=torch.bfloat16, device="cuda")
         dpp.patch_layer_step(prm, {k: t.cuda() for k, t in wts.items()}, state, x.cuda(), out,
@@ -165,17 +198,16 @@ def test_layer_no_sync_leaves_state():
 
 
 @pytest.mark.parametrize("gn_mode", [dpp.GN_SYNC, dpp.GN_PREVIOUS])
-@pytest.mark.parametrize("name", ["tiny_f32", "small_bf16"])
-def test_layer_gn_modes(name, gn_mode):
+@pytest.mark.parametrize("name,fuse", [("tiny_f32", False), ("small_bf16", False),
+                                      ("small_bf16", True)])
+def test_layer_gn_modes(name, fuse, gn_mode):
     """The GroupNorm statistics variants at a stale step: DPP_GN_SYNC (every patch
     fresh, conv and attention still stale) and DPP_GN_PREVIOUS (every patch from the
     previous step).  The GroupNorm stage on the GPU's own bytes, then end to end."""
     cfg = CFGS[name]
     tol = TOL_BF16 if cfg.dtype == "bf16" else TOL_F32
     wts, wn, x, _, _, ostate = _setup(cfg)
-    prm = dpp.make_params(cfg.B, cfg.H, cfg.W, cfg.C, cfg.P, cfg.G, cfg.heads,
-                          dpp.BF16 if cfg.dtype == "bf16" else dpp.F32, eps=cfg.eps,
-                          gn_mode=gn_mode)
+    prm = _params(cfg, fuse_gn=fuse, gn_mode=gn_mode)
     state, ws = _gpu_state_from(ostate, cfg, prm)
     out = torch.empty(cfg.B, cfg.H, cfg.W, cfg.C, dtype=x.dtype, device="cuda")
     dpp.patch_layer_step(prm, {k: t.cuda() for k, t in wts.items()}, state, x.cuda(), out,
@@ -185,7 +217,8 @@ def test_layer_gn_modes(name, gn_mode):
     fresh = oracle.gn_partial_stats(np64(x), cfg.P, cfg.G)
     y = oracle.gn_apply_spliced(np64(x), fresh, ostate["gn_stats"], wn["gamma"], wn["beta"],
                                 cfg.G, cfg.eps, cfg.dtype, gn_mode)
-    assert rel_err(v["y"], y) < tol
+    rows = _y_rows(cfg, fuse)
+    assert rel_err(v["y"][:, rows], y[:, rows]) < tol
     # the state keeps this step's own fresh sums whatever the mode
     np.testing.assert_array_equal(np64(state["gn_stats"]), v["gn_fresh"])
     fwd = oracle.layer_forward(np64(x), ostate, wn, cfg.P, cfg.G, cfg.heads, cfg.eps, cfg.dtype,
@@ -193,8 +226,9 @@ def test_layer_gn_modes(name, gn_mode):
     assert rel_err(np64(out), fwd["out"]) < (TOL_CHAIN_BF16 if cfg.dtype == "bf16" else TOL_F32)
 
 
-@pytest.mark.parametrize("name", ["tiny_f32", "small_bf16"])
-def test_layer_periodic_refresh_sequence(name):
+@pytest.mark.parametrize("name,fuse", [("tiny_f32", False), ("small_bf16", False),
+                                      ("small_bf16", True)])
+def test_layer_periodic_refresh_sequence(name, fuse):
     """Periodic layer-context refresh ("OTIL for SDXL on 4x L40S"): a synchronous step
     every third step, stale steps with the compressed refresh in between.  At every
     step the output matches the oracle run on the same state, and the new state is
@@ -202,7 +236,7 @@ def test_layer_periodic_refresh_sequence(name):
     differs by one rounding may legitimately change a code)."""
     cfg = CFGS[name]
     wts, wn, _, _, _, _ = _setup(cfg)
-    prm = _params(cfg)
+    prm = _params(cfg, fuse_gn=fuse)
     state, ws = dpp.alloc_layer(prm)
     wd = {k: t.cuda() for k, t in wts.items()}
     dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
