@@ -416,6 +416,10 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
   // into fixed-size tables on the stack and launched whenever a table fills up.
   const long long blc = M * p.C;
   dpp::RefreshTable tab{};
+  // The refresh runs alongside the output projection, which touches none of its
+  // buffers; the kernels that read the old state (conv, attention) and wrote the fresh
+  // K, V, y had all completed before the projection passed its own dependency wait.
+  tab.early = 1;
   long long coff = 0, soff = 0;
   auto add = [&](const void* fr, void* stl, long long n) -> int {
     const bool ok = aligned16(fr) && aligned16(stl) && aligned16(st->codes + coff);

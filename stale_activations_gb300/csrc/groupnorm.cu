@@ -26,6 +26,9 @@ __device__ __forceinline__ int lanes_per_sum(int nsum) {
   return t;
 }
 
+// Pixels a thread loads before it uses any of them (one batch in flight).
+constexpr int kGnBatch = 8;
+
 template <typename T>
 __global__ void __launch_bounds__(256) gn_stats_kernel(const T* __restrict__ x,
                                                        float* __restrict__ partial, GnDims g,
@@ -52,26 +55,20 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const T* __restrict__ x,
   for (int i = 0; i < VEC; ++i) { s1[i] = 0.f; s2[i] = 0.f; }
   if (pl < PIX) {
     const T* base = x + (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C + v * VEC;
-    long long px = p0 + pl;
-    for (; px + 3 * PIX < p1; px += 4 * PIX) {  // four independent loads in flight
-      uint4 u[4];
+    for (long long px = p0 + pl; px < p1; px += kGnBatch * PIX) {
+      uint4 u[kGnBatch];
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        u[k] = __ldg(reinterpret_cast<const uint4*>(base + (px + k * PIX) * g.C));
+      for (int k = 0; k < kGnBatch; ++k)
+        if (px + k * PIX < p1)
+          u[k] = __ldg(reinterpret_cast<const uint4*>(base + (px + k * PIX) * g.C));
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kGnBatch; ++k) {
+        if (px + k * PIX >= p1) break;
         float f[VEC];
         unpack16(u[k], f);
 #pragma unroll
         for (int i = 0; i < VEC; ++i) { s1[i] += f[i]; s2[i] = fmaf(f[i], f[i], s2[i]); }
       }
-    }
-    for (; px < p1; px += PIX) {
-      uint4 u = __ldg(reinterpret_cast<const uint4*>(base + px * g.C));
-      float f[VEC];
-      unpack16(u, f);
-#pragma unroll
-      for (int i = 0; i < VEC; ++i) { s1[i] += f[i]; s2[i] = fmaf(f[i], f[i], s2[i]); }
     }
     float* r1 = red + (long long)pl * g.C + v * VEC;
     float* r2 = red + (long long)PIX * g.C + (long long)pl * g.C + v * VEC;
@@ -117,112 +114,135 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
                                                        float* __restrict__ params_out,
                                                        int halo_only) {
   constexpr int VEC = Vec<T>::N;
-  extern __shared__ float sm[];  // mean[C], scale[C], beta[C], group sums [P][G][2]
+  extern __shared__ float sm[];  // group sums [P][G][2], then mean and rstd [G][2]
   const bool all_fresh = mode == DPP_GN_SYNC;
-  float* s_mu = sm;
-  float* s_sc = sm + g.C;
-  float* s_be = sm + 2 * g.C;
-  float* s_tot = sm + 3 * g.C;  // [P][G][2]: own patch fresh, others fresh or stale
+  const int G2 = g.G * 2;
+  float* s_tot = sm;  // own patch fresh, the others fresh or stale
+  float* s_grp = sm + g.P * G2;
   const int chunk = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
+  // each thread keeps one 16-byte channel vector (and its parameters in registers) and
+  // walks the block's pixels
+  const int NV = g.C / VEC;
+  const int PIX = 256 / NV;
+  const int pl = tid / NV, v = tid % NV;
+  const bool active = pl < PIX;
+  const long long band_pix = (long long)g.Hp * g.W;
+  long long p0 = (long long)chunk * g.chunk_pix;
+  long long p1 = min(band_pix, p0 + g.chunk_pix);
+  bool rows = true;
+  if (halo_only) {  // block 0: the band's first row (p > 0), block 1: its last (p < P-1)
+    rows = !((chunk == 0 && p == 0) || (chunk == 1 && p == g.P - 1));
+    p0 = chunk == 0 ? 0 : (long long)(g.Hp - 1) * g.W;
+    p1 = p0 + g.W;
+  }
+  const long long base = (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C + v * VEC;
+
+  // What does not depend on the stats kernel is fetched before waiting for it: the first
+  // batch of x, this thread's gamma and beta, the stale sums.  (Every block of the
+  // stats kernel has passed its own wait for the kernels before it when this grid
+  // starts, so their outputs are complete.)
+  uint4 u[kGnBatch];
+  long long px = p0 + pl;
+  if (active && rows) {
+#pragma unroll
+    for (int k = 0; k < kGnBatch; ++k)
+      if (px + k * PIX < p1)
+        u[k] = __ldcs(reinterpret_cast<const uint4*>(x + base + (px + k * PIX) * g.C));
+  }
+  float ga[VEC], be[VEC];
+  if (active) {
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      ga[k] = __ldg(gamma + v * VEC + k);
+      be[k] = __ldg(beta + v * VEC + k);
+    }
+  }
+  if (!all_fresh)
+    for (int idx = tid; idx < g.P * G2; idx += blockDim.x)
+      if (idx / G2 != p) s_tot[idx] = stale_stats[(long long)b * g.P * G2 + idx];
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   // fresh sums over chunks, for own patch (and every patch when all are fresh): tps
   // threads per sum, each a fixed stride of chunks with eight loads in flight, then a
-  // shuffle tree (fixed order); the other patches' sums come from the stale statistics
-  const int G2 = g.G * 2;
+  // shuffle tree (fixed order)
   const int nq = all_fresh ? g.P : 1;
   const int tps = lanes_per_sum(nq * G2);
   for (int t0 = 0; t0 < nq * G2 * tps; t0 += blockDim.x) {
     const int t = t0 + tid, si = t / tps, part = t % tps;
     const int q = all_fresh ? si / G2 : p, r = si % G2;
-    float v = 0.f;
+    float val = 0.f;
     if (si < nq * G2) {
       const float* src = partial + (((long long)b * g.P + q) * g.nchunk) * G2 + r;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       int c = part;
       for (; c + 7 * tps < g.nchunk; c += 8 * tps) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) acc[u] += src[(long long)(c + u * tps) * G2];
+        for (int k = 0; k < 8; ++k) acc[k] += src[(long long)(c + k * tps) * G2];
       }
 #pragma unroll
-      for (int u = 0; u < 7; ++u)
-        if (c + u * tps < g.nchunk) acc[u] += src[(long long)(c + u * tps) * G2];
-      v = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+      for (int k = 0; k < 7; ++k)
+        if (c + k * tps < g.nchunk) acc[k] += src[(long long)(c + k * tps) * G2];
+      val = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     }
-    for (int m = tps >> 1; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-    if (si < nq * G2 && part == 0) s_tot[q * G2 + r] = v;
+    for (int m = tps >> 1; m > 0; m >>= 1) val += __shfl_xor_sync(0xffffffffu, val, m);
+    if (si < nq * G2 && part == 0) s_tot[q * G2 + r] = val;
   }
-  if (!all_fresh)
-    for (int idx = tid; idx < g.P * G2; idx += blockDim.x)
-      if (idx / G2 != p) s_tot[idx] = stale_stats[((long long)b * g.P) * G2 + idx];
   __syncthreads();
-  if (chunk == 0 && fresh_out) {
-    for (int r = tid; r < g.G * 2; r += blockDim.x)
-      fresh_out[((long long)b * g.P + p) * g.G * 2 + r] = s_tot[p * g.G * 2 + r];
-  }
+  if (chunk == 0 && fresh_out)
+    for (int r = tid; r < G2; r += blockDim.x)
+      fresh_out[((long long)b * g.P + p) * G2 + r] = s_tot[p * G2 + r];
+  // group statistics: own patch first (its previous-step sums under DPP_GN_PREVIOUS),
+  // then the others in order; mu = S1/N, var = max(S2/N - mu^2, 0)
   const int cg = g.C / g.G;
   const double invN = 1.0 / ((double)g.H * g.W * cg);
-  // own patch first (its previous-step sums under DPP_GN_PREVIOUS), then the others
-  const float* own = mode == DPP_GN_PREVIOUS ? stale_stats + ((long long)b * g.P + p) * g.G * 2
-                                             : s_tot + p * g.G * 2;
-  for (int c = tid; c < g.C; c += blockDim.x) {
-    const int gi = c / cg;
+  const float* own = mode == DPP_GN_PREVIOUS ? stale_stats + ((long long)b * g.P + p) * G2
+                                             : s_tot + p * G2;
+  for (int gi = tid; gi < g.G; gi += blockDim.x) {
     float S1 = own[gi * 2], S2 = own[gi * 2 + 1];
     for (int q = 0; q < g.P; ++q)
-      if (q != p) { S1 += s_tot[q * g.G * 2 + gi * 2]; S2 += s_tot[q * g.G * 2 + gi * 2 + 1]; }
+      if (q != p) { S1 += s_tot[q * G2 + gi * 2]; S2 += s_tot[q * G2 + gi * 2 + 1]; }
     const float mu = (float)(S1 * invN);
     const float var = fmaxf((float)(S2 * invN) - mu * mu, 0.f);
-    const float rstd = rsqrtf(var + eps);
-    s_mu[c] = mu;
-    s_sc[c] = rstd * gamma[c];
-    s_be[c] = beta[c];
-    if (params_out && chunk == 0) {  // the per-channel parameters, for a fused consumer
-      float* dst = params_out + ((long long)b * g.P + p) * 3 * g.C;
-      dst[c] = mu;
-      dst[g.C + c] = s_sc[c];
-      dst[2 * g.C + c] = s_be[c];
-    }
+    s_grp[gi * 2] = mu;
+    s_grp[gi * 2 + 1] = rsqrtf(var + eps);
   }
   __syncthreads();
-  // each thread keeps one 16-byte channel vector (and its GroupNorm parameters in
-  // registers) and walks pixels, four loads in flight
-  const int NV = g.C / VEC;
-  const int PIX = 256 / NV;
-  const int pl = tid / NV, v = tid % NV;
-  if (pl >= PIX) return;
-  float mu[VEC], sc[VEC], be[VEC];
+  if (!active) return;
+  float mu[VEC], sc[VEC];
 #pragma unroll
   for (int k = 0; k < VEC; ++k) {
-    mu[k] = s_mu[v * VEC + k];
-    sc[k] = s_sc[v * VEC + k];
-    be[k] = s_be[v * VEC + k];
+    const int gi = (v * VEC + k) / cg;
+    mu[k] = s_grp[gi * 2];
+    sc[k] = s_grp[gi * 2 + 1] * ga[k];
   }
-  const long long band_pix = (long long)g.Hp * g.W;
-  long long p0 = (long long)chunk * g.chunk_pix;
-  long long p1 = min(band_pix, p0 + g.chunk_pix);
-  if (halo_only) {  // block 0: the band's first row (p > 0), block 1: its last (p < P-1)
-    if ((chunk == 0 && p == 0) || (chunk == 1 && p == g.P - 1)) return;
-    p0 = chunk == 0 ? 0 : (long long)(g.Hp - 1) * g.W;
-    p1 = p0 + g.W;
+  if (params_out && chunk == 0 && pl == 0) {  // the per-channel parameters, for a fused consumer
+    float* dst = params_out + ((long long)b * g.P + p) * 3 * g.C + v * VEC;
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      dst[k] = mu[k];
+      dst[g.C + k] = sc[k];
+      dst[2 * g.C + k] = be[k];
+    }
   }
-  const long long base = (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C + v * VEC;
-  auto apply_one = [&](const uint4& u, long long px) {
-    float f[VEC];
-    unpack16(u, f);
+  if (!rows) return;
+  for (;;) {
 #pragma unroll
-    for (int k = 0; k < VEC; ++k) f[k] = fmaf(f[k] - mu[k], sc[k], be[k]);
-    *reinterpret_cast<uint4*>(y + base + px * g.C) = pack16(f);
-  };
-  long long px = p0 + pl;
-  for (; px + 3 * PIX < p1; px += 4 * PIX) {
-    uint4 u[4];
+    for (int k = 0; k < kGnBatch; ++k) {
+      if (px + k * PIX >= p1) break;
+      float f[VEC];
+      unpack16(u[k], f);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) u[k] = __ldcs(reinterpret_cast<const uint4*>(x + base + (px + k * PIX) * g.C));
+      for (int i = 0; i < VEC; ++i) f[i] = fmaf(f[i] - mu[i], sc[i], be[i]);
+      *reinterpret_cast<uint4*>(y + base + (px + k * PIX) * g.C) = pack16(f);
+    }
+    px += kGnBatch * PIX;
+    if (px >= p1) break;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) apply_one(u[k], px + k * PIX);
+    for (int k = 0; k < kGnBatch; ++k)
+      if (px + k * PIX < p1)
+        u[k] = __ldcs(reinterpret_cast<const uint4*>(x + base + (px + k * PIX) * g.C));
   }
-  for (; px < p1; px += PIX) apply_one(__ldcs(reinterpret_cast<const uint4*>(x + base + px * g.C)), px);
 }
 
 GnDims make_gn_dims(int B, int H, int W, int C, int P, int G) {
@@ -230,6 +250,8 @@ GnDims make_gn_dims(int B, int H, int W, int C, int P, int G) {
   g.B = B; g.H = H; g.W = W; g.C = C; g.P = P; g.G = G;
   g.Hp = H / P;
   const long long band_pix = (long long)g.Hp * W;
+  // two blocks per SM in one wave (the apply kernel holds a batch of x in registers,
+  // which allows two 256-thread blocks per SM); long per-thread pixel runs stream best
   long long nchunk = (2ll * kNumSMs + (long long)B * P - 1) / ((long long)B * P);
   if (nchunk > band_pix) nchunk = band_pix;
   if (nchunk < 1) nchunk = 1;
@@ -252,7 +274,7 @@ int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, 
   const int NV = g.C / VEC;
   const int PIX = 256 / NV;
   const size_t red_bytes = 2ull * PIX * g.C * sizeof(float);
-  const size_t app_bytes = (3ull * g.C + 2ull * g.P * g.G) * sizeof(float);
+  const size_t app_bytes = (2ull * g.P * g.G + 2ull * g.G) * sizeof(float);
   using dpp_host::launch_pdl;
   cudaError_t e;
   if (dtype == DPP_BF16) {

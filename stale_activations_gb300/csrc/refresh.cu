@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(256, 4) refresh_kernel(const __grid_constant__
                           (lane >> 4);
   const long long stride = (long long)gridDim.x * (blockDim.x >> 5) * 2;
   const long long total = tab.blk_start[tab.nseg];
-  ptx::grid_dep_wait();
+  if (!tab.early) ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < tab.copy_n; i += blockDim.x) tab.copy_dst[i] = tab.copy_src[i];
@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(256, 4) refresh_kernel(const __grid_constant__
                               (int)min(128ll, sg.n - e0), sub, hmask);
     }
   }
+  if (tab.early) ptx::grid_dep_wait();
 }
 
 int launch_refresh(const RefreshTable& tab, int dtype, cudaStream_t stream) {

@@ -24,6 +24,11 @@ struct RefreshTable {
   int copy_n;
   const float* copy_src;
   float* copy_dst;
+  // 1 when the kernel launched just before this one neither reads nor writes any buffer
+  // of the table, and every kernel that does has completed before that one started
+  // (its griddepcontrol.wait returned): the refresh then runs alongside it and waits
+  // for it only at the end, which keeps completion ordered down the stream
+  int early;
 };
 
 // Launches one refresh over all segments of `tab` (blk_start filled by caller).
