@@ -195,6 +195,11 @@ typedef struct dpp_layer_params {
                       the workspace's y holds only each band's first and last row (the
                       rows the neighbours read as halos); 0 = a separate apply pass
                       writes all of y (the faster choice on the SDXL-1024 layer) */
+  int fuse_refresh; /* DPP_BF16 with C a multiple of 128 only (0 otherwise); used only
+                      when the step gets the second state set: 1 = the K/V refresh runs
+                      in the Q/K/V projection's epilogue instead of a separate pass
+                      after the output projection (same message and values; the
+                      separate pass is the faster choice on the SDXL-1024 layer) */
 } dpp_layer_params;
 
 typedef struct dpp_layer_weights {
@@ -214,6 +219,17 @@ typedef struct dpp_layer_state {
   int8_t* codes;   /* [dpp_message_elems] int8 residual codes (message order: K, V,
                       then for each batch the P-1 halo ranges of 2*W*C elements) */
   float* scales;   /* [dpp_message_blocks] fp32 block scales, same order */
+  /* Optional second state (all four or none; none of them may overlap its counterpart
+     above).  When given, a step reads the state above and leaves it unchanged, and
+     writes the new state here (same layouts): a synchronous step the exact copies, a
+     stale step with refresh the refreshed values, a stale step without refresh nothing
+     (the caller then keeps the state above).  The caller swaps the two sets after a step
+     that wrote them.  The message (codes, scales) is the same as with the in-place
+     state; see fuse_refresh for where the K/V refresh then runs. */
+  float* gn_next;
+  void* y_next;
+  void* k_next;
+  void* v_next;
 } dpp_layer_state;
 
 /* Byte offsets of the pieces of the caller-allocated workspace (all 256-aligned). */

@@ -19,7 +19,8 @@ __all__ = [
     "DppError", "load", "F32", "BF16", "SYNC", "STALE", "LayerParams", "LayerWeights",
     "LayerState", "WorkspaceLayout", "refresh_residual", "halo_conv3x3", "stale_kv_attention",
     "patch_layer_step", "workspace_layout", "workspace_size", "message_sizes",
-    "read_device_status", "layer_kernel_count", "status_string", "dtype_code",
+    "read_device_status", "layer_kernel_count", "status_string", "dtype_code", "alloc_layer",
+    "swap_state",
 ]
 
 F32, BF16 = 0, 1
@@ -37,7 +38,7 @@ class LayerParams(ctypes.Structure):
     _fields_ = [("B", _c_int), ("H", _c_int), ("W", _c_int), ("C", _c_int), ("P", _c_int),
                 ("G", _c_int), ("heads", _c_int), ("head_dim", _c_int), ("dtype", _c_int),
                 ("refresh", _c_int), ("eps", ctypes.c_float), ("gn_mode", _c_int),
-                ("fuse_gn", _c_int)]
+                ("fuse_gn", _c_int), ("fuse_refresh", _c_int)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -47,7 +48,9 @@ class LayerWeights(ctypes.Structure):
 
 class LayerState(ctypes.Structure):
     _fields_ = [("gn_stats", _c_void), ("y_stale", _c_void), ("k_stale", _c_void),
-                ("v_stale", _c_void), ("codes", _c_void), ("scales", _c_void)]
+                ("v_stale", _c_void), ("codes", _c_void), ("scales", _c_void),
+                ("gn_next", _c_void), ("y_next", _c_void), ("k_next", _c_void),
+                ("v_next", _c_void)]
 
 
 class WorkspaceLayout(ctypes.Structure):
@@ -235,9 +238,9 @@ GN_SPLICED, GN_SYNC, GN_PREVIOUS = 0, 1, 2
 
 
 def make_params(B, H, W, C, P, G, heads, dtype, refresh=True, eps=1e-5, head_dim=64,
-                gn_mode=GN_SPLICED, fuse_gn=False):
+                gn_mode=GN_SPLICED, fuse_gn=False, fuse_refresh=False):
     return LayerParams(B, H, W, C, P, G, heads, head_dim, dtype, 1 if refresh else 0, eps,
-                       gn_mode, 1 if fuse_gn else 0)
+                       gn_mode, 1 if fuse_gn else 0, 1 if fuse_refresh else 0)
 
 
 def workspace_layout(prm: LayerParams) -> WorkspaceLayout:
@@ -261,6 +264,18 @@ def layer_kernel_count(prm: LayerParams, mode: int) -> int:
 
 NUM_STAGE_EVENTS = 7
 STAGES = ("groupnorm", "halo_conv", "qkv_proj", "attention", "out_proj", "state_update")
+NEXT_KEYS = ("gn_next", "y_next", "k_next", "v_next")
+STATE_KEYS = ("gn_stats", "y_stale", "k_stale", "v_stale")
+
+
+def _layer_state(state: dict) -> "LayerState":
+    return LayerState(*[_ptr(state.get(k)) for k in STATE_KEYS + ("codes", "scales") + NEXT_KEYS])
+
+
+def swap_state(state: dict):
+    """After a step that wrote the second state set: makes it the current one."""
+    for cur, nxt in zip(STATE_KEYS, NEXT_KEYS):
+        state[cur], state[nxt] = state[nxt], state[cur]
 
 
 def patch_layer_step(prm: LayerParams, weights: dict, state: dict, x, out, mode: int, workspace,
@@ -269,14 +284,14 @@ def patch_layer_step(prm: LayerParams, weights: dict, state: dict, x, out, mode:
 
     weights: gamma, beta (fp32 [C]), w_conv [C,3,3,C], w_qkv [3C,C], w_o [C,C].
     state:   gn_stats [B,P,G,2] fp32, y_stale [B,H,W,C], k_stale/v_stale [B,L,C],
-             codes int8 [message elems], scales fp32 [message blocks].
+             codes int8 [message elems], scales fp32 [message blocks]; optionally the
+             second set gn_next, y_next, k_next, v_next (see swap_state).
     workspace: uint8 device tensor of workspace_size(prm) bytes.
     """
     lib = load()
     w = LayerWeights(_ptr(weights["gamma"]), _ptr(weights["beta"]), _ptr(weights["w_conv"]),
                      _ptr(weights["w_qkv"]), _ptr(weights["w_o"]))
-    s = LayerState(_ptr(state["gn_stats"]), _ptr(state["y_stale"]), _ptr(state["k_stale"]),
-                   _ptr(state["v_stale"]), _ptr(state.get("codes")), _ptr(state.get("scales")))
+    s = _layer_state(state)
     if stage_events is None:
         _check(lib.patch_layer_step(ctypes.byref(prm), ctypes.byref(w), ctypes.byref(s), _ptr(x),
                                     _ptr(out), mode, _ptr(workspace), _stream(stream)),
@@ -302,8 +317,7 @@ def patch_layer_step_noalloc(prm: LayerParams, weights: dict, state: dict, x, ou
     lib = load()
     w = LayerWeights(_ptr(weights["gamma"]), _ptr(weights["beta"]), _ptr(weights["w_conv"]),
                      _ptr(weights["w_qkv"]), _ptr(weights["w_o"]))
-    s = LayerState(_ptr(state["gn_stats"]), _ptr(state["y_stale"]), _ptr(state["k_stale"]),
-                   _ptr(state["v_stale"]), _ptr(state.get("codes")), _ptr(state.get("scales")))
+    s = _layer_state(state)
     _check(lib.patch_layer_step_noalloc(ctypes.byref(prm), ctypes.byref(w), ctypes.byref(s),
                                         _ptr(x), _ptr(out), mode, _stream(stream)),
            "patch_layer_step_noalloc")
@@ -314,8 +328,10 @@ def read_device_status(workspace, stream=None) -> int:
 
 
 # ------------------------------------------------------------------ helpers for callers
-def alloc_layer(prm: LayerParams, device="cuda"):
-    """Allocates (with torch) the state, message and workspace of one layer."""
+def alloc_layer(prm: LayerParams, device="cuda", double_buffer=False):
+    """Allocates (with torch) the state, message and workspace of one layer; with
+    double_buffer also the second state set the step writes (gn_next, y_next, k_next,
+    v_next), to be swapped in after each step that writes it (swap_state)."""
     dt = torch.bfloat16 if prm.dtype == BF16 else torch.float32
     B, H, W, C, P, G = prm.B, prm.H, prm.W, prm.C, prm.P, prm.G
     n_codes, n_scales = message_sizes(prm)
@@ -327,6 +343,9 @@ def alloc_layer(prm: LayerParams, device="cuda"):
         codes=torch.zeros(n_codes, dtype=torch.int8, device=device),
         scales=torch.zeros(n_scales, dtype=torch.float32, device=device),
     )
+    if double_buffer:
+        for cur, nxt in zip(STATE_KEYS, NEXT_KEYS):
+            state[nxt] = torch.zeros_like(state[cur])
     ws = torch.zeros(workspace_size(prm), dtype=torch.uint8, device=device)
     return state, ws
 

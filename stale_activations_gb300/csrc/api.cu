@@ -85,6 +85,9 @@ int check_layer(const dpp_layer_params* p) {
   if (p->refresh != 0 && p->refresh != 1) return DPP_ERR_ARG;
   if (p->gn_mode < DPP_GN_SPLICED || p->gn_mode > DPP_GN_PREVIOUS) return DPP_ERR_ARG;
   if (p->fuse_gn != 0 && !(p->fuse_gn == 1 && p->dtype == DPP_BF16)) return DPP_ERR_ARG;
+  if (p->fuse_refresh != 0 &&
+      !(p->fuse_refresh == 1 && p->dtype == DPP_BF16 && p->C % 128 == 0))
+    return DPP_ERR_ARG;
   if (!(p->eps >= 0.f)) return DPP_ERR_ARG;
   rc = check_conv(p->B, p->H, p->W, p->C, p->C, p->P, p->dtype);
   if (rc) return rc;
@@ -200,7 +203,7 @@ int refresh_residual(const void* fresh, void* stale, int8_t* codes, float* scale
   if (!aligned16(fresh) || !aligned16(stale) || !aligned16(codes) ||
       (reinterpret_cast<uintptr_t>(scales) & 3u))
     return DPP_ERR_ALIGN;
-  dpp::RefreshSeg sg{fresh, stale, codes, scales, (long long)n, 1, 0};
+  dpp::RefreshSeg sg{fresh, stale, codes, scales, (long long)n, 1, 0, stale};
   return refresh_segments(&sg, 1, dtype, static_cast<cudaStream_t>(stream));
 }
 
@@ -326,6 +329,25 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
   if (!st->gn_stats || !st->y_stale || !st->k_stale || !st->v_stale) return DPP_ERR_NULL;
   const bool refresh = mode == DPP_STALE && p.refresh;
   if (refresh && (!st->codes || !st->scales)) return DPP_ERR_NULL;
+  // the second state set: all four buffers or none, none equal to its counterpart
+  const int nnext = (st->gn_next != nullptr) + (st->y_next != nullptr) +
+                    (st->k_next != nullptr) + (st->v_next != nullptr);
+  if (nnext != 0 && nnext != 4) return DPP_ERR_NULL;
+  const bool dbuf = nnext == 4;
+  if (dbuf && (st->gn_next == st->gn_stats || st->y_next == st->y_stale ||
+               st->k_next == st->k_stale || st->v_next == st->v_stale))
+    return DPP_ERR_ARG;
+  if (dbuf && (!aligned16(st->y_next) || !aligned16(st->k_next) || !aligned16(st->v_next) ||
+               (reinterpret_cast<uintptr_t>(st->gn_next) & 3u)))
+    return DPP_ERR_ALIGN;
+  // where the new state goes
+  float* const gn_dst = dbuf ? st->gn_next : st->gn_stats;
+  void* const y_dst = dbuf ? st->y_next : st->y_stale;
+  void* const k_dst = dbuf ? st->k_next : st->k_stale;
+  void* const v_dst = dbuf ? st->v_next : st->v_stale;
+  // with a second set and fuse_refresh (bf16, whole 128-element blocks per K/V row), the
+  // K/V refresh runs in the projection's epilogue
+  const bool fuse_rfx = refresh && dbuf && p.fuse_refresh;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return DPP_ERR_ALIGN;
   if (!aligned16(x) || !aligned16(out) || !aligned16(wts->w_conv) || !aligned16(wts->w_qkv) ||
       !aligned16(wts->w_o) || !aligned16(st->y_stale) || !aligned16(st->k_stale) ||
@@ -357,6 +379,56 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
                ? DPP_OK
                : DPP_ERR_CUDA;
   };
+  // state geometry and the compressed refresh (a7/a8) of the segments in message order:
+  // K, V (with_kv), then each batch's P-1 halo ranges of y, packed into fixed-size
+  // tables and launched whenever a table fills up; the last launch also copies the fresh
+  // GroupNorm sums.  Every launch runs alongside the kernel before it, which must touch
+  // none of its buffers (the table's `early`).
+  const size_t es = esize(p.dtype);
+  const size_t act = (size_t)M * p.C * es;
+  const size_t gn_bytes = (size_t)p.B * p.P * p.G * 2 * sizeof(float);
+  const size_t halo_bytes = 2ull * p.W * p.C * es;            // rows r-1 and r
+  const size_t band_bytes = (size_t)(p.H / p.P) * p.W * p.C * es;
+  const size_t img_bytes = (size_t)p.H * p.W * p.C * es;
+  const long long blc = M * p.C;
+  auto refresh_state = [&](bool with_kv) -> int {
+    dpp::RefreshTable tab{};
+    tab.early = 1;
+    long long coff = with_kv ? 0 : 2 * blc, soff = with_kv ? 0 : 2 * cdiv(blc, 128);
+    auto add = [&](const void* fr, void* stl, void* outp, long long n) -> int {
+      const bool ok = aligned16(fr) && aligned16(stl) && aligned16(outp) &&
+                      aligned16(st->codes + coff);
+      tab.seg[tab.nseg] = dpp::RefreshSeg{fr, stl, st->codes + coff, st->scales + soff, n,
+                                          ok ? 1 : 0, 0, outp};
+      tab.blk_start[tab.nseg + 1] = tab.blk_start[tab.nseg] + cdiv(n, 128);
+      ++tab.nseg;
+      coff += n;
+      soff += cdiv(n, 128);
+      if (tab.nseg == dpp::kMaxRefreshSegs) {
+        const int r = dpp::launch_refresh(tab, p.dtype, s);
+        tab.nseg = 0;
+        tab.blk_start[0] = 0;
+        return r;
+      }
+      return DPP_OK;
+    };
+    int r = DPP_OK;
+    if (with_kv &&
+        ((r = add(k, st->k_stale, k_dst, blc)) || (r = add(v, st->v_stale, v_dst, blc))))
+      return r;
+    for (int b = 0; b < p.B; ++b)
+      for (int pp = 1; pp < p.P; ++pp) {
+        const size_t off = b * img_bytes + pp * band_bytes - halo_bytes / 2;
+        r = add(static_cast<char*>(y) + off, static_cast<char*>(st->y_stale) + off,
+                static_cast<char*>(y_dst) + off, 2ll * p.W * p.C);
+        if (r) return r;
+      }
+    tab.copy_n = (int)(gn_bytes / sizeof(float));
+    tab.copy_src = gn_fresh;
+    tab.copy_dst = gn_dst;
+    return dpp::launch_refresh(tab, p.dtype, s);
+  };
+
   if ((rc = mark(0))) return rc;
   // a1 + a2: fresh sums of every patch, spliced GroupNorm
   const dpp::GnDims g = dpp::make_gn_dims(p.B, p.H, p.W, p.C, p.P, p.G);
@@ -378,8 +450,18 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
   rc = run_conv(fused ? x : y, sync ? y : st->y_stale, wts->w_conv, h, p.B, p.H, p.W, p.C, p.C,
                 p.P, p.dtype, gn_params, status, s);
   if (rc || (rc = mark(2))) return rc;
-  // a4: Q, K, V projections (one GEMM over the packed [3C, C] weight)
-  rc = run_linear(h, wts->w_qkv, q, k, v, M, 3 * p.C, p.C, p.dtype, status, s);
+  // a7 for the halo rows of y and a8, when the projection refreshes K and V: it runs
+  // alongside the conv's end (it writes only the second state set and the message's
+  // halo part; the conv reads the stale y, which it leaves unchanged)
+  if (fuse_rfx && (rc = refresh_state(false))) return rc;
+  // a4: Q, K, V projections (one GEMM over the packed [3C, C] weight); with fuse_rfx its
+  // epilogue also refreshes K and V into the second state set (a7)
+  if (fuse_rfx)
+    rc = dpp::launch_tc_linear_refresh(h, wts->w_qkv, q, k, v, M, 3 * p.C, p.C, st->k_stale,
+                                       st->v_stale, k_dst, v_dst, st->codes, st->scales, status,
+                                       dpp_host::wait_limit_from_env(), s);
+  else
+    rc = run_linear(h, wts->w_qkv, q, k, v, M, 3 * p.C, p.C, p.dtype, status, s);
   if (rc || (rc = mark(3))) return rc;
   // a5: stale-KV attention
   rc = run_attention(q, k, v, sync ? k : st->k_stale, sync ? v : st->v_stale, o, p.B, L, p.heads,
@@ -391,65 +473,25 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
   if (rc || (rc = mark(5))) return rc;
 
   // a7/a8: state update, after every virtual rank has read the old state
-  const size_t es = esize(p.dtype);
-  const size_t act = (size_t)M * p.C * es;
-  const size_t gn_bytes = (size_t)p.B * p.P * p.G * 2 * sizeof(float);
-  const size_t halo_bytes = 2ull * p.W * p.C * es;            // rows r-1 and r
-  const size_t band_bytes = (size_t)(p.H / p.P) * p.W * p.C * es;
-  const size_t img_bytes = (size_t)p.H * p.W * p.C * es;
   if (sync) {
-    DPP_CUDA_CHECK(cudaMemcpyAsync(st->k_stale, k, act, cudaMemcpyDeviceToDevice, s));
-    DPP_CUDA_CHECK(cudaMemcpyAsync(st->v_stale, v, act, cudaMemcpyDeviceToDevice, s));
-    DPP_CUDA_CHECK(cudaMemcpyAsync(st->gn_stats, gn_fresh, gn_bytes, cudaMemcpyDeviceToDevice, s));
+    DPP_CUDA_CHECK(cudaMemcpyAsync(k_dst, k, act, cudaMemcpyDeviceToDevice, s));
+    DPP_CUDA_CHECK(cudaMemcpyAsync(v_dst, v, act, cudaMemcpyDeviceToDevice, s));
+    DPP_CUDA_CHECK(cudaMemcpyAsync(gn_dst, gn_fresh, gn_bytes, cudaMemcpyDeviceToDevice, s));
     if (p.P > 1) {
       for (int b = 0; b < p.B; ++b) {
         const size_t off = b * img_bytes + band_bytes - halo_bytes / 2;  // row Hp-1 of batch b
-        DPP_CUDA_CHECK(cudaMemcpy2DAsync(static_cast<char*>(st->y_stale) + off, band_bytes,
+        DPP_CUDA_CHECK(cudaMemcpy2DAsync(static_cast<char*>(y_dst) + off, band_bytes,
                                          static_cast<char*>(y) + off, band_bytes, halo_bytes,
                                          p.P - 1, cudaMemcpyDeviceToDevice, s));
       }
     }
     return mark(6);
   }
-  if (!refresh) return mark(6);
-  // Segments in message order (K, V, then each batch's P-1 halo ranges), packed
-  // into fixed-size tables on the stack and launched whenever a table fills up.
-  const long long blc = M * p.C;
-  dpp::RefreshTable tab{};
+  if (!refresh || fuse_rfx) return mark(6);
   // The refresh runs alongside the output projection, which touches none of its
   // buffers; the kernels that read the old state (conv, attention) and wrote the fresh
   // K, V, y had all completed before the projection passed its own dependency wait.
-  tab.early = 1;
-  long long coff = 0, soff = 0;
-  auto add = [&](const void* fr, void* stl, long long n) -> int {
-    const bool ok = aligned16(fr) && aligned16(stl) && aligned16(st->codes + coff);
-    tab.seg[tab.nseg] =
-        dpp::RefreshSeg{fr, stl, st->codes + coff, st->scales + soff, n, ok ? 1 : 0, 0};
-    tab.blk_start[tab.nseg + 1] = tab.blk_start[tab.nseg] + cdiv(n, 128);
-    ++tab.nseg;
-    coff += n;
-    soff += cdiv(n, 128);
-    if (tab.nseg == dpp::kMaxRefreshSegs) {
-      const int r = dpp::launch_refresh(tab, p.dtype, s);
-      tab.nseg = 0;
-      tab.blk_start[0] = 0;
-      return r;
-    }
-    return DPP_OK;
-  };
-  if ((rc = add(k, st->k_stale, blc)) || (rc = add(v, st->v_stale, blc))) return rc;
-  for (int b = 0; b < p.B; ++b)
-    for (int pp = 1; pp < p.P; ++pp) {
-      const size_t off = b * img_bytes + pp * band_bytes - halo_bytes / 2;
-      rc = add(static_cast<char*>(y) + off, static_cast<char*>(st->y_stale) + off,
-               2ll * p.W * p.C);
-      if (rc) return rc;
-    }
-  // the last launch also copies the fresh GroupNorm sums into the state
-  tab.copy_n = (int)(gn_bytes / sizeof(float));
-  tab.copy_src = gn_fresh;
-  tab.copy_dst = st->gn_stats;
-  if ((rc = dpp::launch_refresh(tab, p.dtype, s))) return rc;
+  if ((rc = refresh_state(true))) return rc;
   return mark(6);
 }
 

@@ -12,15 +12,9 @@
 // 4 bytes of scale per 128.
 #include "refresh.cuh"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace dpp {
-
-__device__ __forceinline__ int quantise(float d, float s) {
-  if (s == 0.0f) return 0;
-  float t = __fdiv_rn(d, s);                 // IEEE division, as on the CPU
-  int q = __float2int_rn(t);                 // round to nearest, ties to even
-  return max(-127, min(127, q));
-}
 
 template <typename T>
 __device__ __forceinline__ void store8(T* p, const float (&f)[8]);
@@ -39,8 +33,9 @@ __device__ __forceinline__ void store8<float>(float* p, const float (&f)[8]) {
 // elements strided by 16 so that any length nb <= 128 is covered.  Used for ragged
 // last blocks and misaligned segments only (the scalar pass after the streaming loop).
 template <typename T>
-__device__ __forceinline__ void refresh_block_scalar(const T* fr, T* st, int8_t* cd, float* scale,
-                                                  int nb, int sub, unsigned hmask) {
+__device__ __forceinline__ void refresh_block_scalar(const T* fr, const T* st, T* out, int8_t* cd,
+                                                  float* scale, int nb, int sub,
+                                                  unsigned hmask) {
   float d[8], sv[8];
   float a = 0.0f;
 #pragma unroll
@@ -59,7 +54,7 @@ __device__ __forceinline__ void refresh_block_scalar(const T* fr, T* st, int8_t*
     const int e = sub + 16 * i;
     if (e < nb) {
       const int q = quantise(d[i], s);
-      st[e] = from_f32<T>(__fmaf_rn((float)q, s, sv[i]));
+      out[e] = from_f32<T>(__fmaf_rn((float)q, s, sv[i]));
       cd[e] = (int8_t)q;
     }
   }
@@ -68,7 +63,7 @@ __device__ __forceinline__ void refresh_block_scalar(const T* fr, T* st, int8_t*
 // A full, aligned block: each lane holds 8 consecutive elements as raw 128-bit vectors.
 struct VecBlock {
   uint4 fr[2], st[2];
-  void* stale;
+  void* out;  // where the refreshed values go
   int8_t* codes;
   float* scale;
   bool live;
@@ -109,17 +104,11 @@ __device__ __forceinline__ void start_block(const RefreshTable& tab, long long g
     v.fr[k] = __ldcs(reinterpret_cast<const uint4*>(fr + sub * 8) + k);
     v.st[k] = __ldcs(reinterpret_cast<const uint4*>(st + sub * 8) + k);
   }
-  v.stale = st + sub * 8;
+  v.out = static_cast<T*>(sg.out) + e0 + sub * 8;
   v.codes = sg.codes + e0 + sub * 8;
   v.scale = sg.scales + j;
   v.live = true;
 }
-
-// Rounding without conversion instructions: for |t| < 2^22 the fp32 sum t + 1.5 * 2^23
-// (round to nearest, ties to even) is exactly 1.5 * 2^23 + rint(t) with rint's ties to
-// even (the constant is even), so subtracting it back gives rint(t) as a float and the
-// low byte of the sum's bits is rint(t) as a two's-complement int8.
-constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 
 template <typename T>
 __device__ __forceinline__ void finish_block(const VecBlock& v, int sub, unsigned hmask) {
@@ -131,37 +120,12 @@ __device__ __forceinline__ void finish_block(const VecBlock& v, int sub, unsigne
   for (int i = 0; i < 8; ++i) { d[i] = f[i] - sv[i]; a = fmaxf(a, fabsf(d[i])); }
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(hmask, a, o));
-  const float s = __fdiv_rn(a, 127.0f);
-  if (sub == 0) *v.scale = s;
-  // With r = rn(1/s), t = rn(d*r) lies within 2e-5 of rn(d/s) (|d/s| <= 127.0001 and
-  // three roundings of relative size 2^-24), so both round to the same integer unless
-  // t is within 1e-4 of a half-integer; only then is the IEEE quotient formed.  A zero
-  // or subnormal s (1/s not finite) takes the IEEE rule for every element.
-  const bool fast = s >= 1.17549435e-38f;  // FLT_MIN
-  const float rc = fast ? __frcp_rn(s) : 0.0f;
-  float nv[8];
-  uint32_t c0 = 0, c1 = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float tm;
-    if (fast) {
-      const float t = d[i] * rc;
-      tm = t + kRoundMagic;
-      if (0.5f - fabsf(t - (tm - kRoundMagic)) < 1e-4f) tm = __fdiv_rn(d[i], s) + kRoundMagic;
-    } else {
-      tm = (float)quantise(d[i], s) + kRoundMagic;
-    }
-    tm = fminf(fmaxf(tm, kRoundMagic - 127.0f), kRoundMagic + 127.0f);  // clamp to +-127
-    nv[i] = __fmaf_rn(tm - kRoundMagic, s, sv[i]);
-    // the code byte (low byte of tm's bits) into byte i % 4 of c0 / c1
-    constexpr uint32_t kSel[4] = {0x3214u, 0x3240u, 0x3410u, 0x4210u};
-    if (i < 4)
-      c0 = __byte_perm(c0, __float_as_uint(tm), kSel[i]);
-    else
-      c1 = __byte_perm(c1, __float_as_uint(tm), kSel[i - 4]);
-  }
-  store8<T>(static_cast<T*>(v.stale), nv);
-  __stcs(reinterpret_cast<uint2*>(v.codes), make_uint2(c0, c1));
+  const QuantBlock qb = quant_block(a);
+  if (sub == 0) *v.scale = qb.s;
+  float tm[8], nv[8];
+  quant8(qb, d, sv, tm, nv);
+  store8<T>(static_cast<T*>(v.out), nv);
+  __stcs(reinterpret_cast<uint2*>(v.codes), pack_codes(tm));
 }
 
 // Each half warp takes two blocks per pass, issuing all four 128-bit loads before
@@ -196,7 +160,8 @@ __global__ void __launch_bounds__(256, 4) refresh_kernel(const __grid_constant__
     for (long long j = (sg.vec_ok ? sg.n / 128 : 0) + group; j < nblk; j += stride) {
       const long long e0 = j * 128;
       refresh_block_scalar<T>(reinterpret_cast<const T*>(sg.fresh) + e0,
-                              reinterpret_cast<T*>(sg.stale) + e0, sg.codes + e0, sg.scales + j,
+                              reinterpret_cast<const T*>(sg.stale) + e0,
+                              reinterpret_cast<T*>(sg.out) + e0, sg.codes + e0, sg.scales + j,
                               (int)min(128ll, sg.n - e0), sub, hmask);
     }
   }

@@ -8,12 +8,13 @@ constexpr int kMaxRefreshSegs = 48;
 
 struct RefreshSeg {
   const void* fresh;  // [n] elements of the storage type
-  void* stale;        // [n], refreshed in place
+  void* stale;        // [n] the stale values
   int8_t* codes;      // [n]
   float* scales;      // [ceil(n/128)]
   long long n;
-  int vec_ok;         // fresh/stale/codes 16-byte aligned: 128-bit path for full blocks
+  int vec_ok;         // fresh/stale/out/codes 16-byte aligned: 128-bit path for full blocks
   int pad_;
+  void* out;          // [n] where the refreshed values go (== stale: in place)
 };
 
 struct RefreshTable {

@@ -13,6 +13,17 @@ bool tc_linear_supported(long long M, int C);
 int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2, long long M,
                      int N, int K, int* status, long long wait_limit, cudaStream_t s);
 
+// The packed Q, K, V projection (N = 3 * ncols, ncols a multiple of 128, 128-wide tiles)
+// with the compressed-residual refresh of K and V in its epilogue: besides storing fresh
+// K and V (o1, o2), each K / V row block is quantised against k_stale / v_stale and the
+// refreshed values go to k_out / v_out (which must not alias the stale inputs: the
+// attention still reads them), the codes to codes (K then V, flat) and the block scales
+// to scales (the same order) -- the same message and values as the refresh kernel.
+int launch_tc_linear_refresh(const void* a, const void* w, void* o0, void* o1, void* o2,
+                             long long M, int N, int K, const void* k_stale, const void* v_stale,
+                             void* k_out, void* v_out, int8_t* codes, float* scales,
+                             int* status, long long wait_limit, cudaStream_t s);
+
 // Implicit-GEMM halo conv3x3 (see halo_conv3x3 in dpp.h).  With gn_par non-NULL, yf is
 // the raw GroupNorm input x and the kernel applies GroupNorm to its in-band rows on the
 // fly (gn_par: [B][P][3][Cin] fp32 mean, rstd * gamma, beta); ys is the stale y.

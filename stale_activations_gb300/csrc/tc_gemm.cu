@@ -21,6 +21,7 @@
 #include <mutex>
 
 #include "ptx.cuh"
+#include "quant.cuh"
 #include "tc.cuh"
 
 namespace dpp {
@@ -63,6 +64,13 @@ struct GemmArgs {
   // (mean, rstd * gamma, beta per channel of each batch and patch)
   const float* gn_par;
   int P;
+  // linear whose K and V outputs (1, 2) are also refreshed (RFX): against the stale
+  // values at rfx_stale[i] into rfx_out[i], codes and block scales at the message
+  // offsets of each
+  const void* rfx_stale[2];
+  void* rfx_out[2];
+  int8_t* rfx_codes[2];
+  float* rfx_scales[2];
 };
 
 // What the producer fetched into a stage, for the GroupNorm warps: the boxes' first
@@ -74,8 +82,97 @@ struct StageNote {
 // GNF (conv only): tmA maps the raw input x, tmA2 the stale GroupNorm output; warps
 // 6-9 turn each landed in-band box of x into y = (x - mean) * scale + beta in place
 // (the zero fill of out-of-image positions stays 0) before the MMA reads the stage.
-template <bool CONV, int BN, bool GNF>
-__global__ void __launch_bounds__(GNF ? GEMM_GN_THREADS : GEMM_THREADS, 1)
+// The epilogue of one 128-column K or V row with its refresh: the accumulator row is
+// rounded to bf16 and stored as fresh K/V (as in the plain epilogue), the residual
+// against the stale row is quantised (one 128-element block: shared quantiser) and the
+// refreshed row, the 128 codes and the block scale are written.  `flat` is the row's
+// offset in the flat [B*L*C] tensor, a multiple of 128.  The stale row is loaded at once
+// (one memory latency per row); the quantising pass walks the four 32-column chunks in
+// a loop that is not unrolled (the unrolled row did not fit the instruction cache),
+// re-reading each chunk from TMEM and picking its stale vectors by compares.
+__device__ __forceinline__ uint4 pick4(const uint4 (&v)[16], int ch, int i) {
+  const uint4 a = v[i], b = v[4 + i], c = v[8 + i], d = v[12 + i];
+  return ch == 0 ? a : ch == 1 ? b : ch == 2 ? c : d;
+}
+
+__device__ __forceinline__ void pack_row32(const uint32_t (&v)[32], uint4 (&f)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[i].x = pack_bf16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1]));
+    f[i].y = pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
+    f[i].z = pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
+    f[i].w = pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
+  }
+}
+
+__device__ __forceinline__ void refresh_row(uint32_t t_row, __nv_bfloat16* dst, bool live,
+                                            bool is_k, const GemmArgs& args, long long flat) {
+  const __nv_bfloat16* sp =
+      static_cast<const __nv_bfloat16*>(is_k ? args.rfx_stale[0] : args.rfx_stale[1]) + flat;
+  __nv_bfloat16* op = static_cast<__nv_bfloat16*>(is_k ? args.rfx_out[0] : args.rfx_out[1]) + flat;
+  int8_t* cp = (is_k ? args.rfx_codes[0] : args.rfx_codes[1]) + flat;
+  float* scp = (is_k ? args.rfx_scales[0] : args.rfx_scales[1]) + flat / 128;
+  uint4 sb[16];  // the stale row, 8 values per vector
+  if (live) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sb[i] = __ldcs(reinterpret_cast<const uint4*>(sp) + i);
+  }
+  // pass 1: fresh K/V out, and the block's absolute maximum of fresh - stale
+  float amax = 0.0f;
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t v[32];
+    ptx::tmem_ld32(t_row + ch * 32, v);
+    ptx::tmem_ld_wait();
+    uint4 f[4];
+    pack_row32(v, f);
+    if (live) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        reinterpret_cast<uint4*>(dst)[4 * ch + i] = f[i];
+        float fv[8], sv[8];
+        unpack16(f[i], fv);
+        unpack16(pick4(sb, ch, i), sv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(fv[e] - sv[e]));
+      }
+    }
+  }
+  if (!live) return;
+  const QuantBlock qb = quant_block(amax);
+  *scp = qb.s;
+  // pass 2: codes and refreshed values
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t v[32];
+    ptx::tmem_ld32(t_row + ch * 32, v);
+    ptx::tmem_ld_wait();
+    uint4 f[4];
+    pack_row32(v, f);
+    uint32_t cw[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float fv[8], sv[8], d[8], tm[8], nv[8];
+      unpack16(f[i], fv);
+      unpack16(pick4(sb, ch, i), sv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) d[e] = fv[e] - sv[e];
+      quant8(qb, d, sv, tm, nv);
+      const uint2 c = pack_codes(tm);
+      cw[2 * i] = c.x;
+      cw[2 * i + 1] = c.y;
+      __stcs(reinterpret_cast<uint4*>(op) + 4 * ch + i, pack16(nv));
+    }
+    __stcs(reinterpret_cast<uint4*>(cp) + 2 * ch, make_uint4(cw[0], cw[1], cw[2], cw[3]));
+    __stcs(reinterpret_cast<uint4*>(cp) + 2 * ch + 1, make_uint4(cw[4], cw[5], cw[6], cw[7]));
+  }
+}
+
+// RFX (linear, 128-wide tiles): a K or V tile row is exactly one 128-element refresh
+// block, so the epilogue thread that stores a row of fresh K or V also quantises its
+// residual against the stale row and writes the refreshed row, the codes and the scale.
+template <bool CONV, int BN, bool GNF, bool RFX = false>
+__global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
   using C = Cfg<BN>;
@@ -325,10 +422,14 @@ __global__ void __launch_bounds__(GNF ? GEMM_GN_THREADS : GEMM_THREADS, 1)
       }
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------ epilogue (warps 2..5; RFX: 2..9)
+    // With RFX two groups of four warps take alternate tiles (group g drains
+    // accumulator g), so a refreshing epilogue may take two main loops' time.
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int group = RFX ? (warp - 2) >> 2 : 0;
     int it = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+      if (RFX && (it & 1) != group) continue;
       const int ab = it % C::NACC;
       if (!ptx::mbar_wait(&acc_full[ab], (it / C::NACC) & 1, args.wait_limit, abort_flag)) {
         set_status(args.status, DPP_ERR_TIMEOUT);
@@ -346,8 +447,10 @@ __global__ void __launch_bounds__(GNF ? GEMM_GN_THREADS : GEMM_THREADS, 1)
       void* const obase = which == 0 ? args.out[0] : which == 1 ? args.out[1] : args.out[2];
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(obase) + row * args.ncols + col0;
       const uint32_t t_base = tmem + ab * BN + ((uint32_t)(quarter * 32) << 16);
+      const bool rfx_row = RFX && which > 0;
+      if (rfx_row) refresh_row(t_base, dst, row < args.M, which == 1, args, row * args.ncols + col0);
 #pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
+      for (int ch = 0; ch < (rfx_row ? 0 : BN / 32); ++ch) {
         uint32_t v[32];
         ptx::tmem_ld32(t_base + ch * 32, v);
         ptx::tmem_ld_wait();
@@ -410,12 +513,12 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
   return r == CUDA_SUCCESS;
 }
 
-template <bool CONV, int BN, bool GNF>
+template <bool CONV, int BN, bool GNF, bool RFX = false>
 int prepare() {
   static std::once_flag once;
   static int rc = DPP_OK;
   std::call_once(once, [] {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<CONV, BN, GNF>,
+    if (cudaFuncSetAttribute(tc_gemm_kernel<CONV, BN, GNF, RFX>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<BN>::SMEM) != cudaSuccess)
       rc = DPP_ERR_CUDA;
@@ -440,17 +543,17 @@ int pick_bn(int N, int ncols, int nkb) {
 
 constexpr int mma_n(int bn) { return bn > 256 ? bn / 2 : bn; }
 
-template <bool CONV, int BN, bool GNF>
+template <bool CONV, int BN, bool GNF, bool RFX = false>
 int launch(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, GemmArgs g,
            cudaStream_t s) {
-  int rc = prepare<CONV, BN, GNF>();
+  int rc = prepare<CONV, BN, GNF, RFX>();
   if (rc) return rc;
   g.n_tiles = g.N / BN;
   const long long ntiles = (long long)g.m_tiles * g.n_tiles;
   const int grid = (int)(ntiles < dpp_host::sm_count() ? ntiles : dpp_host::sm_count());
   const cudaError_t e =
-      dpp_host::launch_pdl(tc_gemm_kernel<CONV, BN, GNF>, dim3(grid),
-                           dim3(GNF ? GEMM_GN_THREADS : GEMM_THREADS), Cfg<BN>::SMEM, s, ta, ta2,
+      dpp_host::launch_pdl(tc_gemm_kernel<CONV, BN, GNF, RFX>, dim3(grid),
+                           dim3(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS), Cfg<BN>::SMEM, s, ta, ta2,
                            tb, g);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
@@ -501,6 +604,34 @@ int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2,
   g.status = status;
   g.wait_limit = wait_limit;
   return dispatch<false, false>(bn, ta, ta, tb, g, s);
+}
+
+int launch_tc_linear_refresh(const void* a, const void* w, void* o0, void* o1, void* o2,
+                             long long M, int N, int K, const void* k_stale, const void* v_stale,
+                             void* k_out, void* v_out, int8_t* codes, float* scales,
+                             int* status, long long wait_limit, cudaStream_t s) {
+  if (M % BM || N % 384 || K % BK || !o1 || !o2) return DPP_ERR_SHAPE;
+  const int ncols = N / 3;
+  if (ncols % 128) return DPP_ERR_SHAPE;
+  CUtensorMap ta, tb;
+  const uint64_t da[2] = {(uint64_t)K, (uint64_t)M}, sa[1] = {(uint64_t)K * 2};
+  const uint32_t ba[2] = {BK, BM};
+  const uint64_t db[2] = {(uint64_t)K, (uint64_t)N}, sb[1] = {(uint64_t)K * 2};
+  const uint32_t bb[2] = {BK, 128};
+  if (!make_map(&ta, a, 2, da, sa, ba) || !make_map(&tb, w, 2, db, sb, bb)) return DPP_ERR_CUDA;
+  GemmArgs g{};
+  g.M = M; g.N = N; g.K = K; g.nkb = K / BK;
+  g.m_tiles = (int)(M / BM);
+  g.out[0] = o0; g.out[1] = o1; g.out[2] = o2;
+  g.ncols = ncols;
+  g.status = status;
+  g.wait_limit = wait_limit;
+  const long long blc = M * ncols;  // elements of K (and of V): V's codes follow K's
+  g.rfx_stale[0] = k_stale; g.rfx_stale[1] = v_stale;
+  g.rfx_out[0] = k_out; g.rfx_out[1] = v_out;
+  g.rfx_codes[0] = codes; g.rfx_codes[1] = codes + blc;
+  g.rfx_scales[0] = scales; g.rfx_scales[1] = scales + blc / 128;
+  return launch<false, 128, false, true>(ta, ta, tb, g, s);
 }
 
 int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,

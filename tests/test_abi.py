@@ -82,6 +82,7 @@ def test_workspace_layout_sizes(lib):
 @pytest.mark.parametrize("kw", [dict(H=63), dict(P=3), dict(C=600, heads=10), dict(G=7),
                                 dict(heads=5), dict(dtype=7), dict(W=48), dict(gn_mode=3),
                                 dict(gn_mode=-1), dict(fuse_gn_raw=2),
+                                dict(dtype=dpp.F32, fuse_refresh=1),
                                 dict(B=1, H=32, W=32, C=64, P=2, G=8, heads=1, dtype=dpp.F32,
                                      fuse_gn=1)])
 def test_invalid_params_rejected(lib, kw):
@@ -135,6 +136,15 @@ def test_host_checks_without_launch(lib):
     st = dpp.LayerState()
     assert lib.patch_layer_step(ctypes.byref(prm), ctypes.byref(w), ctypes.byref(st), a, a, 0, a,
                                 None) == 1
+    # the second state set: all four or none (1), none equal to its counterpart (9), the
+    # same alignment rules (3) -- all refused before any launch
+    w = dpp.LayerWeights(*[vp(256 * (i + 1)) for i in range(5)])
+    cur = [vp(0x10000 * (i + 1)) for i in range(6)]
+    nxt = [vp(0x100000 * (i + 1)) for i in range(4)]
+    for bad, code in ((nxt[:3] + [None], 1), ([cur[0]] + nxt[1:], 9), (nxt[:1] + [vp(0x200008)] + nxt[2:], 3)):
+        st = dpp.LayerState(*cur, *bad)
+        assert lib.patch_layer_step(ctypes.byref(prm), ctypes.byref(w), ctypes.byref(st), a, a,
+                                    dpp.STALE, a, None) == code, bad
 
 
 def test_otil_host_checks(lib):

@@ -30,9 +30,9 @@ def _setup(cfg, seed=0, affine=True):
     return wts, wn, x, x_prev, sync_fwd, ostate
 
 
-def _gpu_state_from(ostate, cfg, prm, dev="cuda"):
+def _gpu_state_from(ostate, cfg, prm, dev="cuda", dbuf=False):
     dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
-    state, ws = dpp.alloc_layer(prm, device=dev)
+    state, ws = dpp.alloc_layer(prm, device=dev, double_buffer=dbuf)
     state["gn_stats"].copy_(torch.from_numpy(ostate["gn_stats"]).float())
     for k in ("y_stale", "k_stale", "v_stale"):
         src = torch.from_numpy(np.ascontiguousarray(ostate[k])).to(dt)
@@ -40,10 +40,11 @@ def _gpu_state_from(ostate, cfg, prm, dev="cuda"):
     return state, ws
 
 
-def _params(cfg, refresh=True, fuse_gn=False, gn_mode=dpp.GN_SPLICED):
+def _params(cfg, refresh=True, fuse_gn=False, gn_mode=dpp.GN_SPLICED, fuse_refresh=False):
     return dpp.make_params(cfg.B, cfg.H, cfg.W, cfg.C, cfg.P, cfg.G, cfg.heads,
                            dpp.BF16 if cfg.dtype == "bf16" else dpp.F32, refresh=refresh,
-                           eps=cfg.eps, fuse_gn=fuse_gn, gn_mode=gn_mode)
+                           eps=cfg.eps, fuse_gn=fuse_gn, gn_mode=gn_mode,
+                           fuse_refresh=fuse_refresh)
 
 
 CFGS = {
@@ -60,6 +61,31 @@ CFGS = {
 }
 
 
+NEXT = dict(zip(dpp.STATE_KEYS, dpp.NEXT_KEYS))
+
+
+def _halo_rows(cfg):
+    Hp = cfg.H // cfg.P
+    return np.array(sorted({r for p in range(1, cfg.P) for r in (p * Hp - 1, p * Hp)}),
+                    dtype=np.int64)
+
+
+def _check_new_state(state, new_state, cfg, dbuf, old=None):
+    """The step's new state against the oracle's: in place, or in the second set (whose
+    y holds only the halo rows: no other row of y is ever read) with the first set
+    unchanged."""
+    for k in ("k_stale", "v_stale", "y_stale"):
+        got = np64(state[NEXT[k] if dbuf else k]).reshape(new_state[k].shape)
+        want = new_state[k]
+        if dbuf and k == "y_stale":
+            rows = _halo_rows(cfg)
+            got, want = got[:, rows], want[:, rows]
+        np.testing.assert_array_equal(got, want, err_msg=k)
+    if dbuf and old is not None:
+        for k in dpp.STATE_KEYS:
+            assert torch.equal(state[k], old[k]), k
+
+
 def _y_rows(cfg, fuse):
     """Rows of the workspace's y the step writes: all of them, or with the fused GroupNorm
     only each band's first and last row (the conv normalises its own band's rows of x)."""
@@ -70,14 +96,23 @@ def _y_rows(cfg, fuse):
                     dtype=np.int64)
 
 
-@pytest.mark.parametrize("name,fuse", [(n, False) for n in CFGS] +
-                         [(n, True) for n in CFGS if CFGS[n].dtype == "bf16"])
-def test_layer_stale_step_stagewise_and_end_to_end(name, fuse):
+BF16_CFGS = [n for n in CFGS if CFGS[n].dtype == "bf16"]
+
+
+@pytest.mark.parametrize("name,fuse,dbuf,frx",
+                         [(n, False, False, False) for n in CFGS] +
+                         [(n, True, False, False) for n in BF16_CFGS] +
+                         [(n, False, True, False) for n in CFGS] +
+                         [(n, False, True, True) for n in BF16_CFGS] +
+                         [("small_bf16", True, True, True)])
+def test_layer_stale_step_stagewise_and_end_to_end(name, fuse, dbuf, frx):
+    """dbuf: the new state goes to the second set; frx: there the projection's epilogue
+    refreshes K and V (and a pass beside the conv the halo rows of y)."""
     cfg = CFGS[name]
     tol = TOL_BF16 if cfg.dtype == "bf16" else TOL_F32
     wts, wn, x, _, _, ostate = _setup(cfg)
-    prm = _params(cfg, fuse_gn=fuse)
-    state, ws = _gpu_state_from(ostate, cfg, prm)
+    prm = _params(cfg, fuse_gn=fuse, fuse_refresh=frx)
+    state, ws = _gpu_state_from(ostate, cfg, prm, dbuf=dbuf)
     old = {k: v.clone() for k, v in state.items()}
     wd = {k: v.cuda() for k, v in wts.items()}
     out = torch.empty(cfg.B, cfg.H, cfg.W, cfg.C, dtype=x.dtype, device="cuda")
@@ -128,24 +163,27 @@ def test_layer_stale_step_stagewise_and_end_to_end(name, fuse):
     new_state, codes, scales = oracle.layer_state_update(fwd_gpu, ost, P, dt, oracle.STALE, True)
     np.testing.assert_array_equal(state["codes"].cpu().numpy(), codes)
     np.testing.assert_array_equal(state["scales"].cpu().numpy(), scales)
-    for k in ("k_stale", "v_stale", "y_stale"):
-        np.testing.assert_array_equal(np64(state[k]).reshape(new_state[k].shape), new_state[k])
-    np.testing.assert_array_equal(np64(state["gn_stats"]), np64(torch.from_numpy(
-        v["gn_fresh"]).float()))
+    _check_new_state(state, new_state, cfg, dbuf, old)
+    np.testing.assert_array_equal(np64(state["gn_next" if dbuf else "gn_stats"]),
+                                  np64(torch.from_numpy(v["gn_fresh"]).float()))
     # end to end against the oracle run from x alone
     fwd = oracle.layer_forward(np64(x), ostate, wn, P, G, cfg.heads, cfg.eps, dt, oracle.STALE)
     e2e = rel_err(np64(out), fwd["out"])
     assert e2e < (TOL_CHAIN_BF16 if dt == "bf16" else TOL_F32), e2e
 
 
-@pytest.mark.parametrize("name,fuse", [("tiny_f32", False), ("small_bf16", False),
-                                      ("small_bf16", True)])
-def test_layer_sync_step_and_state(name, fuse):
+@pytest.mark.parametrize("name,fuse,dbuf", [("tiny_f32", False, False),
+                                           ("small_bf16", False, False),
+                                           ("small_bf16", True, False),
+                                           ("tiny_f32", False, True),
+                                           ("small_bf16", False, True)])
+def test_layer_sync_step_and_state(name, fuse, dbuf):
     cfg = CFGS[name]
     wts, wn, _, x_prev, sync_fwd, ostate = _setup(cfg)
     prm = _params(cfg, fuse_gn=fuse)
-    state, ws = dpp.alloc_layer(prm)
+    state, ws = dpp.alloc_layer(prm, double_buffer=dbuf)
     state["k_stale"].fill_(7.0)
+    old = {k: state[k].clone() for k in dpp.STATE_KEYS}
     wd = {k: t.cuda() for k, t in wts.items()}
     out = torch.empty(cfg.B, cfg.H, cfg.W, cfg.C, dtype=x_prev.dtype, device="cuda")
     dpp.patch_layer_step(prm, wd, state, x_prev.cuda(), out, dpp.SYNC, ws)
@@ -153,14 +191,18 @@ def test_layer_sync_step_and_state(name, fuse):
     e2e = rel_err(np64(out), sync_fwd["out"])
     assert e2e < (TOL_CHAIN_BF16 if cfg.dtype == "bf16" else TOL_F32)
     v = {k: np64(t) for k, t in dpp.workspace_views(prm, ws).items()}
-    # the state is the exact copy of this step's fresh tensors
-    np.testing.assert_array_equal(np64(state["k_stale"]), v["k"])
-    np.testing.assert_array_equal(np64(state["v_stale"]), v["v"])
-    np.testing.assert_array_equal(np64(state["gn_stats"]), v["gn_fresh"])
+    # the (new) state is the exact copy of this step's fresh tensors
+    nk = (lambda k: NEXT[k]) if dbuf else (lambda k: k)
+    np.testing.assert_array_equal(np64(state[nk("k_stale")]), v["k"])
+    np.testing.assert_array_equal(np64(state[nk("v_stale")]), v["v"])
+    np.testing.assert_array_equal(np64(state[nk("gn_stats")]), v["gn_fresh"])
     Hp = cfg.H // cfg.P
     for p in range(1, cfg.P):
         rows = [p * Hp - 1, p * Hp]
-        np.testing.assert_array_equal(np64(state["y_stale"])[:, rows], v["y"][:, rows])
+        np.testing.assert_array_equal(np64(state[nk("y_stale")])[:, rows], v["y"][:, rows])
+    if dbuf:  # the current set is left as it was
+        for k in dpp.STATE_KEYS:
+            assert torch.equal(state[k], old[k]), k
 
 
 @pytest.mark.parametrize("fuse", [False, True])
@@ -183,11 +225,12 @@ def test_layer_sync_equals_unpartitioned_on_gpu(fuse):
     assert rel_err(outs[1], outs[0]) < 1e-2
 
 
-def test_layer_no_sync_leaves_state():
+@pytest.mark.parametrize("dbuf", [False, True])
+def test_layer_no_sync_leaves_state(dbuf):
     cfg = CFGS["small_bf16"]
     wts, wn, x, _, _, ostate = _setup(cfg)
     prm = _params(cfg, refresh=False)
-    state, ws = _gpu_state_from(ostate, cfg, prm)
+    state, ws = _gpu_state_from(ostate, cfg, prm, dbuf=dbuf)
     before = {k: v.clone() for k, v in state.items()}
     out = torch.empty(cfg.B, cfg.H, cfg.W, cfg.C, dtype=torch.bfloat16, device="cuda")
     dpp.patch_layer_step(prm, {k: t.cuda() for k, t in wts.items()}, state, x.cuda(), out,
@@ -226,9 +269,13 @@ def test_layer_gn_modes(name, fuse, gn_mode):
     assert rel_err(np64(out), fwd["out"]) < (TOL_CHAIN_BF16 if cfg.dtype == "bf16" else TOL_F32)
 
 
-@pytest.mark.parametrize("name,fuse", [("tiny_f32", False), ("small_bf16", False),
-                                      ("small_bf16", True)])
-def test_layer_periodic_refresh_sequence(name, fuse):
+@pytest.mark.parametrize("name,fuse,dbuf,frx", [("tiny_f32", False, False, False),
+                                               ("small_bf16", False, False, False),
+                                               ("small_bf16", True, False, False),
+                                               ("tiny_f32", False, True, False),
+                                               ("small_bf16", False, True, False),
+                                               ("small_bf16", False, True, True)])
+def test_layer_periodic_refresh_sequence(name, fuse, dbuf, frx):
     """Periodic layer-context refresh ("OTIL for SDXL on 4x L40S"): a synchronous step
     every third step, stale steps with the compressed refresh in between.  At every
     step the output matches the oracle run on the same state, and the new state is
@@ -236,12 +283,13 @@ def test_layer_periodic_refresh_sequence(name, fuse):
     differs by one rounding may legitimately change a code)."""
     cfg = CFGS[name]
     wts, wn, _, _, _, _ = _setup(cfg)
-    prm = _params(cfg, fuse_gn=fuse)
-    state, ws = dpp.alloc_layer(prm)
+    prm = _params(cfg, fuse_gn=fuse, fuse_refresh=frx)
+    state, ws = dpp.alloc_layer(prm, double_buffer=dbuf)
     wd = {k: t.cuda() for k, t in wts.items()}
     dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     tol = TOL_CHAIN_BF16 if cfg.dtype == "bf16" else TOL_F32
     names = ("gn_stats", "y_stale", "k_stale", "v_stale")
+    rows = _halo_rows(cfg) if dbuf else np.arange(cfg.H)
     for i, mode in enumerate([dpp.SYNC, dpp.STALE, dpp.STALE, dpp.SYNC, dpp.STALE]):
         x, _ = synth.layer_inputs(cfg, seed=10 + i)
         ost = {k: np64(state[k]).reshape(oracle.empty_state(cfg.B, cfg.H, cfg.W, cfg.C, cfg.P,
@@ -257,32 +305,43 @@ def test_layer_periodic_refresh_sequence(name, fuse):
         gpu_fwd = dict(gn_fresh=v["gn_fresh"], y=v["y"], k=v["k"], v=v["v"])
         new, _, _ = oracle.layer_state_update(gpu_fwd, ost, cfg.P, cfg.dtype, omode, True)
         for k in names:
-            np.testing.assert_array_equal(np64(state[k]).reshape(new[k].shape),
-                                          np64(torch.from_numpy(new[k]).to(torch.float32))
-                                          if k == "gn_stats" else new[k], err_msg=f"{i} {k}")
+            got = np64(state[NEXT[k] if dbuf else k]).reshape(new[k].shape)
+            want = np64(torch.from_numpy(new[k]).to(torch.float32)) if k == "gn_stats" else new[k]
+            if k == "y_stale":  # the second set's y holds only the halo rows
+                got, want = got[:, rows], want[:, rows]
+            np.testing.assert_array_equal(got, want, err_msg=f"{i} {k}")
+        if dbuf:
+            dpp.swap_state(state)
 
 
-@pytest.mark.parametrize("name", ["tiny_f32", "small_bf16"])
-def test_layer_message_keeps_rank_copies_identical(name):
+@pytest.mark.parametrize("name,dbuf,frx", [("tiny_f32", False, False),
+                                           ("small_bf16", False, False),
+                                           ("tiny_f32", True, False), ("small_bf16", True, False),
+                                           ("small_bf16", True, True)])
+def test_layer_message_keeps_rank_copies_identical(name, dbuf, frx):
     """The exchange of the multi-GPU method on one device: besides the sender's state,
     P-1 other ranks each hold their own copy of it and receive only the messages
     (codes, scales and the GroupNorm sums) of each stale step.  After a synchronous
     step and three stale steps every copy equals the sender's state bit for bit."""
     cfg = CFGS[name]
     wts, _, _, _, _, _ = _setup(cfg)
-    prm = _params(cfg)
-    state, ws = dpp.alloc_layer(prm)
+    prm = _params(cfg, fuse_refresh=frx)
+    state, ws = dpp.alloc_layer(prm, double_buffer=dbuf)
     wd = {k: t.cuda() for k, t in wts.items()}
     dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     out = torch.empty(cfg.B, cfg.H, cfg.W, cfg.C, dtype=dt, device="cuda")
     x, _ = synth.layer_inputs(cfg, seed=20)
     dpp.patch_layer_step(prm, wd, state, x.cuda(), out, dpp.SYNC, ws)
+    if dbuf:
+        dpp.swap_state(state)
     copies = [{k: state[k].clone() for k in ("gn_stats", "y_stale", "k_stale", "v_stale")}
               for _ in range(cfg.P - 1)]
     for i in range(3):
         x, _ = synth.layer_inputs(cfg, seed=21 + i)
         dpp.patch_layer_step(prm, wd, state, x.cuda(), out, dpp.STALE, ws)
         assert dpp.read_device_status(ws) == 0
+        if dbuf:
+            dpp.swap_state(state)
         for c in copies:
             dpp.apply_layer_message(prm, state["codes"], state["scales"], state["gn_stats"], c)
         torch.cuda.synchronize()
