@@ -417,7 +417,7 @@ def run_gpu(args):
                              "layer_2x256x256x640_p8": measure_large_layer(dev, peaks),
                              "halo_conv_vae": measure_vae_conv(dev, peaks),
                              "otil_exchange_2x4x128x128_p4": measure_otil(dev),
-                             "layer_fused_gn": measure_fused_gn(dev)}
+                             "layer_fusions": measure_fusions(dev)}
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
     if ws_n > 1:
@@ -583,16 +583,34 @@ def measure_otil(dev, iters=20):
             "note": "back-to-back exchange steps (launch-bound at this size)"}
 
 
-def measure_fused_gn(dev, iters=20):
-    """The headline layer step with the GroupNorm apply fused into the conv's operand
-    path (fuse_gn = 1) against the separate apply, same workload and L2 flush."""
+def measure_fusions(dev, iters=20):
+    """The headline layer step in its four arrangements, same workload and L2 flush:
+    the default; the GroupNorm apply fused into the conv's operand path (fuse_gn); the
+    new state written to a second set (swapped after each step) by the separate refresh
+    pass; and that with the K/V refresh in the projection epilogue (fuse_refresh)."""
     import torch
 
     import stale_activations_gb300 as dpp
     res = {}
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    for fuse in (False, True):
-        cfg, prm, wd, state, ws, _, xd, out = _layer_setup(dev, fuse_gn=fuse)
+    for name, fuse_gn, dbuf, frx in (("separate", False, False, False),
+                                     ("fuse_gn", True, False, False),
+                                     ("second_state", False, True, False),
+                                     ("second_state_fuse_refresh", False, True, True)):
+        cfg, prm, wd, state, ws, _, xd, out = _layer_setup(dev, fuse_gn=fuse_gn)
+        prm.fuse_refresh = 1 if frx else 0
+        if dbuf:
+            st2, _ = dpp.alloc_layer(prm, device=dev, double_buffer=True)
+            for k in dpp.STATE_KEYS:
+                st2[k].copy_(state[k])
+            st2["codes"], st2["scales"] = state["codes"], state["scales"]
+            state = st2
+
+        def step(evs=None):
+            dpp.patch_layer_step(prm, wd, state, xd, out, dpp.STALE, ws, stage_events=evs)
+            if dbuf:
+                dpp.swap_state(state)
+
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(dpp.NUM_STAGE_EVENTS)]
                for _ in range(iters)]
         pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -602,19 +620,19 @@ def measure_fused_gn(dev, iters=20):
                 e.record()
         for _ in range(3):
             flush.fill_(1)
-            dpp.patch_layer_step(prm, wd, state, xd, out, dpp.STALE, ws)
+            step()
         for i in range(iters):
             flush.fill_(1)
             pairs[i][0].record()
-            dpp.patch_layer_step(prm, wd, state, xd, out, dpp.STALE, ws)
+            step()
             pairs[i][1].record()
         for i in range(iters):
             flush.fill_(1)
-            dpp.patch_layer_step(prm, wd, state, xd, out, dpp.STALE, ws, stage_events=evs[i])
+            step(evs[i])
         torch.cuda.synchronize()
         if dpp.read_device_status(ws) != 0:
-            raise RuntimeError("device status set in the fused-GroupNorm comparison")
-        res["fused" if fuse else "separate"] = {
+            raise RuntimeError(f"device status set in the {name} arrangement")
+        res[name] = {
             "ms_per_step": statistics.median(a.elapsed_time(b) for a, b in pairs),
             "stage_ms": {n: statistics.median(evs[i][k].elapsed_time(evs[i][k + 1])
                                               for i in range(iters))
