@@ -111,7 +111,7 @@ int apply_residual(const int8_t* codes, const float* scales, void* stale, int64_
  * y_fresh, y_stale: [B,H,W,Cin]; w: [Cout,3,3,Cin]; out: [B,H,W,Cout]; all `dtype`.
  * With y_stale == y_fresh the result is the unbanded convolution.
  * Requires H % P == 0.  DPP_BF16 also requires Cin % 64 == 0, Cout a multiple of
- * 128 or of 160, W % 128 == 0 or 128 % W == 0, and (H/P)*W % 128 == 0.
+ * 128 or of 160, W % 8 == 0 and H*W % 128 == 0.
  * dev_status: device int (may be NULL) that receives a give-up code.
  */
 int halo_conv3x3(const void* y_fresh, const void* y_stale, const void* w, void* out,
@@ -190,7 +190,8 @@ typedef struct dpp_layer_params {
   int refresh;     /* DPP_STALE only: 1 = refresh the state, 0 = leave it (no_sync) */
   float eps;       /* GroupNorm epsilon */
   int gn_mode;     /* DPP_GN_SPLICED (0), DPP_GN_SYNC or DPP_GN_PREVIOUS */
-  int fuse_gn;     /* DPP_BF16 only (0 for DPP_F32): 1 = the conv applies GroupNorm to its
+  int fuse_gn;     /* DPP_BF16 only (0 for DPP_F32), and W % 128 == 0 or 128 % W == 0,
+                      (H/P)*W % 128 == 0: 1 = the conv applies GroupNorm to its
                       own band's rows of x as its input tiles land in shared memory, and
                       the workspace's y holds only each band's first and last row (the
                       rows the neighbours read as halos); 0 = a separate apply pass

@@ -85,6 +85,7 @@ int check_layer(const dpp_layer_params* p) {
   if (p->refresh != 0 && p->refresh != 1) return DPP_ERR_ARG;
   if (p->gn_mode < DPP_GN_SPLICED || p->gn_mode > DPP_GN_PREVIOUS) return DPP_ERR_ARG;
   if (p->fuse_gn != 0 && !(p->fuse_gn == 1 && p->dtype == DPP_BF16)) return DPP_ERR_ARG;
+  if (p->fuse_gn && !dpp::tc_conv_gn_supported(p->H, p->W, p->P)) return DPP_ERR_SHAPE;
   if (p->fuse_refresh != 0 &&
       !(p->fuse_refresh == 1 && p->dtype == DPP_BF16 && p->C % 128 == 0))
     return DPP_ERR_ARG;

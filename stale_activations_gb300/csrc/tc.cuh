@@ -19,6 +19,10 @@ int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2,
 // refreshed values go to k_out / v_out (which must not alias the stale inputs: the
 // attention still reads them), the codes to codes (K then V, flat) and the block scales
 // to scales (the same order) -- the same message and values as the refresh kernel.
+// The shapes the GroupNorm-fused conv (gn_par) takes: W % 128 == 0 or 128 % W == 0,
+// and (H/P)*W % 128 == 0.
+bool tc_conv_gn_supported(int H, int W, int P);
+
 int launch_tc_linear_refresh(const void* a, const void* w, void* o0, void* o1, void* o2,
                              long long M, int N, int K, const void* k_stale, const void* v_stale,
                              void* k_out, void* v_out, int8_t* codes, float* scales,

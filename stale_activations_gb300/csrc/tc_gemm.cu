@@ -274,12 +274,19 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
             const int tap = kb / args.cin_blocks;
             const int cb = kb - tap * args.cin_blocks;
             const int di = tap / 3 - 1, dj = tap % 3 - 1;
+            // box bx holds pixels [m0 + bx * box_px, +box_px) of the image: one row
+            // segment (box_px divides W), starting at row rk, column ck
+            int rk = r, ck = c0;
             for (int bx = 0; bx < args.boxes; ++bx) {
-              const int rk = r + bx;   // image row of this box's pixels
               const int rr = rk + di;  // source row
               const bool stale = rr >= 0 && rr < args.H && (rr / args.Hp) != (rk / args.Hp);
               ptx::tma_load_4d(a_dst + bx * args.box_px * 128, stale ? &tmA2 : &tmA, &full[s],
-                               cb * BK, c0 + dj, rr, b);
+                               cb * BK, ck + dj, rr, b);
+              ck += args.box_px;
+              if (ck == args.W) {
+                ck = 0;
+                ++rk;
+              }
             }
           } else {
             ptx::tma_load_2d(a_dst, &tmA, &full[s], kb * BK, (int)m0);
@@ -576,12 +583,19 @@ bool tc_linear_supported(long long M, int C) {
   return M % BM == 0 && C % 128 == 0 && C % BK == 0 && M < (1ll << 31);
 }
 
+// Tiles of 128 pixels never straddle two images; each is fetched per tap as 128 / box_px
+// row segments of box_px = gcd(W, 128) pixels (at least 8: W a multiple of 8).
 bool tc_conv_supported(int B, int H, int W, int Cin, int Cout, int P) {
   if (Cin % BK || Cin <= 0 || Cout <= 0 || !pick_bn(Cout, Cout, 9 * Cin / BK)) return false;
-  if (!(W % 128 == 0 || (128 % W == 0 && W >= 8))) return false;
-  if (((long long)(H / P) * W) % BM) return false;
+  if (W % 8 || ((long long)H * W) % BM) return false;
   (void)B;
+  (void)P;
   return true;
+}
+
+// The GroupNorm-fused variant assumes one band and one starting column per tile.
+bool tc_conv_gn_supported(int H, int W, int P) {
+  return (W % 128 == 0 || 128 % W == 0) && ((long long)(H / P) * W) % BM == 0;
 }
 
 int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2, long long M,
@@ -640,7 +654,9 @@ int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int
   if (!tc_conv_supported(B, H, W, Cin, Cout, P)) return DPP_ERR_SHAPE;
   const int bn = pick_bn(Cout, Cout, 9 * Cin / BK);
   if (!bn) return DPP_ERR_SHAPE;
-  const int box_px = W < 128 ? W : 128;
+  int box_px = 128;  // gcd(W, 128)
+  while (W % box_px) box_px >>= 1;
+  if (gn_par && !tc_conv_gn_supported(H, W, P)) return DPP_ERR_SHAPE;
   CUtensorMap tf, ts, tw;
   const uint64_t dy[4] = {(uint64_t)Cin, (uint64_t)W, (uint64_t)H, (uint64_t)B};
   const uint64_t sy[3] = {(uint64_t)Cin * 2, (uint64_t)W * Cin * 2, (uint64_t)H * W * Cin * 2};

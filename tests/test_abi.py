@@ -80,7 +80,8 @@ def test_workspace_layout_sizes(lib):
 
 
 @pytest.mark.parametrize("kw", [dict(H=63), dict(P=3), dict(C=600, heads=10), dict(G=7),
-                                dict(heads=5), dict(dtype=7), dict(W=48), dict(gn_mode=3),
+                                dict(heads=5), dict(dtype=7), dict(W=44), dict(W=48, fuse_gn=1),
+                                dict(gn_mode=3),
                                 dict(gn_mode=-1), dict(fuse_gn_raw=2),
                                 dict(dtype=dpp.F32, fuse_refresh=1),
                                 dict(B=1, H=32, W=32, C=64, P=2, G=8, heads=1, dtype=dpp.F32,

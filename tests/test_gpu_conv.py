@@ -30,6 +30,11 @@ def _conv_gpu(yf, ys, w, P):
     ("bf16", 1, 16, 128, 192, 128, 8),    # one row per tile, 1-row bands (both halos stale)
     ("bf16", 1, 16, 64, 256, 320, 2),     # 36 K slices: 128 x 320 tiles (two MMAs per step)
     ("bf16", 1, 160, 128, 256, 320, 4),   # 160 such tiles: some CTAs reuse one accumulator
+    # W neither a divisor nor a multiple of 128: tiles of 128 / gcd(W, 128) row segments
+    # that wrap across rows, bands whose pixel count is not a multiple of 128
+    ("bf16", 2, 16, 240, 64, 128, 4),     # 16-pixel segments (the SDXL-3840 latent width)
+    ("bf16", 1, 12, 96, 128, 128, 3),     # 32-pixel segments, 4-row bands
+    ("bf16", 1, 16, 40, 64, 160, 8),      # 8-pixel segments, 2-row bands
     ("f32", 1, 32, 32, 64, 64, 2),
     ("f32", 1, 6, 5, 3, 7, 3),            # ragged sizes on the SIMT path
 ])
@@ -40,7 +45,7 @@ def test_conv_matches_oracle(dtype, B, H, W, Cin, Cout, P):
     assert rel_err(np64(out), ref) < (TOL_BF16 if dtype == "bf16" else TOL_F32)
 
 
-@pytest.mark.parametrize("W", [32, 64, 256])
+@pytest.mark.parametrize("W", [32, 64, 256, 240, 40])
 def test_conv_sentinel_halo_rows_bitexact(W):
     """fresh = +1, stale = -1 and one-hot weights (output channel o reads tap o % 9
     of input channel o % Cin): every output is -1, 0 or +1 by the band rule alone."""
