@@ -415,6 +415,8 @@ def run_gpu(args):
         line["secondary"] = {"attention_sdxl3840": measure_attention_3840(dev, peaks),
                              "refresh_sweep": measure_refresh_sweep(dev, peaks),
                              "layer_2x256x256x640_p8": measure_large_layer(dev, peaks),
+                             "layer_sdxl3840_2x240x240x640_p8": measure_large_layer(
+                                 dev, peaks, H=240, W=240),
                              "halo_conv_vae": measure_vae_conv(dev, peaks),
                              "otil_exchange_2x4x128x128_p4": measure_otil(dev),
                              "layer_fusions": measure_fusions(dev)}
@@ -641,13 +643,14 @@ def measure_fusions(dev, iters=20):
     return res
 
 
-def measure_large_layer(dev, peaks, iters=3):
-    """One STALE layer step on a map larger than L2 (B=2, 256x256, C=640, P=8, 10 heads):
-    the GroupNorm and refresh stages as HBM streams, with per-stage CUDA events."""
+def measure_large_layer(dev, peaks, iters=3, H=256, W=256):
+    """One STALE layer step on a map larger than L2 (B=2, HxW = 256x256 or the SDXL-3840
+    latent 240x240, C=640, P=8, 10 heads): the GroupNorm and refresh stages as HBM
+    streams, with per-stage CUDA events."""
     import torch
 
     import stale_activations_gb300 as dpp
-    B, H, W, C, P, G, heads = 2, 256, 256, 640, 8, 32, 10
+    B, C, P, G, heads = 2, 640, 8, 32, 10
     prm = dpp.make_params(B, H, W, C, P, G, heads, dpp.BF16, refresh=True)
     state, ws = dpp.alloc_layer(prm, device=dev)
     g = torch.Generator(device=dev).manual_seed(3)
