@@ -171,7 +171,7 @@ __device__ __forceinline__ void refresh_row(uint32_t t_row, __nv_bfloat16* dst, 
 // RFX (linear, 128-wide tiles): a K or V tile row is exactly one 128-element refresh
 // block, so the epilogue thread that stores a row of fresh K or V also quantises its
 // residual against the stale row and writes the refreshed row, the codes and the scale.
-template <bool CONV, int BN, bool GNF, bool RFX = false>
+template <bool CONV, int BN, bool GNF, bool RFX = false, bool WRAP = false>
 __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
@@ -275,17 +275,29 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
             const int cb = kb - tap * args.cin_blocks;
             const int di = tap / 3 - 1, dj = tap % 3 - 1;
             // box bx holds pixels [m0 + bx * box_px, +box_px) of the image: one row
-            // segment (box_px divides W), starting at row rk, column ck
-            int rk = r, ck = c0;
-            for (int bx = 0; bx < args.boxes; ++bx) {
-              const int rr = rk + di;  // source row
-              const bool stale = rr >= 0 && rr < args.H && (rr / args.Hp) != (rk / args.Hp);
-              ptx::tma_load_4d(a_dst + bx * args.box_px * 128, stale ? &tmA2 : &tmA, &full[s],
-                               cb * BK, ck + dj, rr, b);
-              ck += args.box_px;
-              if (ck == args.W) {
-                ck = 0;
-                ++rk;
+            // segment (box_px divides W).  Whole rows (box_px == W) or one box per tile
+            // (W a multiple of 128): box bx is row r + bx from column c0; with WRAP the
+            // segments wrap across rows.
+            if (!WRAP) {
+              for (int bx = 0; bx < args.boxes; ++bx) {
+                const int rk = r + bx;   // image row of this box's pixels
+                const int rr = rk + di;  // source row
+                const bool stale = rr >= 0 && rr < args.H && (rr / args.Hp) != (rk / args.Hp);
+                ptx::tma_load_4d(a_dst + bx * args.box_px * 128, stale ? &tmA2 : &tmA,
+                                 &full[s], cb * BK, c0 + dj, rr, b);
+              }
+            } else {
+              int rk = r, ck = c0;
+              for (int bx = 0; bx < args.boxes; ++bx) {
+                const int rr = rk + di;
+                const bool stale = rr >= 0 && rr < args.H && (rr / args.Hp) != (rk / args.Hp);
+                ptx::tma_load_4d(a_dst + bx * args.box_px * 128, stale ? &tmA2 : &tmA,
+                                 &full[s], cb * BK, ck + dj, rr, b);
+                ck += args.box_px;
+                if (ck == args.W) {
+                  ck = 0;
+                  ++rk;
+                }
               }
             }
           } else {
@@ -520,12 +532,12 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
   return r == CUDA_SUCCESS;
 }
 
-template <bool CONV, int BN, bool GNF, bool RFX = false>
+template <bool CONV, int BN, bool GNF, bool RFX = false, bool WRAP = false>
 int prepare() {
   static std::once_flag once;
   static int rc = DPP_OK;
   std::call_once(once, [] {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<CONV, BN, GNF, RFX>,
+    if (cudaFuncSetAttribute(tc_gemm_kernel<CONV, BN, GNF, RFX, WRAP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<BN>::SMEM) != cudaSuccess)
       rc = DPP_ERR_CUDA;
@@ -550,29 +562,29 @@ int pick_bn(int N, int ncols, int nkb) {
 
 constexpr int mma_n(int bn) { return bn > 256 ? bn / 2 : bn; }
 
-template <bool CONV, int BN, bool GNF, bool RFX = false>
+template <bool CONV, int BN, bool GNF, bool RFX = false, bool WRAP = false>
 int launch(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, GemmArgs g,
            cudaStream_t s) {
-  int rc = prepare<CONV, BN, GNF, RFX>();
+  int rc = prepare<CONV, BN, GNF, RFX, WRAP>();
   if (rc) return rc;
   g.n_tiles = g.N / BN;
   const long long ntiles = (long long)g.m_tiles * g.n_tiles;
   const int grid = (int)(ntiles < dpp_host::sm_count() ? ntiles : dpp_host::sm_count());
   const cudaError_t e =
-      dpp_host::launch_pdl(tc_gemm_kernel<CONV, BN, GNF, RFX>, dim3(grid),
+      dpp_host::launch_pdl(tc_gemm_kernel<CONV, BN, GNF, RFX, WRAP>, dim3(grid),
                            dim3(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS), Cfg<BN>::SMEM, s, ta, ta2,
                            tb, g);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
 
-template <bool CONV, bool GNF>
+template <bool CONV, bool GNF, bool WRAP = false>
 int dispatch(int bn, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
              const GemmArgs& g, cudaStream_t s) {
   switch (bn) {
-    case 320: return launch<CONV, 320, GNF>(ta, ta2, tb, g, s);
-    case 256: return launch<CONV, 256, GNF>(ta, ta2, tb, g, s);
-    case 160: return launch<CONV, 160, GNF>(ta, ta2, tb, g, s);
-    case 128: return launch<CONV, 128, GNF>(ta, ta2, tb, g, s);
+    case 320: return launch<CONV, 320, GNF, false, WRAP>(ta, ta2, tb, g, s);
+    case 256: return launch<CONV, 256, GNF, false, WRAP>(ta, ta2, tb, g, s);
+    case 160: return launch<CONV, 160, GNF, false, WRAP>(ta, ta2, tb, g, s);
+    case 128: return launch<CONV, 128, GNF, false, WRAP>(ta, ta2, tb, g, s);
     default: return DPP_ERR_SHAPE;
   }
 }
@@ -678,8 +690,11 @@ int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int
   g.box_px = box_px;
   g.gn_par = gn_par;
   g.P = P;
-  return gn_par ? dispatch<true, true>(bn, tf, ts, tw, g, s)
-                : dispatch<true, false>(bn, tf, ts, tw, g, s);
+  if (gn_par) return dispatch<true, true>(bn, tf, ts, tw, g, s);
+  // segments that wrap across rows get their own kernel, so that the common shapes keep
+  // the simpler producer (the branch alone cost the SDXL-1024 conv 7%)
+  return box_px == W || box_px == 128 ? dispatch<true, false>(bn, tf, ts, tw, g, s)
+                                      : dispatch<true, false, true>(bn, tf, ts, tw, g, s);
 }
 
 }  // namespace dpp
