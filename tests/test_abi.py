@@ -40,6 +40,27 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(dpp.EXPORTS) <= set(names)
 
 
+def test_plain_c_consumer_compiles_links_and_agrees_on_layouts(lib, tmp_path):
+    """tests/abi_check.c, plain C99 against include/dpp.h, linked with libdpp.so: host
+    checks from C, and the struct sizes C sees equal the binding's."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = tmp_path / "abi_check"
+    libdir = os.path.dirname(dbuild.LIB)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "abi_check.c"), "-o", str(exe), "-L", libdir,
+                    "-ldpp", f"-Wl,-rpath,{libdir}"], check=True)
+    env = dict(os.environ)
+    env["LD_LIBRARY_PATH"] = libdir + os.pathsep + env.get("LD_LIBRARY_PATH", "")
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True, env=env).stdout
+    sizes = [int(v) for v in out.split("sizes")[1].split()]
+    assert sizes == [ctypes.sizeof(dpp.LayerParams), ctypes.sizeof(dpp.LayerWeights),
+                     ctypes.sizeof(dpp.LayerState), ctypes.sizeof(dpp.WorkspaceLayout)]
+
+
 def test_status_strings(lib):
     assert dpp.status_string(0) == "ok"
     assert "timeout" in dpp.status_string(6)
