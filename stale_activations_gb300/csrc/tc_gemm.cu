@@ -12,10 +12,16 @@
 // Halo conv staging ("Benchmarking DistVAE", Glossary: the halo rows a sharded
 // convolution needs; "OTIL for SDXL on 4x L40S", item 3: the conv halo buffers
 // are stale): for tap (di, dj) the A slice of an M tile is the tile's pixels
-// shifted by (di, dj), fetched per image row with a 4-D tensor map over the
-// NHWC map.  A row inside the tile's band comes from the fresh map, a row of
-// the neighbouring band (the halo) from the stale map, and the TMA zero fill
-// of out-of-range rows/columns is the convolution's zero padding.
+// shifted by (di, dj), fetched as row segments of gcd(W, 128) pixels with a 4-D
+// tensor map over the NHWC map.  A segment whose source row is inside its own
+// row's band comes from the fresh map, one whose source row is the neighbouring
+// band's (the halo) from the stale map, and the TMA zero fill of out-of-range
+// rows/columns is the convolution's zero padding.
+//
+// Two opt-in variants: GNF (the conv's A is raw x; warps 6-9 apply GroupNorm to the
+// landed in-band segments before the MMA reads a stage) and RFX (the Q/K/V projection
+// whose epilogue, warps 2-9 in two groups taking alternate tiles, also quantises the
+// K/V residual against the stale rows and writes the refreshed rows and the message).
 #include <cudaTypedefs.h>
 
 #include <mutex>
