@@ -54,8 +54,8 @@ extern "C" {
 #define DPP_ERR_CUDA 5        /* a CUDA runtime/driver call failed */
 #define DPP_ERR_TIMEOUT 6     /* device status: a bounded wait gave up */
 #define DPP_ERR_BOUNDS 7      /* reserved for a device index check; no kernel of this
-                                 build sets it (every launch's indices are checked on
-                                 the host against the buffer sizes it is given) */
+                                 build sets it (the host checks the shapes that each
+                                 launch's index arithmetic relies on) */
 #define DPP_ERR_UNSUPPORTED 8 /* the combination is not implemented */
 #define DPP_ERR_ARG 9         /* an enum/flag argument is invalid */
 #define DPP_ERR_SCRATCH_LIMIT 10 /* the layer needs more workspace than the fixed
