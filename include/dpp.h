@@ -276,6 +276,9 @@ int64_t dpp_message_blocks(const dpp_layer_params* prm);
  *     DPP_STALE, refresh = 1: refresh_residual of K, V and the halo rows of y
  *       (message in codes/scales), GN sums copied exactly.
  *     DPP_STALE, refresh = 0 (no_sync): the state is left untouched.
+ *   The new state is written in place, or into the second state set when the state
+ *   carries one (dpp_layer_state: gn_next, y_next, k_next, v_next), leaving the old one
+ *   as it was.
  * x, out: [B,H,W,C] `dtype`.  workspace: dpp_workspace_size() bytes, 256-aligned.
  * Requirements: those of halo_conv3x3 (Cin = Cout = C) and stale_kv_attention
  * (L = H*W), C % G == 0, C == heads*64, and for DPP_BF16 C % 128 == 0.
