@@ -38,6 +38,22 @@ __device__ __forceinline__ QuantBlock quant_block(float absmax) {
   return b;
 }
 
+// One element, the same rule as quant8 with a branch per element: returns
+// kRoundMagic + q and sets the new value.
+__device__ __forceinline__ float quant_elem(const QuantBlock& b, float d, float sv, float& nv) {
+  float tm;
+  if (b.fast) {
+    const float t = d * b.rc;
+    tm = t + kRoundMagic;
+    if (0.5f - fabsf(t - (tm - kRoundMagic)) < 1e-4f) tm = __fdiv_rn(d, b.s) + kRoundMagic;
+  } else {
+    tm = (float)quantise(d, b.s) + kRoundMagic;
+  }
+  tm = fminf(fmaxf(tm, kRoundMagic - 127.0f), kRoundMagic + 127.0f);  // clamp to +-127
+  nv = __fmaf_rn(tm - kRoundMagic, b.s, sv);
+  return tm;
+}
+
 // Eight elements: codes (kRoundMagic + q per element, its low byte the code) and new
 // values.  With r = rn(1/s), t = rn(d*r) lies within 2e-5 of rn(d/s) (|d/s| <= 127.0001
 // and three roundings of relative size 2^-24), so both round to the same integer unless
