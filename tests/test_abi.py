@@ -139,6 +139,9 @@ def test_host_checks_without_launch(lib):
     a = vp(256)
     assert lib.halo_conv3x3(a, a, a, a, 1, 9, 64, 64, 128, 2, dpp.BF16, None, None) == 2
     assert lib.halo_conv3x3(a, a, a, a, 1, 8, 64, 64, 100, 2, dpp.BF16, None, None) == 2
+    # bf16: W a multiple of 8 and H*W a multiple of 128 (row segments of gcd(W, 128))
+    assert lib.halo_conv3x3(a, a, a, a, 1, 16, 44, 64, 128, 2, dpp.BF16, None, None) == 2
+    assert lib.halo_conv3x3(a, a, a, a, 1, 3, 40, 64, 128, 3, dpp.BF16, None, None) == 2
     assert lib.stale_kv_attention(a, a, a, a, a, a, 1, 1024, 2, 32, 2, dpp.BF16, None, None) == 2
     assert lib.stale_kv_attention(a, a, a, a, a, a, 1, 1000, 2, 64, 3, dpp.BF16, None, None) == 2
     assert lib.stale_kv_attention(a, a, a, a, a, vp(8), 1, 1024, 2, 64, 2, dpp.BF16, None,
