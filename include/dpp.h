@@ -34,6 +34,10 @@
  *     word is already 0) and returns early, leaving its output incomplete.
  *     The environment variable DPP_DEBUG_WAIT_LIMIT (read at each call)
  *     overrides the wait bound; 0 makes every such wait give up at once.
+ *   - DPP_DEBUG_REFRESH_FORM (read at each call): 1 or 2 selects which of the two
+ *     equivalent forms of the residual quantiser the refresh kernel runs (with a
+ *     branch per element, or branch-free); both give the same bits, and the default
+ *     picks the faster one for the call.  For tests that run each form on one input.
  */
 #ifndef DPP_H_
 #define DPP_H_
@@ -337,12 +341,18 @@ int dpp_apply_layer_message(const dpp_layer_params* prm, const int8_t* codes,
  *   - All calls share the one array and it keeps the last call's contents:
  *     calls whose work overlaps on the GPU (different streams, or another
  *     thread) race on it and must be serialised by the caller.
- *   - The device status word lives inside the array and is not readable by the
- *     caller; a kernel that gives up still returns early, as with patch_layer_step.
+ *   - The device status word lives at the start of the array; a kernel that gives
+ *     up stores DPP_ERR_TIMEOUT there and returns early, as with patch_layer_step.
+ *     dpp_noalloc_read_status reads it.
  */
 int patch_layer_step_noalloc(const dpp_layer_params* prm, const dpp_layer_weights* wts,
                              const dpp_layer_state* st, const void* x, void* out, int mode,
                              void* stream);
+
+/* Synchronizes `stream` and returns the device status word of the last
+ * patch_layer_step_noalloc on the current device (DPP_OK, DPP_ERR_TIMEOUT, ...), or
+ * DPP_ERR_CUDA if the read fails.  Allocates nothing.  (No counterpart on the pages.) */
+int dpp_noalloc_read_status(void* stream);
 
 /* ---------------------------------------------------------------- OTIL exchange */
 

@@ -69,6 +69,7 @@ EXPORTS = ("dpp_status_string", "dpp_version", "refresh_residual", "halo_conv3x3
            "apply_residual", "dpp_apply_layer_message", "dpp_workspace_query", "dpp_workspace_size", "dpp_message_elems",
            "dpp_message_blocks", "patch_layer_step", "patch_layer_step_timed",
            "dpp_read_device_status", "dpp_layer_kernel_count", "patch_layer_step_noalloc",
+           "dpp_noalloc_read_status",
            "dpp_otil_blocks", "dpp_otil_step", "dpp_otil_finalize")
 
 
@@ -120,6 +121,8 @@ def load(build_if_missing: bool = False):
     lib.patch_layer_step_noalloc.restype = _c_int
     lib.patch_layer_step_noalloc.argtypes = [P(LayerParams), P(LayerWeights), P(LayerState),
                                              _c_void, _c_void, _c_int, _c_void]
+    lib.dpp_noalloc_read_status.restype = _c_int
+    lib.dpp_noalloc_read_status.argtypes = [_c_void]
     lib.dpp_read_device_status.restype = _c_int
     lib.dpp_read_device_status.argtypes = [_c_void, _c_void]
     lib.dpp_otil_blocks.restype = _c_int
@@ -325,6 +328,11 @@ def patch_layer_step_noalloc(prm: LayerParams, weights: dict, state: dict, x, ou
 
 def read_device_status(workspace, stream=None) -> int:
     return load().dpp_read_device_status(_ptr(workspace), _stream(stream))
+
+
+def noalloc_read_status(stream=None) -> int:
+    """Device status word of the last patch_layer_step_noalloc on the current device."""
+    return load().dpp_noalloc_read_status(_stream(stream))
 
 
 # ------------------------------------------------------------------ helpers for callers

@@ -24,6 +24,13 @@ long long wait_limit_from_env() {
   return v < 0 ? dpp::kDefaultWaitLimit : v;
 }
 
+int refresh_form_from_env() {
+  const char* s = getenv("DPP_DEBUG_REFRESH_FORM");
+  if (!s || !*s) return 0;
+  const int v = atoi(s);
+  return v == 1 || v == 2 ? v : 0;
+}
+
 int sm_count() {
   static std::mutex mu;
   static int cached[64] = {0};

@@ -64,3 +64,19 @@ extern "C" int patch_layer_step_noalloc(const dpp_layer_params* prm,
   // other workspace byte is written before it is read within the same call.
   return patch_layer_step(prm, wts, st, x, out, mode, scratch, stream);
 }
+
+// The device status word of the last patch_layer_step_noalloc on the current device
+// (offset 0 of the fixed scratch, zeroed at the start of each call and set by a kernel
+// whose bounded wait gave up): synchronizes `stream` and returns it, like
+// dpp_read_device_status does for a caller's workspace.  Allocates nothing.
+extern "C" int dpp_noalloc_read_status(void* stream) {
+  void* scratch = nullptr;
+  const int rc = scratch_for_current_device(&scratch);
+  if (rc) return rc;
+  int v = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, scratch, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DPP_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DPP_ERR_CUDA;
+  return v;
+}

@@ -186,7 +186,8 @@ int launch_refresh(const RefreshTable& tab, int dtype, cudaStream_t stream) {
   const int grid = (int)(want < 1 ? 1 : want < cap ? want : cap);  // >= 1 for the side copy
   // measured: the per-element form for a refresh of its own (4.94 -> 5.08 TB/s on the
   // 200 MiB sweep), the branch-free form beside the layer's output projection
-  const bool per_elem = !tab.early;
+  const int form = dpp_host::refresh_form_from_env();
+  const bool per_elem = form == 1 ? true : form == 2 ? false : !tab.early;
   using dpp_host::launch_pdl;
   cudaError_t e;
   if (dtype == DPP_BF16)

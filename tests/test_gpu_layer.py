@@ -5,7 +5,8 @@ Stage-wise checks feed each oracle step the GPU's own input bytes for that step
 bar on its own; the int8 residual codes are compared bit-exactly with the oracle
 refreshing the same fresh bytes.  The end-to-end output against an oracle run
 from x alone passes through six bf16-stored stages, each of which can flip a
-last bit; its bound is derived from that chain in the design notes (1e-2).
+last bit; it is held to the same 2e-3 (the bound stated for bf16 outputs), and each
+check reports the error it measured.
 """
 import numpy as np
 import pytest
@@ -17,7 +18,7 @@ import synth
 from tests.util import TOL_BF16, TOL_F32, np64, rel_err
 
 pytestmark = pytest.mark.gpu
-TOL_CHAIN_BF16 = 1e-2
+TOL_CHAIN_BF16 = 2e-3
 
 
 def _setup(cfg, seed=0, affine=True):
@@ -193,7 +194,7 @@ def test_layer_sync_step_and_state(name, fuse, dbuf):
     dpp.patch_layer_step(prm, wd, state, x_prev.cuda(), out, dpp.SYNC, ws)
     assert dpp.read_device_status(ws) == 0
     e2e = rel_err(np64(out), sync_fwd["out"])
-    assert e2e < (TOL_CHAIN_BF16 if cfg.dtype == "bf16" else TOL_F32)
+    assert e2e < (TOL_CHAIN_BF16 if cfg.dtype == "bf16" else TOL_F32), e2e
     v = {k: np64(t) for k, t in dpp.workspace_views(prm, ws).items()}
     # the (new) state is the exact copy of this step's fresh tensors
     nk = (lambda k: NEXT[k]) if dbuf else (lambda k: k)
@@ -211,10 +212,14 @@ def test_layer_sync_step_and_state(name, fuse, dbuf):
 
 @pytest.mark.parametrize("fuse", [False, True])
 def test_layer_sync_equals_unpartitioned_on_gpu(fuse):
-    """At the synchronous step the P-patch layer equals the P = 1 layer."""
+    """At the synchronous step the P-patch layer equals the unpartitioned layer, for
+    any P ("DistriFusion", How It Works: the first step is synchronous): the GPU's
+    output for P = 1, 2, 4, 8 against the oracle's P = 1 layer and against the GPU's
+    own P = 1 output, each within the bf16 bound."""
     base = CFGS["small_bf16"]
-    outs = []
-    for P in (1, 4):
+    outs = {}
+    ref = None
+    for P in (1, 2, 4, 8):
         cfg = synth.LayerConfig("s", B=base.B, H=base.H, W=base.W, C=base.C, P=P, G=base.G,
                                 heads=base.heads, head_dim=64, dtype="bf16")
         wts = synth.layer_weights(cfg, seed=1, affine=True)
@@ -224,9 +229,16 @@ def test_layer_sync_equals_unpartitioned_on_gpu(fuse):
         out = torch.empty(cfg.B, cfg.H, cfg.W, cfg.C, dtype=torch.bfloat16, device="cuda")
         dpp.patch_layer_step(prm, {k: t.cuda() for k, t in wts.items()}, state, x.cuda(), out,
                              dpp.SYNC, ws)
-        outs.append(np64(out))
-    # GroupNorm sums are grouped per patch, so equality holds to rounding
-    assert rel_err(outs[1], outs[0]) < 1e-2
+        assert dpp.read_device_status(ws) == 0
+        outs[P] = np64(out)
+        if ref is None:
+            wn = {k: np64(v) for k, v in wts.items()}
+            ref = oracle.layer_forward(np64(x), None, wn, 1, cfg.G, cfg.heads, cfg.eps, "bf16",
+                                       oracle.SYNC)["out"]
+    errs = {P: rel_err(o, ref) for P, o in outs.items()}
+    errs_gpu = {P: rel_err(o, outs[1]) for P, o in outs.items()}
+    assert max(errs.values()) < TOL_CHAIN_BF16, errs
+    assert max(errs_gpu.values()) < TOL_CHAIN_BF16, errs_gpu
 
 
 @pytest.mark.parametrize("dbuf", [False, True])
@@ -270,7 +282,8 @@ def test_layer_gn_modes(name, fuse, gn_mode):
     np.testing.assert_array_equal(np64(state["gn_stats"]), v["gn_fresh"])
     fwd = oracle.layer_forward(np64(x), ostate, wn, cfg.P, cfg.G, cfg.heads, cfg.eps, cfg.dtype,
                                oracle.STALE, gn_mode=gn_mode)
-    assert rel_err(np64(out), fwd["out"]) < (TOL_CHAIN_BF16 if cfg.dtype == "bf16" else TOL_F32)
+    e2e = rel_err(np64(out), fwd["out"])
+    assert e2e < (TOL_CHAIN_BF16 if cfg.dtype == "bf16" else TOL_F32), e2e
 
 
 @pytest.mark.parametrize("name,fuse,dbuf,frx", [("tiny_f32", False, False, False),
@@ -304,7 +317,8 @@ def test_layer_periodic_refresh_sequence(name, fuse, dbuf, frx):
         omode = oracle.SYNC if mode == dpp.SYNC else oracle.STALE
         fwd = oracle.layer_forward(np64(x), ost, wn, cfg.P, cfg.G, cfg.heads, cfg.eps, cfg.dtype,
                                    omode)
-        assert rel_err(np64(out), fwd["out"]) < tol, (i, mode)
+        e2e = rel_err(np64(out), fwd["out"])
+        assert e2e < tol, (i, mode, e2e)
         v = {k: np64(t) for k, t in dpp.workspace_views(prm, ws).items()}
         gpu_fwd = dict(gn_fresh=v["gn_fresh"], y=v["y"], k=v["k"], v=v["v"])
         new, _, _ = oracle.layer_state_update(gpu_fwd, ost, cfg.P, cfg.dtype, omode, True)

@@ -97,3 +97,31 @@ def test_apply_residual_matches_oracle_bitexact(dtype, n):
     dpp.apply_residual(torch.from_numpy(ec).cuda(), torch.from_numpy(es).cuda(), copy)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(np64(copy), en)
+
+
+@pytest.mark.parametrize("form", ["1", "2"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_refresh_edge_blocks_bitexact(dtype, form, monkeypatch):
+    """Blocks at the quantiser's edges (tests/refresh_edges.py): half-integer quotients
+    with scales that are not powers of two and their neighbours, |a/s| just above and
+    below 127, subnormal scales.  Each form of the kernel's quantiser (form 1: a branch
+    per element, form 2: branch-free), and the scalar pass on a ragged copy of the first
+    blocks, give the oracle's codes, scales and refreshed values bit for bit; the
+    receiver's apply of the oracle's message gives its refreshed buffer."""
+    from tests.refresh_edges import edge_blocks
+    monkeypatch.setenv("DPP_DEBUG_REFRESH_FORM", form)
+    f64, s64, _ = edge_blocks(dtype)
+    f64 = np.concatenate([f64, f64[:200]])
+    s64 = np.concatenate([s64, s64[:200]])
+    fresh = torch.from_numpy(f64).to(DT[dtype])
+    stale = torch.from_numpy(s64).to(DT[dtype])
+    assert np.array_equal(np64(fresh), f64) and np.array_equal(np64(stale), s64)
+    s, codes, scales = _run_gpu(fresh, stale)
+    en, ec, es = oracle.refresh_residual(f64, s64, dtype)
+    np.testing.assert_array_equal(codes.cpu().numpy(), ec)
+    np.testing.assert_array_equal(scales.cpu().numpy(), es)
+    np.testing.assert_array_equal(np64(s), en)
+    copy = stale.clone().cuda()
+    dpp.apply_residual(torch.from_numpy(ec).cuda(), torch.from_numpy(es).cuda(), copy)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(np64(copy), en)

@@ -483,3 +483,79 @@ def test_conv_rows_subset_matches_full():
     rows = np.array([0, 3, 4, 7, 11])
     np.testing.assert_allclose(oracle.halo_conv3x3(yf, ys, w, P, "f64", rows=rows), full[:, rows],
                                rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("P", [2, 4])
+def test_state_update_stale_refreshes_exactly_the_halo_rows_of_y(P):
+    """The STALE branch of the state update ("OTIL for SDXL on 4x L40S", item 3: the
+    stale state is the conv halo rows, the attention K/V and the two GroupNorm scalars
+    per group), pinned with sentinels.  Fresh y = +1 and stale y = -1 everywhere, so
+    each refreshed block has delta 2, scale 2/127 and codes 127, and its refreshed bf16
+    value rounds to exactly +1; h carries a third value (+5) that a refresh of the
+    wrong tensor would show.  Exactly rows r-1 and r at each interior boundary r become
+    +1, every other row stays -1; the message holds K, V, then 2*W*C codes of 127 per
+    (batch, boundary); the GroupNorm sums are copied exactly, not quantised."""
+    B, H, W, C, G = 2, 4 * P, 4, 8, 2
+    L = H * W
+    rng = np.random.default_rng(11)
+    y_f = np.ones((B, H, W, C))
+    fwd = dict(y=y_f, h=np.full((B, H, W, C), 5.0),
+               k=oracle.round_bf16(rng.standard_normal((B, L, C))),
+               v=oracle.round_bf16(rng.standard_normal((B, L, C))),
+               gn_fresh=rng.standard_normal((B, P, G, 2)) * 10.0 + 0.123456789)
+    state = dict(gn_stats=rng.standard_normal((B, P, G, 2)),
+                 y_stale=-np.ones((B, H, W, C)),
+                 k_stale=oracle.round_bf16(rng.standard_normal((B, L, C))),
+                 v_stale=oracle.round_bf16(rng.standard_normal((B, L, C))))
+    new, codes, scales = oracle.layer_state_update(fwd, state, P, "bf16", oracle.STALE, True)
+    Hp = H // P
+    halo = sorted({r for p in range(1, P) for r in (p * Hp - 1, p * Hp)})
+    assert len(halo) == 2 * (P - 1)
+    want = -np.ones((B, H, W, C))
+    want[:, halo] = 1.0
+    np.testing.assert_array_equal(new["y_stale"], want)
+    # GroupNorm sums: a bit-exact copy of this step's fresh sums
+    np.testing.assert_array_equal(new["gn_stats"], fwd["gn_fresh"])
+    # K and V refreshed towards the fresh values (not copied, not left alone)
+    for name in ("k", "v"):
+        got, fresh, old = new[name + "_stale"], fwd[name], state[name + "_stale"]
+        assert not np.array_equal(got, fresh) and not np.array_equal(got, old)
+        assert np.abs(got - fresh).max() < 0.05 * np.abs(fresh - old).max() + 2 ** -7
+    # message order and content: K (B*L*C), V (B*L*C), then per batch and boundary 2*W*C
+    n_kv = B * L * C
+    assert codes.size == 2 * n_kv + B * (P - 1) * 2 * W * C
+    np.testing.assert_array_equal(codes[2 * n_kv:], 127)
+    halo_scales = scales[2 * ((n_kv + 127) // 128):]
+    np.testing.assert_array_equal(halo_scales, np.float32(2.0) / np.float32(127.0))
+    # no refresh (no_sync) leaves every part of the state as it was
+    same, c0, s0 = oracle.layer_state_update(fwd, state, P, "bf16", oracle.STALE, False)
+    assert c0 is None and s0 is None
+    for k in state:
+        np.testing.assert_array_equal(same[k], state[k])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_refresh_edge_blocks_match_exact_rational_evaluation(dtype):
+    """Hand-built blocks at the quantiser's edges: fp32 quotients d/s exactly on a
+    half-integer with scales that are not powers of two (and their fp32 neighbours),
+    maxima whose rounded scale puts |a/s| just above or below 127, and subnormal scales.
+    The oracle's codes, scales and refreshed values equal the rule evaluated with exact
+    rationals and one rounding per IEEE operation; a ragged copy of the first blocks
+    checks a partial last block too."""
+    from tests.refresh_edges import edge_blocks
+    fresh, stale, _ = edge_blocks(dtype)
+    fresh = np.concatenate([fresh, fresh[:200]])
+    stale = np.concatenate([stale, stale[:200]])
+    new, codes, scales = oracle.refresh_residual(fresh, stale, dtype)
+    en, ec, es = _refresh_exact(fresh, stale, 8 if dtype == "bf16" else 24)
+    np.testing.assert_array_equal(codes, ec)
+    np.testing.assert_array_equal(scales, es)
+    np.testing.assert_array_equal(new, en)
+    # the blocks do reach the edges they were built for
+    q = (fresh - stale).astype(np.float32)
+    blk = q[:(q.size // 128) * 128].reshape(-1, 128)
+    s = (np.abs(blk).max(axis=1) / np.float32(127)).astype(np.float32)
+    t = (blk / s[:, None]).astype(np.float32)
+    assert np.sum(t - np.floor(t) == 0.5) >= 15
+    assert np.any(s < np.finfo(np.float32).tiny) and np.all(s > 0)
+    assert np.any(np.abs(codes) == 127)
