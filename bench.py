@@ -449,16 +449,17 @@ def measure_attention_3840(dev, peaks, iters=5):
     vs = (vf.float() + 0.05 * torch.randn(vf.shape, generator=g, device=dev)).to(torch.bfloat16)
     o = torch.empty_like(q)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    npart = dpp.attention_partials_size(B, L, heads, P)
-    part = torch.empty(max(npart, 16), dtype=torch.uint8, device=dev)
+    scratch = {sp: torch.empty(dpp.attention_scratch_size(B, L, heads, P, split=sp),
+                               dtype=torch.uint8, device=dev) for sp in (True, False)}
     flop = 4.0 * B * heads * L * L * 64
 
     def run(split):
         if split:
-            dpp.stale_kv_attention_split(q, kf, vf, ks, vs, o, heads, P,
-                                         partials=part if npart else None, dev_status=st)
+            dpp.stale_kv_attention_split(q, kf, vf, ks, vs, o, heads, P, scratch=scratch[True],
+                                         dev_status=st)
         else:
-            dpp.stale_kv_attention(q, kf, vf, ks, vs, o, heads, P, dev_status=st)
+            dpp.stale_kv_attention(q, kf, vf, ks, vs, o, heads, P, scratch=scratch[False],
+                                   dev_status=st)
 
     res = {}
     for split in (True, False):

@@ -38,6 +38,11 @@
  *     equivalent forms of the residual quantiser the refresh kernel runs (with a
  *     branch per element, or branch-free); both give the same bits, and the default
  *     picks the faster one for the call.  For tests that run each form on one input.
+ *   - DPP_DEBUG_SKIP_LOAD=<kind>:<i> (read at each call; kind attn, conv or linear):
+ *     every CTA of the attention kernel, of the conv's GEMM or of the projections'
+ *     GEMM leaves its i-th K/V tile or K slice unloaded, so its bounded waits give up
+ *     and the device status becomes DPP_ERR_TIMEOUT.  For tests of that path; unset in
+ *     normal use.
  */
 #ifndef DPP_H_
 #define DPP_H_
@@ -135,12 +140,24 @@ int halo_conv3x3(const void* y_fresh, const void* y_stale, const void* w, void* 
  * keys, no mask.  q, k_*, v_*, o: [B, L, heads*head_dim] of `dtype`.
  * Requires head_dim == 64, L % P == 0 and (L/P) % 8 == 0; for DPP_BF16 also
  * B*heads*P*ceil(L/P/256) * ceil(L/128) < 2^31 (the kernel's step counter).
+ * Values must be finite.  DPP_BF16 numerics: fp32 scores and softmax, the
+ * probabilities rounded to fp16 for the P.V product, V widened to fp16 after an exact
+ * scaling by a power of two per (batch, head) chosen from max|V| over the fresh and
+ * stale V (no scaling when max|V| lies in [2^-6, 2^15); otherwise the scaled maximum
+ * lies in [2^14, 2^15)), so that any finite bf16 V keeps fp16's full precision
+ * relative to its largest value (down to max|V| of about 2^-111).
+ * scratch: caller-owned device buffer, 16-byte aligned, of at least
+ * dpp_attention_scratch_size(..., split = 0) bytes for DPP_BF16 (it receives the
+ * per-(batch, head) maxima of |V|; its contents are not used after the call); may be
+ * NULL for DPP_F32, whose size is 0.  Returns DPP_ERR_ARG if it is missing or short.
  * dev_status: device int (may be NULL) that receives a give-up code.
  */
+size_t dpp_attention_scratch_size(int B, int L, int heads, int head_dim, int P, int dtype,
+                                  int split);
 int stale_kv_attention(const void* q, const void* k_fresh, const void* v_fresh,
                        const void* k_stale, const void* v_stale, void* o,
                        int B, int L, int heads, int head_dim, int P, int dtype,
-                       int* dev_status, void* stream);
+                       void* scratch, size_t scratch_bytes, int* dev_status, void* stream);
 
 /*
  * stale_kv_attention_split -- the same operation and result (up to rounding) with
@@ -152,24 +169,19 @@ int stale_kv_attention(const void* q, const void* k_fresh, const void* v_fresh,
  * each CTA whole units, so when their number is not a multiple of the SM count
  * the last round leaves SMs idle.  Here those last units are cut into runs of
  * 128-key tiles shared evenly by all CTAs; each piece leaves a partial result
- * (O/l rounded to fp16, the running maximum m and sum l in fp32) in `partials`,
+ * (O/l rounded to fp16, the running maximum m and sum l in fp32) in the scratch,
  * and whichever piece of a unit finishes last merges them all in a fixed order
  * (deterministic; the call zeroes the counters it uses for this at the start of the
  * buffer).  The merge reads O/l in fp16, whose rounding (2^-11 relative) stays well
  * below that of the bf16 output.
- * partials: caller-owned device buffer, 16-byte aligned, of at least
- * dpp_attention_partials_size() bytes; that size depends on the current device's
- * SM count, so query it on the device that runs the call.  It may be NULL when
- * the size is 0 (the units divide evenly; both calls then run the same kernel).
- * The buffer is scratch: its contents are not used after the call.
- * Returns DPP_ERR_ARG if the buffer is missing or too small.  DPP_F32 runs the
- * fp32 kernel of stale_kv_attention and ignores `partials`.
+ * scratch: as for stale_kv_attention, of at least
+ * dpp_attention_scratch_size(..., split = 1) bytes; that size depends on the current
+ * device's SM count, so query it on the device that runs the call.
  */
-size_t dpp_attention_partials_size(int B, int L, int heads, int head_dim, int P, int dtype);
 int stale_kv_attention_split(const void* q, const void* k_fresh, const void* v_fresh,
                              const void* k_stale, const void* v_stale, void* o,
                              int B, int L, int heads, int head_dim, int P, int dtype,
-                             void* partials, size_t partials_bytes,
+                             void* scratch, size_t scratch_bytes,
                              int* dev_status, void* stream);
 
 /* ---------------------------------------------------------------- layer step */
@@ -251,10 +263,10 @@ typedef struct dpp_workspace_layout {
   size_t h;          /* [B,H,W,C] conv output */
   size_t q, k, v;    /* [B,L,C] fresh projections */
   size_t o;          /* [B,L,C] attention output */
-  size_t attn_partial;       /* partial results of the split attention schedule
-                                (dpp_attention_partials_size bytes) */
-  size_t attn_partial_bytes; /* their size, 0 when the units divide evenly (a size, not an
-                                offset) */
+  size_t attn_partial;       /* the attention's scratch: per-(batch, head) range of V and
+                                the split schedule's partial results
+                                (dpp_attention_scratch_size(..., split = 1) bytes) */
+  size_t attn_partial_bytes; /* its size (a size, not an offset; 0 for DPP_F32) */
   size_t total;      /* bytes to allocate */
 } dpp_workspace_layout;
 

@@ -65,7 +65,7 @@ class OtilParams(ctypes.Structure):
 
 _lib = None
 EXPORTS = ("dpp_status_string", "dpp_version", "refresh_residual", "halo_conv3x3",
-           "stale_kv_attention", "stale_kv_attention_split", "dpp_attention_partials_size",
+           "stale_kv_attention", "stale_kv_attention_split", "dpp_attention_scratch_size",
            "apply_residual", "dpp_apply_layer_message", "dpp_workspace_query", "dpp_workspace_size", "dpp_message_elems",
            "dpp_message_blocks", "patch_layer_step", "patch_layer_step_timed",
            "dpp_read_device_status", "dpp_layer_kernel_count", "patch_layer_step_noalloc",
@@ -98,12 +98,13 @@ def load(build_if_missing: bool = False):
     lib.halo_conv3x3.restype = _c_int
     lib.halo_conv3x3.argtypes = [_c_void] * 4 + [_c_int] * 7 + [_c_void, _c_void]
     lib.stale_kv_attention.restype = _c_int
-    lib.stale_kv_attention.argtypes = [_c_void] * 6 + [_c_int] * 6 + [_c_void, _c_void]
+    lib.stale_kv_attention.argtypes = ([_c_void] * 6 + [_c_int] * 6 +
+                                       [_c_void, ctypes.c_size_t, _c_void, _c_void])
     lib.stale_kv_attention_split.restype = _c_int
     lib.stale_kv_attention_split.argtypes = ([_c_void] * 6 + [_c_int] * 6 +
                                              [_c_void, ctypes.c_size_t, _c_void, _c_void])
-    lib.dpp_attention_partials_size.restype = ctypes.c_size_t
-    lib.dpp_attention_partials_size.argtypes = [_c_int] * 6
+    lib.dpp_attention_scratch_size.restype = ctypes.c_size_t
+    lib.dpp_attention_scratch_size.argtypes = [_c_int] * 7
     lib.dpp_workspace_query.restype = _c_int
     lib.dpp_workspace_query.argtypes = [P(LayerParams), P(WorkspaceLayout)]
     lib.dpp_workspace_size.restype = ctypes.c_size_t
@@ -208,33 +209,40 @@ def halo_conv3x3(y_fresh, y_stale, w, out, P: int, dev_status=None, stream=None)
            "halo_conv3x3")
 
 
-def stale_kv_attention(q, k_fresh, v_fresh, k_stale, v_stale, o, heads: int, P: int,
-                       dev_status=None, stream=None):
-    lib = load()
+def attention_scratch_size(B: int, L: int, heads: int, P: int, dtype: int = BF16,
+                           split: bool = False) -> int:
+    """Bytes of the scratch buffer stale_kv_attention (split=False) or
+    stale_kv_attention_split (split=True) needs on the current device."""
+    return load().dpp_attention_scratch_size(B, L, heads, 64, P, dtype, 1 if split else 0)
+
+
+def _attention(fn, name, q, k_fresh, v_fresh, k_stale, v_stale, o, heads, P, scratch,
+               dev_status, stream, split):
     B, L, C = q.shape
-    _check(lib.stale_kv_attention(_ptr(q), _ptr(k_fresh), _ptr(v_fresh), _ptr(k_stale),
-                                  _ptr(v_stale), _ptr(o), B, L, heads, C // heads, P,
-                                  dtype_code(q), _ptr(dev_status), _stream(stream)),
-           "stale_kv_attention")
+    if scratch is None:
+        n = attention_scratch_size(B, L, heads, P, dtype_code(q), split)
+        scratch = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+    nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
+    _check(fn(_ptr(q), _ptr(k_fresh), _ptr(v_fresh), _ptr(k_stale), _ptr(v_stale), _ptr(o), B, L,
+              heads, C // heads, P, dtype_code(q), _ptr(scratch), nbytes, _ptr(dev_status),
+              _stream(stream)), name)
 
 
-def attention_partials_size(B: int, L: int, heads: int, P: int, dtype: int = BF16) -> int:
-    """Bytes of the partials buffer stale_kv_attention_split needs on the current device."""
-    return load().dpp_attention_partials_size(B, L, heads, 64, P, dtype)
+def stale_kv_attention(q, k_fresh, v_fresh, k_stale, v_stale, o, heads: int, P: int,
+                       scratch=None, dev_status=None, stream=None):
+    """Whole units per CTA.  ``scratch``: a device buffer of at least
+    attention_scratch_size(split=False) bytes, or None to have one allocated here (by
+    torch, the caller's allocator)."""
+    _attention(load().stale_kv_attention, "stale_kv_attention", q, k_fresh, v_fresh, k_stale,
+               v_stale, o, heads, P, scratch, dev_status, stream, False)
 
 
 def stale_kv_attention_split(q, k_fresh, v_fresh, k_stale, v_stale, o, heads: int, P: int,
-                             partials=None, dev_status=None, stream=None):
-    """stale_kv_attention with the last units shared by all SMs; ``partials`` is a device
-    buffer of at least attention_partials_size() bytes (None when that is 0)."""
-    lib = load()
-    B, L, C = q.shape
-    nbytes = 0 if partials is None else partials.numel() * partials.element_size()
-    _check(lib.stale_kv_attention_split(_ptr(q), _ptr(k_fresh), _ptr(v_fresh), _ptr(k_stale),
-                                        _ptr(v_stale), _ptr(o), B, L, heads, C // heads, P,
-                                        dtype_code(q), _ptr(partials), nbytes,
-                                        _ptr(dev_status), _stream(stream)),
-           "stale_kv_attention_split")
+                             scratch=None, dev_status=None, stream=None):
+    """stale_kv_attention with the last units shared by all SMs; ``scratch`` as above with
+    attention_scratch_size(split=True) bytes."""
+    _attention(load().stale_kv_attention_split, "stale_kv_attention_split", q, k_fresh, v_fresh,
+               k_stale, v_stale, o, heads, P, scratch, dev_status, stream, True)
 
 
 GN_SPLICED, GN_SYNC, GN_PREVIOUS = 0, 1, 2

@@ -5,6 +5,7 @@
 // GroupNorm, the patched conv and the patched attention on their synchronous
 // branch).  Every step of the path runs in this library's kernels.
 #include <stdlib.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -22,6 +23,15 @@ long long wait_limit_from_env() {
   if (!s || !*s) return dpp::kDefaultWaitLimit;
   long long v = atoll(s);
   return v < 0 ? dpp::kDefaultWaitLimit : v;
+}
+
+int skip_load_from_env(const char* kind) {
+  const char* s = getenv("DPP_DEBUG_SKIP_LOAD");
+  if (!s || !*s) return -1;
+  const size_t n = strlen(kind);
+  if (strncmp(s, kind, n) != 0 || s[n] != ':') return -1;
+  const int v = atoi(s + n + 1);
+  return v < 0 ? -1 : v;
 }
 
 int refresh_form_from_env() {
@@ -124,10 +134,11 @@ int layout(const dpp_layer_params* p, dpp_workspace_layout* o) {
   o->k = off; off = align256(off + act);
   o->v = off; off = align256(off + act);
   o->o = off; off = align256(off + act);
-  // partial results of the split attention schedule (a region of their own, so that
-  // every stage's output stays readable after the step)
-  const size_t part = p->dtype == DPP_BF16 ? dpp::tc_attention_partial_bytes(
-                                                 p->B, p->H * p->W, p->heads, p->P)
+  // the attention's scratch: the per-(batch, head) range of V and the partial results of
+  // the split schedule (a region of its own, so that every stage's output stays
+  // readable after the step)
+  const size_t part = p->dtype == DPP_BF16 ? dpp::tc_attention_scratch_bytes(
+                                                 p->B, p->H * p->W, p->heads, p->P, true)
                                            : 0;
   o->attn_partial = off; off = align256(off + part);
   o->attn_partial_bytes = part;
@@ -144,10 +155,11 @@ int run_conv(const void* yf, const void* ys, const void* w, void* out, int B, in
 }
 
 int run_linear(const void* a, const void* w, void* o0, void* o1, void* o2, long long M, int N,
-               int K, int dtype, int* st, cudaStream_t s) {
+               int K, int dtype, int* st, cudaStream_t s, unsigned* vmax = nullptr,
+               int vmax_L = 0, int vmax_heads = 0) {
   if (dtype == DPP_BF16)
     return dpp::launch_tc_linear(a, w, o0, o1, o2, M, N, K, st, dpp_host::wait_limit_from_env(),
-                                 s);
+                                 s, vmax, vmax_L, vmax_heads);
   dpp::SimtOut o{};
   o.ptr[0] = o0; o.ptr[1] = o1; o.ptr[2] = o2;
   o.ncols = o1 ? N / 3 : N;
@@ -155,11 +167,14 @@ int run_linear(const void* a, const void* w, void* o0, void* o1, void* o2, long 
 }
 
 int run_attention(const void* q, const void* kf, const void* vf, const void* ks, const void* vs,
-                  void* o, int B, int L, int heads, int P, int dtype, void* part,
-                  size_t part_bytes, bool counters_zeroed, int* st, cudaStream_t s) {
+                  void* o, int B, int L, int heads, int P, int dtype, bool split, void* scratch,
+                  size_t scratch_bytes, bool scratch_zeroed, int* st, cudaStream_t s,
+                  bool vmax_ready = false) {
   if (dtype == DPP_BF16)
-    return dpp::launch_tc_attention(q, kf, vf, ks, vs, o, B, L, heads, P, part, part_bytes,
-                                    counters_zeroed, st, dpp_host::wait_limit_from_env(), s);
+    return dpp::launch_tc_attention(q, kf, vf, ks, vs, o, B, L, heads, P, split, scratch,
+                                    scratch_bytes, scratch_zeroed, vmax_ready, st,
+                                    dpp_host::wait_limit_from_env(),
+                                    dpp_host::skip_load_from_env("attn"), s);
   return dpp::launch_simt_attention(q, kf, vf, ks, vs, o, B, L, heads, P, dtype, s);
 }
 
@@ -199,7 +214,7 @@ const char* dpp_status_string(int status) {
   }
 }
 
-int dpp_version(void) { return 100; }
+int dpp_version(void) { return 200; }
 
 int refresh_residual(const void* fresh, void* stale, int8_t* codes, float* scales, int64_t n,
                      int dtype, void* stream) {
@@ -244,44 +259,45 @@ int halo_conv3x3(const void* y_fresh, const void* y_stale, const void* w, void* 
                   static_cast<cudaStream_t>(stream));
 }
 
-int stale_kv_attention(const void* q, const void* k_fresh, const void* v_fresh,
-                       const void* k_stale, const void* v_stale, void* o, int B, int L, int heads,
-                       int head_dim, int P, int dtype, int* dev_status, void* stream) {
+size_t dpp_attention_scratch_size(int B, int L, int heads, int head_dim, int P, int dtype,
+                                  int split) {
+  if (check_dtype(dtype) || check_attn(B, L, heads, head_dim, P, dtype)) return 0;
+  return dtype == DPP_BF16 ? dpp::tc_attention_scratch_bytes(B, L, heads, P, split != 0) : 0;
+}
+
+static int attention_call(const void* q, const void* k_fresh, const void* v_fresh,
+                          const void* k_stale, const void* v_stale, void* o, int B, int L,
+                          int heads, int head_dim, int P, int dtype, bool split, void* scratch,
+                          size_t scratch_bytes, int* dev_status, void* stream) {
   int rc = check_dtype(dtype);
   if (rc) return rc;
   if (!q || !k_fresh || !v_fresh || !k_stale || !v_stale || !o) return DPP_ERR_NULL;
   rc = check_attn(B, L, heads, head_dim, P, dtype);
   if (rc) return rc;
   if (!aligned16(q) || !aligned16(k_fresh) || !aligned16(v_fresh) || !aligned16(k_stale) ||
-      !aligned16(v_stale) || !aligned16(o))
+      !aligned16(v_stale) || !aligned16(o) || (scratch && !aligned16(scratch)))
     return DPP_ERR_ALIGN;
-  return run_attention(q, k_fresh, v_fresh, k_stale, v_stale, o, B, L, heads, P, dtype, nullptr,
-                       0, false, dev_status, static_cast<cudaStream_t>(stream));
+  const size_t need = dpp_attention_scratch_size(B, L, heads, head_dim, P, dtype, split);
+  if (need && (!scratch || scratch_bytes < need)) return DPP_ERR_ARG;
+  return run_attention(q, k_fresh, v_fresh, k_stale, v_stale, o, B, L, heads, P, dtype, split,
+                       scratch, scratch_bytes, false, dev_status,
+                       static_cast<cudaStream_t>(stream));
 }
 
-size_t dpp_attention_partials_size(int B, int L, int heads, int head_dim, int P, int dtype) {
-  if (check_dtype(dtype) || check_attn(B, L, heads, head_dim, P, dtype)) return 0;
-  return dtype == DPP_BF16 ? dpp::tc_attention_partial_bytes(B, L, heads, P) : 0;
+int stale_kv_attention(const void* q, const void* k_fresh, const void* v_fresh,
+                       const void* k_stale, const void* v_stale, void* o, int B, int L, int heads,
+                       int head_dim, int P, int dtype, void* scratch, size_t scratch_bytes,
+                       int* dev_status, void* stream) {
+  return attention_call(q, k_fresh, v_fresh, k_stale, v_stale, o, B, L, heads, head_dim, P, dtype,
+                        false, scratch, scratch_bytes, dev_status, stream);
 }
 
 int stale_kv_attention_split(const void* q, const void* k_fresh, const void* v_fresh,
                              const void* k_stale, const void* v_stale, void* o, int B, int L,
-                             int heads, int head_dim, int P, int dtype, void* partials,
-                             size_t partials_bytes, int* dev_status, void* stream) {
-  int rc = check_dtype(dtype);
-  if (rc) return rc;
-  if (!q || !k_fresh || !v_fresh || !k_stale || !v_stale || !o) return DPP_ERR_NULL;
-  rc = check_attn(B, L, heads, head_dim, P, dtype);
-  if (rc) return rc;
-  if (!aligned16(q) || !aligned16(k_fresh) || !aligned16(v_fresh) || !aligned16(k_stale) ||
-      !aligned16(v_stale) || !aligned16(o) || (partials && !aligned16(partials)))
-    return DPP_ERR_ALIGN;
-  const size_t need = dpp_attention_partials_size(B, L, heads, head_dim, P, dtype);
-  if (need && (!partials || partials_bytes < need)) return DPP_ERR_ARG;
-  // with `need` 0 the units divide evenly and both schedules are the same
-  return run_attention(q, k_fresh, v_fresh, k_stale, v_stale, o, B, L, heads, P, dtype,
-                       need ? partials : nullptr, partials_bytes, false, dev_status,
-                       static_cast<cudaStream_t>(stream));
+                             int heads, int head_dim, int P, int dtype, void* scratch,
+                             size_t scratch_bytes, int* dev_status, void* stream) {
+  return attention_call(q, k_fresh, v_fresh, k_stale, v_stale, o, B, L, heads, head_dim, P, dtype,
+                        true, scratch, scratch_bytes, dev_status, stream);
 }
 
 int dpp_workspace_query(const dpp_layer_params* prm, dpp_workspace_layout* out) {
@@ -440,19 +456,25 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
   if ((rc = mark(0))) return rc;
   // a1 + a2: fresh sums of every patch, spliced GroupNorm
   const dpp::GnDims g = dpp::make_gn_dims(p.B, p.H, p.W, p.C, p.P, p.G);
-  // the first kernel also zeroes the status word and the attention's piece counters
-  const int ncnt = p.dtype == DPP_BF16 && lo.attn_partial_bytes
-                       ? dpp::tc_attention_counters(p.B, L, p.heads, p.P)
-                       : 0;
+  // the first kernel also zeroes the status word and the start of the attention's scratch
+  // (its V maxima and piece counters)
+  const int ncnt = p.dtype == DPP_BF16 ? dpp::tc_attention_zero_ints(p.B, L, p.heads, p.P, true)
+                                        : 0;
   // fuse_gn: the apply writes only the rows other bands read as halos (and the state
   // update reads), plus the per-channel parameters; the conv normalises its own band's
   // rows of x as its tiles land in shared memory
   const bool fused = p.fuse_gn != 0;
   float* gn_params = fused ? reinterpret_cast<float*>(ws + lo.gn_params) : nullptr;
+  // The attention's V scaling needs max |V| per (batch, head) of the V it reads: on the
+  // plain bf16 path the GroupNorm apply takes it over the stale V (a stale step with P > 1)
+  // and the Q/K/V projection's epilogue over the fresh V, instead of a separate pass.
+  const bool vmax_fold = p.dtype == DPP_BF16 && !fused && !fuse_rfx;
+  unsigned* vmax = reinterpret_cast<unsigned*>(ws + lo.attn_partial);
   rc = dpp::launch_gn(x, y, gn_partial, sync ? nullptr : st->gn_stats, gn_fresh, wts->gamma,
                       wts->beta, g, p.eps, sync ? DPP_GN_SYNC : p.gn_mode, p.dtype, status,
                       reinterpret_cast<int*>(ws + lo.attn_partial), ncnt, gn_params,
-                      fused ? 1 : 0, s);
+                      fused ? 1 : 0, vmax_fold && !sync && p.P > 1 ? st->v_stale : nullptr,
+                      vmax, p.heads, s);
   if (rc || (rc = mark(1))) return rc;
   // a3: halo conv, halo rows from the stale conv input (fresh at the synchronous step)
   rc = run_conv(fused ? x : y, sync ? y : st->y_stale, wts->w_conv, h, p.B, p.H, p.W, p.C, p.C,
@@ -469,12 +491,13 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
                                        st->v_stale, k_dst, v_dst, st->codes, st->scales, status,
                                        dpp_host::wait_limit_from_env(), s);
   else
-    rc = run_linear(h, wts->w_qkv, q, k, v, M, 3 * p.C, p.C, p.dtype, status, s);
+    rc = run_linear(h, wts->w_qkv, q, k, v, M, 3 * p.C, p.C, p.dtype, status, s,
+                    vmax_fold ? vmax : nullptr, L, p.heads);
   if (rc || (rc = mark(3))) return rc;
   // a5: stale-KV attention
   rc = run_attention(q, k, v, sync ? k : st->k_stale, sync ? v : st->v_stale, o, p.B, L, p.heads,
-                     p.P, p.dtype, lo.attn_partial_bytes ? ws + lo.attn_partial : nullptr,
-                     lo.attn_partial_bytes, true /* zeroed by gn_stats */, status, s);
+                     p.P, p.dtype, true, ws + lo.attn_partial, lo.attn_partial_bytes,
+                     true /* zeroed by gn_stats */, status, s, vmax_fold);
   if (rc || (rc = mark(4))) return rc;
   // a6: output projection
   rc = run_linear(o, wts->w_o, out, nullptr, nullptr, M, p.C, p.C, p.dtype, status, s);

@@ -72,6 +72,10 @@ long long wait_limit_from_env();  // DPP_DEBUG_WAIT_LIMIT, else the default
 // one, anything else = the default choice (both forms give the same bits; the variable
 // lets the tests run each form on the same inputs)
 int refresh_form_from_env();
+// DPP_DEBUG_SKIP_LOAD=<kind>:<i> (kind "attn", "conv" or "linear"): a test hook that makes the TMA
+// producer of every CTA of that kernel kind leave its i-th load unissued, so that the
+// kernel's bounded waits give up and report DPP_ERR_TIMEOUT; -1 when unset
+int skip_load_from_env(const char* kind);
 int sm_count();                   // SMs of the current device (cached per device)
 
 // Launches kernel<<<grid, block, smem, s>>>(args...) with programmatic stream

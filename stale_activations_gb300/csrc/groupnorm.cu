@@ -112,8 +112,10 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
                                                        const float* __restrict__ beta, GnDims g,
                                                        float eps, int mode,
                                                        float* __restrict__ params_out,
-                                                       int halo_only) {
+                                                       int halo_only, const T* __restrict__ vstale,
+                                                       unsigned* __restrict__ vmax, int heads) {
   constexpr int VEC = Vec<T>::N;
+  __shared__ unsigned s_hmax[32];  // max |V_stale| bits per head of this block
   extern __shared__ float sm[];  // group sums [P][G][2], then mean and rstd [G][2]
   const bool all_fresh = mode == DPP_GN_SYNC;
   const int G2 = g.G * 2;
@@ -161,8 +163,38 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
   if (!all_fresh)
     for (int idx = tid; idx < g.P * G2; idx += blockDim.x)
       if (idx / G2 != p) s_tot[idx] = stale_stats[(long long)b * g.P * G2 + idx];
+  // The stale V has x's layout ([B, H*W, C]): its max |V| per (batch, head) over this
+  // block's pixels, for the attention's fp16 scaling of V.  It is state written before the
+  // stats kernel started, so it is read before the wait; the per-(batch, head) maxima are
+  // zeroed by the stats kernel, so they are updated after it.
+  if (vstale) {
+    if (tid < 32) s_hmax[tid] = 0;
+    __syncthreads();
+    unsigned vm = 0;
+    if (active) {
+      for (long long q = p0 + pl; q < p1; q += 4 * PIX) {
+        uint4 w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (q + k * PIX < p1)
+            w[k] = __ldcs(reinterpret_cast<const uint4*>(vstale + base + (q + k * PIX) * g.C));
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (q + k * PIX < p1) {
+            const uint32_t h4[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              vm = max(vm, max(h4[e] & 0x7FFFu, (h4[e] >> 16) & 0x7FFFu));
+          }
+      }
+      if (vm) atomicMax(&s_hmax[(v * VEC) / 64], vm);
+    }
+    __syncthreads();
+  }
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
+  if (vstale && tid < heads && s_hmax[tid])
+    atomicMax(vmax + (long long)b * heads + tid, s_hmax[tid] << 16);  // bf16 -> fp32 bits
   // fresh sums over chunks, for own patch (and every patch when all are fresh): tps
   // threads per sum, each a fixed stride of chunks with eight loads in flight, then a
   // shuffle tree (fixed order)
@@ -267,7 +299,8 @@ size_t gn_partial_bytes(const GnDims& g) {
 int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, float* fresh_out,
               const float* gamma, const float* beta, const GnDims& g, float eps, int mode,
               int dtype, int* status_to_zero, int* zero_ints, int nzero, float* params_out,
-              int halo_only, cudaStream_t stream) {
+              int halo_only, const void* vstale, unsigned* vmax, int heads,
+              cudaStream_t stream) {
   dim3 grid(g.nchunk, g.P, g.B);
   const dim3 agrid = halo_only ? dim3(2, g.P, g.B) : grid;
   const int VEC = dtype == DPP_BF16 ? 8 : 4;
@@ -284,7 +317,8 @@ int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, 
     if (e == cudaSuccess)
       e = launch_pdl(gn_apply_kernel<__nv_bfloat16>, agrid, dim3(256), app_bytes, stream, xs,
                      static_cast<__nv_bfloat16*>(y), (const float*)partial, stale_stats, fresh_out,
-                     gamma, beta, g, eps, mode, params_out, halo_only);
+                     gamma, beta, g, eps, mode, params_out, halo_only,
+                     static_cast<const __nv_bfloat16*>(vstale), vmax, heads);
   } else {
     auto* xs = static_cast<const float*>(x);
     e = launch_pdl(gn_stats_kernel<float>, grid, dim3(256), red_bytes, stream, xs, partial, g,
@@ -292,7 +326,7 @@ int launch_gn(const void* x, void* y, float* partial, const float* stale_stats, 
     if (e == cudaSuccess)
       e = launch_pdl(gn_apply_kernel<float>, agrid, dim3(256), app_bytes, stream, xs,
                      static_cast<float*>(y), (const float*)partial, stale_stats, fresh_out, gamma,
-                     beta, g, eps, mode, params_out, halo_only);
+                     beta, g, eps, mode, params_out, halo_only, nullptr, nullptr, 0);
   }
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }

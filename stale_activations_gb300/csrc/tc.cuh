@@ -10,8 +10,12 @@ bool tc_linear_supported(long long M, int C);
 
 // out[M, N] = a[M, K] * w[N, K]^T (bf16, fp32 accumulation).  If o1/o2 are
 // non-NULL, N is split into three equal column blocks written to o0, o1, o2.
+// With vmax non-NULL (three-way split only, vmax_L a multiple of 128): also the max |o2|
+// per (batch of vmax_L rows, 64-column head) into vmax [batches][vmax_heads] as fp32 bits
+// by atomicMax (vmax zeroed before the launch).
 int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2, long long M,
-                     int N, int K, int* status, long long wait_limit, cudaStream_t s);
+                     int N, int K, int* status, long long wait_limit, cudaStream_t s,
+                     unsigned* vmax = nullptr, int vmax_L = 0, int vmax_heads = 0);
 
 // The packed Q, K, V projection (N = 3 * ncols, ncols a multiple of 128, 128-wide tiles)
 // with the compressed-residual refresh of K and V in its epilogue: besides storing fresh
@@ -35,18 +39,23 @@ int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int
                    int Cin, int Cout, int P, const float* gn_par, int* status,
                    long long wait_limit, cudaStream_t s);
 
-// Stale-KV flash attention (see stale_kv_attention in dpp.h), head_dim 64.  With
-// `partials` non-NULL the units that do not divide evenly over the CTAs are shared key
-// tile by key tile and merged in the kernel; partial_bytes must then be at least
-// tc_attention_partial_bytes() (0 when the units divide evenly).  The buffer starts
-// with tc_attention_counters() ints that must be zero when the kernel starts: the
-// launch zeroes them unless counters_zeroed says an earlier kernel of the stream did
-// (the kernel leaves them zero).
+// Stale-KV flash attention (see stale_kv_attention in dpp.h), head_dim 64.  `scratch`
+// (tc_attention_scratch_bytes() bytes) holds the per-(batch, head) maxima of |V| that
+// set V's fp16 scaling and, with `split`, the counters and partial records of the units
+// shared key tile by key tile; its first tc_attention_zero_ints() ints must be zero when
+// the launch runs: the launch zeroes them unless scratch_zeroed says an earlier kernel of
+// the stream did (the kernel leaves the counters zero, not the maxima).  Launches a
+// small max|V| pass, then the attention kernel.  skip_load (test hook, normally -1):
+// the producer of every CTA leaves the K/V tile of that step unloaded, so the kernel's
+// bounded waits give up with DPP_ERR_TIMEOUT.
+// vmax_ready: the maxima at the start of the scratch were already computed by earlier
+// kernels of the stream (then the max |V| pass is not launched; scratch_zeroed must hold).
 int launch_tc_attention(const void* q, const void* kf, const void* vf, const void* ks,
-                        const void* vs, void* o, int B, int L, int heads, int P, void* partials,
-                        size_t partial_bytes, bool counters_zeroed, int* status,
-                        long long wait_limit, cudaStream_t s);
-size_t tc_attention_partial_bytes(int B, int L, int heads, int P);
-int tc_attention_counters(int B, int L, int heads, int P);
+                        const void* vs, void* o, int B, int L, int heads, int P, bool split,
+                        void* scratch, size_t scratch_bytes, bool scratch_zeroed,
+                        bool vmax_ready, int* status, long long wait_limit, int skip_load,
+                        cudaStream_t s);
+size_t tc_attention_scratch_bytes(int B, int L, int heads, int P, bool split);
+int tc_attention_zero_ints(int B, int L, int heads, int P, bool split);
 
 }  // namespace dpp

@@ -15,9 +15,11 @@
 // cut between CTAs leaves one partial result per piece (O/l in fp16, the running
 // maximum m and sum l in fp32); the warpgroup that finishes a unit's last piece
 // (an atomic count per unit and query tile) merges all of them in CTA order, so the
-// result does not depend on which piece finished last.  A CTA's steps run through one pipeline:
-// the next unit's Q is loaded into the second Q buffer while the current unit
-// finishes, and its first S = Q K^T is issued right after the last P V.
+// result does not depend on which piece finished last.
+//
+// A CTA's steps run through one pipeline: the next unit's Q is loaded into the second
+// Q buffer while the current unit finishes, and its first S = Q K^T is issued right
+// after the last P V.
 // Per CTA, 12 warps:
 //   warps 0-3 / 4-7  softmax of query tile 0 / 1 (thread = query row = TMEM lane):
 //                    read S_t from TMEM, write fp16 P_t back to TMEM.
@@ -27,22 +29,32 @@
 //                    from the fresh or the stale tensor map -- the splice.
 //   warp 9           MMA issuer (one thread) and TMEM owner.  Per key tile j and
 //                    query tile t, once softmax t has written P_t(j):
+//                    S_t = Q_t K(j+1)^T (M=128, N=128, K=16 steps over d=64), then
 //                    O_t += P_t(j) V(j) (M=128, N=64, K=16 steps over keys, P from
-//                    TMEM), then S_t = Q_t K(j+1)^T (M=128, N=128, K=16 steps over
-//                    d=64).  The two query tiles alternate, so the tensor pipe works
-//                    on one tile while the other's softmax runs; and because the
-//                    tensor pipe completes one thread's MMAs in order, "S_t(j+1)
-//                    ready" also means P_t(j) and O_t are free again.
-//   warps 10-11      idle (they keep the warpgroup whole for the register split).
-// Each softmax warp also widens a 1/8 share of the next V tile from bf16 to fp16 in
-// place, one key tile ahead, so that this work is spread evenly over the four SM
-// quarters instead of slowing the softmax warps that share a quarter with helpers.
-// P is rounded to fp16, not bf16: its 11-bit significand keeps the rounding of
-// the probabilities well inside the 2e-3 output tolerance (bf16's 8 bits would
-// not), and V is widened to fp16 exactly so that P V runs as kind::f16 with
-// both operands fp16 (|V| must stay below 65504).
-// Online softmax in the log2 domain with a lazily moved reference maximum: the
-// running O is rescaled only when a row's maximum grows by more than 2^8.
+//                    TMEM), each with its own commit.  The scores come first because the
+//                    softmax waits for them, while P V only has to finish before the next
+//                    P store; the two query tiles alternate, so the tensor pipe works on
+//                    one tile while the other's softmax runs (one batch for both tiles
+//                    after both P were written measured slower: the two softmaxes then
+//                    run in step and contend for the exponential unit).  All MMAs of the
+//                    CTA come from this one thread: issuing tcgen05.mma from two warps of
+//                    one CTA at once faulted the GPU (an illegal memory access) in two
+//                    independent implementations.
+//   warps 10-11      widen each landed V tile from bf16 to fp16 in place (half a tile
+//                    each), times the (batch, head) power of two; the MMA thread waits
+//                    for this before P V.
+// P is rounded to fp16, not bf16: its 11-bit significand keeps the rounding of the
+// probabilities well inside the 2e-3 output tolerance (bf16's 8 bits would not), and
+// V is widened to fp16 so that P V runs as kind::f16 with both operands fp16.  fp16
+// covers [2^-14, 65504] at full precision; V is brought into that range by a power of
+// two 2^e per (batch, head), found by a small pass over the fresh and stale V before
+// the kernel (e = 0 when max|V| lies in [2^-6, 2^15), the usual case), applied in the
+// widening and removed again from O in the epilogue.
+// Online softmax in the log2 domain with a lazily moved reference maximum: the row
+// maximum of a unit's first key tile is the reference, later tiles are exponentiated
+// against it without a maximum pass, and the reference moves (O and l rescaled, P
+// recomputed from the scores still in TMEM) only for a row whose tile sum of P reaches
+// 2^15, before any P could exceed fp16's range.
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
@@ -63,7 +75,7 @@ constexpr int KT = 128;                 // keys per tile
 constexpr int KV_STAGES = 5;
 constexpr int TILE_BYTES = KT * D * 2;  // 16 KB (K or V tile, Q tile)
 constexpr int ATTN_THREADS = 384;
-constexpr int NUM_CONVERTERS = 8;       // the softmax warps, a 1/8 share each
+constexpr int NUM_CONVERTERS = 2;       // warps 10 and 11, half a V tile each
 // smem: two Q buffers (Q0 Q1 each) | (K V) x stages | barriers.  TMEM (512 columns):
 // S0 S1 (128 each), O0 O1 (64 each), P0 P1 (64 each: 128 fp16 probabilities per row,
 // two per column).
@@ -73,7 +85,9 @@ constexpr int OFF_BAR = OFF_KV + KV_STAGES * 2 * TILE_BYTES;
 constexpr int ATTN_SMEM = OFF_BAR + 512 + 1024;
 static_assert(ATTN_SMEM <= 227 * 1024, "shared memory per CTA");
 constexpr float kScaleLog2 = 0.18033688011112042f;  // log2(e) / sqrt(64)
-constexpr float kRescaleThreshold = 8.0f;           // log2 units
+// A key tile whose probabilities (against the row's reference maximum) sum to 2^15 or
+// more moves the reference: below that every P < 2^15 fits fp16 (max 65504).
+constexpr float kRefSum = 32768.0f;
 // Partial result of one piece of a cut unit: O/l as fp16 [2 tiles][128 rows][64],
 // then the reference maximum m (log2 units) and the sum l, fp32 [2][128] each.
 constexpr int REC_M = 2 * QT * D * 2;
@@ -90,14 +104,17 @@ struct AttnArgs {
   long long tailT;  // split: their (unit, key tile) steps
   __nv_bfloat16* o;
   uint8_t* part;    // split: G + (U - W*G) partial records
+  const unsigned* vmax;  // [B*heads] fp32 bits of max |V| over the fresh and stale V
   int* status;
   long long wait_limit;
+  int skip_load;    // test hook: the producer never loads the K/V tile of this step (-1)
 };
 
 struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[KV_STAGES], v_full[KV_STAGES], v_conv[KV_STAGES], kv_empty[KV_STAGES];
-  uint64_t s_full[2], p_full[2], o_done[2], drain;
+  uint64_t s_full[2], p_full[2], pv_done[2], drain;
+  uint64_t rec_done[2], merge_go[2];  // per tile: a cut unit's record written / merge decided
   uint32_t tmem_slot;
   int abort_flag;
   int merge_from[2];  // per query tile: first CTA of the unit to merge, or -1
@@ -180,6 +197,20 @@ __host__ __device__ __forceinline__ UnitPos unit_pos(int u, const AttnArgs& a) {
   return x;
 }
 
+// The power of two 2^e that brings V of (batch b, head h) into fp16's full-precision
+// range: e = 0 when max|V| lies in [2^-6, 2^15); otherwise 14 - floor(log2 max|V|), so
+// that the scaled maximum lies in [2^14, 2^15), clamped to [-125, 125] (only |V| below
+// 2^-111 then keeps some fp16 subnormals).  An all-zero V gets 0.
+__device__ __forceinline__ int v_exponent(const AttnArgs& a, int b, int h) {
+  const unsigned bits = __ldg(a.vmax + b * a.heads + h);
+  const float amax = __uint_as_float(bits);
+  if (bits == 0 || (amax >= 0.015625f && amax < 32768.0f)) return 0;
+  const int E = (int)(bits >> 23) - 127;  // floor(log2 amax); a subnormal amax gives -127
+  return max(-125, min(125, 14 - E));
+}
+
+__device__ __forceinline__ float pow2(int e) { return __int_as_float((e + 127) << 23); }
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -225,10 +256,11 @@ __device__ __forceinline__ void store_f16x16(uint4* d4, const uint32_t (&o)[16],
 
 // Merges the pieces of tail unit ut for row r of query tile t: records of CTAs
 // ca..cb (those with a non-empty run), in that order.  With pieces i = (m_i, l_i,
-// O_i/l_i): M = max m_i, w_i = l_i 2^(m_i - M), o = sum_i w_i (O_i/l_i) / sum_i w_i.
+// O_i/l_i): M = max m_i, w_i = l_i 2^(m_i - M), o = sum_i w_i (O_i/l_i) / sum_i w_i,
+// times 2^-e (the records hold O in V's scaled units).
 // The records were written by other SMs: read through L2 (ld.global.cg).
 __device__ __forceinline__ void merge_rows(const AttnArgs& a, int ut, int t, int r, int ca, int cb,
-                                           const UnitPos& up) {
+                                           const UnitPos& up, int e) {
   const long long s_a = (long long)ut * a.nkt;
   auto record = [&](int c, long long b0) -> const uint8_t* {
     // a CTA's first tail segment, or the last one of the CTA that started before the unit
@@ -259,10 +291,10 @@ __device__ __forceinline__ void merge_rows(const AttnArgs& a, int ut, int t, int
     for (int q = 0; q < D / 8; ++q) {
       const uint32_t hw[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[e]));
-        acc[8 * q + 2 * e] = fmaf(w, f.x, acc[8 * q + 2 * e]);
-        acc[8 * q + 2 * e + 1] = fmaf(w, f.y, acc[8 * q + 2 * e + 1]);
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[k]));
+        acc[8 * q + 2 * k] = fmaf(w, f.x, acc[8 * q + 2 * k]);
+        acc[8 * q + 2 * k + 1] = fmaf(w, f.y, acc[8 * q + 2 * k + 1]);
       }
     }
   }
@@ -270,7 +302,7 @@ __device__ __forceinline__ void merge_rows(const AttnArgs& a, int ut, int t, int
   if (row_in_patch >= a.Lp) return;
   __nv_bfloat16* dst =
       a.o + ((long long)up.b * a.L + up.patch0 + row_in_patch) * (long long)(a.heads * D) + up.h * D;
-  const float inv = 1.f / wsum;
+  const float inv = pow2(-e) / wsum;
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int q = 0; q < D / 8; ++q)
@@ -278,6 +310,120 @@ __device__ __forceinline__ void merge_rows(const AttnArgs& a, int ut, int t, int
                        pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
                        pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv),
                        pack_bf16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
+}
+
+// Row maximum of a thread's 128 raw scores (four independent max3 chains).
+__device__ __forceinline__ float row_max(const uint32_t (&sv)[128]) {
+  float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 128; i += 8) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      mq[u] = ptx::max3(mq[u], __uint_as_float(sv[i + 2 * u]), __uint_as_float(sv[i + 2 * u + 1]));
+  }
+  return ptx::max3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+}
+
+// p = 2^(s log2(e)/sqrt(64) - m_ref) for the 128 scores, as fp16 pairs (column c holds keys
+// 2c in the low half and 2c+1 in the high half); pairs of keys in packed fp32x2 (one FMA
+// and one add per two keys).  Returns the fp32 sum of the p.
+__device__ __forceinline__ float exp_tile(const uint32_t (&sv)[128], float m_ref,
+                                          uint32_t (&pk)[64]) {
+  const uint64_t c2 = ptx::pack_f32x2(kScaleLog2, kScaleLog2);
+  const uint64_t nm2 = ptx::pack_f32x2(-m_ref, -m_ref);
+  uint64_t lq[2] = {ptx::pack_f32x2(0.f, 0.f), ptx::pack_f32x2(0.f, 0.f)};
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const uint64_t s2 = ptx::pack_f32x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+    float a0, a1;
+    ptx::unpack_f32x2(ptx::fma_f32x2(s2, c2, nm2), a0, a1);
+    const float p0 = ex2(a0), p1 = ex2(a1);
+    lq[i & 1] = ptx::add_f32x2(lq[i & 1], ptx::pack_f32x2(p0, p1));
+    pk[i] = pack_f16x2(p0, p1);
+  }
+  float x0, x1, y0, y1;
+  ptx::unpack_f32x2(lq[0], x0, x1);
+  ptx::unpack_f32x2(lq[1], y0, y1);
+  return (x0 + x1) + (y0 + y1);
+}
+
+// The row maximum re-read from the scores in TMEM, 32 columns at a time (keys >= nvalid
+// excluded).  Warp-collective.
+__device__ __forceinline__ float tile_max(uint32_t t_row, int nvalid) {
+  float m = -INFINITY;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t x[32];
+    ptx::tmem_ld32(t_row + c * 32, x);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (c * 32 + i < nvalid) m = fmaxf(m, __uint_as_float(x[i]));
+  }
+  return m;
+}
+
+// exp_tile from the scores in TMEM, written straight to P in TMEM, 32 keys at a time;
+// returns the sum.  Warp-collective.
+__device__ __forceinline__ float exp_store(uint32_t s_row, uint32_t p_row, int nvalid,
+                                           float m_ref) {
+  float sum = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t x[32], pk[16];
+    ptx::tmem_ld32(s_row + c * 32, x);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float s0 = c * 32 + 2 * i < nvalid ? __uint_as_float(x[2 * i]) : -INFINITY;
+      const float s1 = c * 32 + 2 * i + 1 < nvalid ? __uint_as_float(x[2 * i + 1]) : -INFINITY;
+      const float p0 = ex2(fmaf(s0, kScaleLog2, -m_ref)), p1 = ex2(fmaf(s1, kScaleLog2, -m_ref));
+      sum += p0 + p1;
+      pk[i] = pack_f16x2(p0, p1);
+    }
+    ptx::tmem_st16(p_row + c * 16, pk);
+  }
+  return sum;
+}
+
+// max |V| of each (batch, head) over the fresh V and, when P > 1, the stale V (every
+// row of both is read by some patch); the result goes to vmax (zero before the launch)
+// as fp32 bits through atomicMax, which orders non-negative floats like their bits.
+// Grid (chunks, heads, B); a warp reads four 128-byte head rows per load.
+__global__ void __launch_bounds__(256) vrange_kernel(const __nv_bfloat16* vf,
+                                                     const __nv_bfloat16* vs, int L, int heads,
+                                                     int rows_per_block, int use_stale,
+                                                     unsigned* vmax) {
+  __shared__ unsigned red[8];
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long C = (long long)heads * D;
+  const int r0 = blockIdx.x * rows_per_block;
+  const int r1 = min(L, r0 + rows_per_block);
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  unsigned m = 0;
+  for (int r = r0 + warp * 4 + (lane >> 3); r < r1; r += 32) {
+    const long long off = ((long long)b * L + r) * C + h * D + (lane & 7) * 8;
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(vf + off));
+    unsigned w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m = max(m, max(w4[k] & 0x7FFFu, (w4[k] >> 16) & 0x7FFFu));
+    if (use_stale) {
+      u = __ldg(reinterpret_cast<const uint4*>(vs + off));
+      const unsigned s4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m = max(m, max(s4[k] & 0x7FFFu, (s4[k] >> 16) & 0x7FFFu));
+    }
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = max(m, red[i]);
+    if (m) atomicMax(vmax + b * heads + h, m << 16);  // bf16 bits -> fp32 bits
+  }
 }
 
 __global__ void __launch_bounds__(ATTN_THREADS, 1)
@@ -304,7 +450,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(&bars->s_full[t], 1);
       ptx::mbar_init(&bars->p_full[t], 4);  // one arrival per softmax warp
-      ptx::mbar_init(&bars->o_done[t], 1);  // committed after a segment's last P V
+      ptx::mbar_init(&bars->pv_done[t], 1);  // committed after each P V
+      ptx::mbar_init(&bars->rec_done[t], 4);  // one arrival per softmax warp
+      ptx::mbar_init(&bars->merge_go[t], 1);  // the warpgroup's deciding thread
     }
     ptx::mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -358,6 +506,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
               ok = false;
               break;
             }
+            ++issued;
+            if (v == a.skip_load) continue;  // test hook: this step's K and V never land
             uint8_t* kdst = smem + OFF_KV + st * 2 * TILE_BYTES;
             uint8_t* vdst = kdst + TILE_BYTES;
             ptx::mbar_arrive_expect_tx(&bars->k_full[st], TILE_BYTES);
@@ -374,16 +524,17 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
               ptx::tma_load_3d(vdst + i * a.g * 128, fresh ? &tmVf : &tmVs, &bars->v_full[st],
                                up.h * D, row, up.b);
             }
-            ++issued;
           }
         }
-        if (bars->abort_flag) {  // wait for own copies in flight before exiting
-          // a Q load is issued only after the MMAs of the unit two before it have
-          // completed, so only the last two can still be in flight
+        if (*reinterpret_cast<volatile int*>(&bars->abort_flag)) {
+          // wait for own copies in flight before exiting: a Q load is issued only after
+          // the MMAs of the unit two before it have completed, so only the last two can
+          // still be in flight
           for (int n = q_issued > 2 ? q_issued - 2 : 0; n < q_issued; ++n)
             ptx::mbar_wait(&bars->q_full[n & 1], (n >> 1) & 1, kDrainWaitLimit, nullptr);
           const int first = issued > KV_STAGES ? issued - KV_STAGES : 0;
           for (int j = first; j < issued; ++j) {
+            if (j == a.skip_load) continue;
             ptx::mbar_wait(&bars->k_full[j % KV_STAGES], (j / KV_STAGES) & 1, kDrainWaitLimit,
                            nullptr);
             ptx::mbar_wait(&bars->v_full[j % KV_STAGES], (j / KV_STAGES) & 1, kDrainWaitLimit,
@@ -447,10 +598,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
               }
               ptx::tc_fence_after();
               const uint32_t tO = tmem + 256u + 64u * t, tP = tmem + 384u + 64u * t;
-#pragma unroll
-              for (int k = 0; k < KT / 16; ++k)  // O_t += P_t(v) V(v)
-                ptx::mma_ts(tO, tP + k * 8, vd + 128 * k, idesc_pv, k ? 1u : acc0);
-              if (last) ptx::mma_commit(&bars->o_done[t]);
+              // The next scores first: the softmax of tile t waits for them, while P V
+              // is needed only before its next P store.  Two independent accumulator
+              // chains in flight also keep the tensor pipe busier than one after the
+              // other (measured: 720 vs 865 cycles for one tile's batch).
               if (more) {  // S_t = Q_t K(v+1)^T, Q of the unit of step v+1
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
@@ -458,6 +609,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
                               k ? 1u : 0u);
                 ptx::mma_commit(&bars->s_full[t]);
               }
+#pragma unroll
+              for (int k = 0; k < KT / 16; ++k)  // O_t += P_t(v) V(v)
+                ptx::mma_ts(tO, tP + k * 8, vd + 128 * k, idesc_pv, k ? 1u : acc0);
+              ptx::mma_commit(&bars->pv_done[t]);
             }
             if (!ok) break;
             ptx::mma_commit(&bars->kv_empty[st]);
@@ -470,8 +625,48 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           ptx::mbar_wait(&bars->drain, 0, kDrainWaitLimit, nullptr);
         }
       }
+    } else if (warp >= 10) {
+      // ------------------------------------------------ V widening (warps 10, 11)
+      // Each landed V tile: this warp's half, 16 KB / 2 / 32 lanes = 16 vectors per lane,
+      // in two passes of 8, bf16 -> fp16 times 2^e (exact: a power of two, and fp16 holds
+      // every bf16 value of the scaled range).  The MMA thread issues P V only after both
+      // halves are done (v_conv).
+      const int half = warp - 10;
+      bool ok = true;
+      for (int v = 0; v < sc.nsteps && ok;) {
+        const Seg sg = seg_at(sc, v, a);
+        const UnitPos up = unit_pos(sg.u, a);
+        const int e = v_exponent(a, up.b, up.h);
+        const float scale = pow2(e);
+        for (const int vend = v + sg.len; v < vend; ++v) {
+          const int st = v % KV_STAGES;
+          if (!wait_or_abort(&bars->v_full[st], (v / KV_STAGES) & 1, a, bars)) {
+            ok = false;
+            break;
+          }
+          uint4* vt = reinterpret_cast<uint4*>(smem + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES) +
+                      half * (TILE_BYTES / 16 / NUM_CONVERTERS);
+#pragma unroll 1
+          for (int pass = 0; pass < 2; ++pass) {
+            uint4 u[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) u[i] = vt[lane + 32 * (8 * pass + i)];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                w[k] = pack_f16x2(__uint_as_float(w[k] << 16) * scale,
+                                  __uint_as_float(w[k] & 0xFFFF0000u) * scale);
+              vt[lane + 32 * (8 * pass + i)] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&bars->v_conv[st]);
+        }
+      }
     }
-    // warps 10-11: nothing to do
   } else {
     ptx::regs_inc<208>();
     // ------------------------------------------------------------ softmax (warps 0-7)
@@ -482,44 +677,18 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     const uint32_t tS = tmem + 128u * (uint32_t)t;        // S_t: 128 columns
     const uint32_t tO = tmem + 256u + 64u * (uint32_t)t;  // O_t: 64 columns
     const uint32_t tP = tmem + 384u + 64u * (uint32_t)t;  // P_t: 64 columns
-    // Widens this warp's 1/8 share of the V tile of step vv in place once it has landed.
-    auto convert_share = [&](int vv) -> bool {
-      const int st = vv % KV_STAGES;
-      const uint32_t par = (vv / KV_STAGES) & 1;
-      // lane 0 sleeps on the barrier; then every lane observes the completed phase
-      // (returns at once) so that all lanes see the landed tile
-      int okw = 1;
-      if (lane == 0) okw = wait_or_abort(&bars->v_full[st], par, a, bars);
-      if (!__shfl_sync(0xffffffffu, okw, 0)) return false;
-      if (!wait_or_abort(&bars->v_full[st], par, a, bars)) return false;
-      uint4* v = reinterpret_cast<uint4*>(smem + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES) +
-                 warp * (TILE_BYTES / 16 / NUM_CONVERTERS);
-      uint4 u[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) u[i] = v[lane + 32 * i];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          w[e] = pack_f16x2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
-        v[lane + 32 * i] = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars->v_conv[st]);
-      return true;
-    };
-    bool ok = sc.nsteps == 0 || convert_share(0);
+    bool ok = true;
     bool tail_seen = false;  // a tail segment of this CTA has ended
+    uint32_t pieces = 0;     // pieces of cut units this warpgroup has recorded
     for (int v = 0, n = 0; v < sc.nsteps && ok; ++n) {
       const Seg sg = seg_at(sc, v, a);
       const int vbeg = v, vend = v + sg.len;
+      const UnitPos up = unit_pos(sg.u, a);
+      const int e_cur = v_exponent(a, up.b, up.h);
       float m_ref = -INFINITY, l = 0.f;
       for (int j = sg.j0; v < vend; ++v, ++j) {
-        if (v + 1 < sc.nsteps && !convert_share(v + 1)) { ok = false; break; }
-        // S_t(v) ready; the MMA thread issued it after P_t(v-1) V(v-1), so that
-        // product has completed too: P_t and O_t may be touched.
+        // S_t(v) ready (the MMA thread issues it before P_t(v-1) V(v-1), which may still
+        // be running: P_t and O_t are touched only after pv_done below)
         if (!wait_or_abort(&bars->s_full[t], v & 1, a, bars)) { ok = false; break; }
         ptx::tc_fence_after();
         uint32_t sv[128];
@@ -533,24 +702,35 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           for (int i = 0; i < 128; ++i)
             if (i >= nvalid) sv[i] = __float_as_uint(-INFINITY);
         }
-        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 independent chains
-#pragma unroll
-        for (int i = 0; i < 128; i += 8) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            mq[u] = ptx::max3(mq[u], __uint_as_float(sv[i + 2 * u]),
-                              __uint_as_float(sv[i + 2 * u + 1]));
+        // The reference maximum m_ref (log2 units) is the row maximum of the segment's
+        // first key tile; later tiles are exponentiated against it directly, and only a
+        // row whose tile sum reaches 2^15 (so that some P might come near fp16's 65504, or
+        // overflow) takes its true maximum as the new reference: then O and l are
+        // rescaled and that warp recomputes its P from the scores still in TMEM.
+        if (v == vbeg) {
+          m_ref = row_max(sv) * kScaleLog2;
+          l = 0.f;
         }
-        const float mx = ptx::max3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
-        const float m_new = mx * kScaleLog2;
-        const bool resc = m_new > m_ref + kRescaleThreshold;
+        uint32_t pk[64];
+        float s_step = exp_tile(sv, m_ref, pk);
+        const bool big = v > vbeg && !(s_step < kRefSum);
+        const bool redo = __any_sync(0xffffffffu, big);
         float alpha = 1.f;
-        if (resc) {
-          alpha = ex2(m_ref - m_new);  // 0 on the first tile of a segment
-          m_ref = m_new;
-          l *= alpha;
+        if (redo) {  // rare
+          const float m_new = fmaxf(tile_max(tS + lane_off, nvalid) * kScaleLog2, m_ref);
+          if (big) {
+            alpha = ex2(m_ref - m_new);
+            m_ref = m_new;
+            l *= alpha;
+          }
         }
-        if (v > vbeg && __any_sync(0xffffffffu, resc)) {  // rescale the running O_t
+        // P_t and O_t are free once P_t(v-1) V(v-1) has completed
+        if (v > 0 && !wait_or_abort(&bars->pv_done[t], (v - 1) & 1, a, bars)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        if (redo) {  // rescale the running O_t, then P from the scores in TMEM
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t o[16];
@@ -560,34 +740,13 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
             for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
             ptx::tmem_st16(tO + lane_off + c * 16, o);
           }
-        }
-        // exponentials 32 keys at a time, stored at once as fp16 P into TMEM (column c
-        // holds keys 2c in the low half and 2c+1 in the high half)
-        // pairs of keys in packed fp32x2: one FMA and one add per two keys
-        const uint64_t c2 = ptx::pack_f32x2(kScaleLog2, kScaleLog2);
-        const uint64_t nm2 = ptx::pack_f32x2(-m_ref, -m_ref);
-        uint64_t lq[2] = {ptx::pack_f32x2(0.f, 0.f), ptx::pack_f32x2(0.f, 0.f)};  // row sums
+          s_step = exp_store(tS + lane_off, tP + lane_off, nvalid, m_ref);
+        } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint64_t s2 = ptx::pack_f32x2(__uint_as_float(sv[32 * c + 2 * i]),
-                                                __uint_as_float(sv[32 * c + 2 * i + 1]));
-            float a0, a1;
-            ptx::unpack_f32x2(ptx::fma_f32x2(s2, c2, nm2), a0, a1);
-            const float p0 = ex2(a0), p1 = ex2(a1);
-            lq[i & 1] = ptx::add_f32x2(lq[i & 1], ptx::pack_f32x2(p0, p1));
-            pk[i] = pack_f16x2(p0, p1);
-          }
-          ptx::tmem_st16(tP + lane_off + 16 * c, pk);
+          for (int c = 0; c < 4; ++c)
+            ptx::tmem_st16(tP + lane_off + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
         }
-        {
-          float x0, x1, y0, y1;
-          ptx::unpack_f32x2(lq[0], x0, x1);
-          ptx::unpack_f32x2(lq[1], y0, y1);
-          l += (x0 + x1) + (y0 + y1);
-        }
+        l += s_step;
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
@@ -595,11 +754,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       }
       if (!ok) break;
       // ---- end of the segment: O_t complete once its last P V has finished
-      if (!wait_or_abort(&bars->o_done[t], n & 1, a, bars)) { ok = false; break; }
+      if (!wait_or_abort(&bars->pv_done[t], (vend - 1) & 1, a, bars)) { ok = false; break; }
       ptx::tc_fence_after();
-      const UnitPos up = unit_pos(sg.u, a);
-      const float inv = 1.f / l;
       if (sg.j0 == 0 && sg.len == a.nkt) {  // whole unit: normalised bf16 output
+        const float inv = pow2(-e_cur) / l;
         const int row_in_patch = up.q0 + t * QT + r;
         const bool valid = row_in_patch < a.Lp;
         __nv_bfloat16* dst = a.o + ((long long)up.b * a.L + up.patch0 + row_in_patch) *
@@ -611,7 +769,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           ptx::tmem_ld_wait();
           if (valid) store_bf16x16(dst + c * 16, o, inv);
         }
-      } else {  // one piece of a cut unit: O/l in fp16, m and l in fp32
+      } else {  // one piece of a cut unit: O/l in fp16 (V's scaled units), m and l in fp32
+        const float inv = 1.f / l;
         const int ut = sg.u - a.W * a.G;
         const int rec = tail_seen ? a.G + ut : (int)blockIdx.x;
         uint8_t* base = a.part + (size_t)rec * REC_BYTES;
@@ -626,23 +785,34 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         reinterpret_cast<float*>(base + REC_M)[t * QT + r] = m_ref;
         reinterpret_cast<float*>(base + REC_L)[t * QT + r] = l;
         // The last piece of the unit to finish (for this query tile) merges them all.
+        // The hand-offs are mbarriers with bounded waits, so that a warp that gave up
+        // cannot leave the others waiting.
         __threadfence();
-        ptx::named_bar_sync(1 + t, 128);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->rec_done[t]);
         if (quarter == 0 && lane == 0) {
-          const long long s_a = (long long)ut * a.nkt;
-          const int ca = tail_cta(s_a, a), cb = tail_cta(s_a + a.nkt - 1, a);
-          int np = 0;
-          for (int c = ca; c <= cb; ++c) np += tail_bound(c, a) != tail_bound(c + 1, a);
-          const bool last = atomicAdd(&a.cnt[2 * ut + t], 1) == np - 1;
-          if (last) atomicExch(&a.cnt[2 * ut + t], 0);  // all arrived: ready for the next call
-          bars->merge_from[t] = last ? ca : -1;
-          bars->merge_to[t] = cb;
+          int from = -1, to = 0;
+          if (wait_or_abort(&bars->rec_done[t], pieces & 1, a, bars)) {
+            __threadfence();
+            const long long s_a = (long long)ut * a.nkt;
+            const int ca = tail_cta(s_a, a), cb = tail_cta(s_a + a.nkt - 1, a);
+            int np = 0;
+            for (int c = ca; c <= cb; ++c) np += tail_bound(c, a) != tail_bound(c + 1, a);
+            const bool last = atomicAdd(&a.cnt[2 * ut + t], 1) == np - 1;
+            if (last) atomicExch(&a.cnt[2 * ut + t], 0);  // all arrived: ready for the next call
+            from = last ? ca : -1;
+            to = cb;
+          }
+          bars->merge_from[t] = from;
+          bars->merge_to[t] = to;
+          ptx::mbar_arrive(&bars->merge_go[t]);
         }
-        ptx::named_bar_sync(1 + t, 128);
+        if (!wait_or_abort(&bars->merge_go[t], pieces & 1, a, bars)) { ok = false; break; }
+        ++pieces;
         const int ca = bars->merge_from[t], cb = bars->merge_to[t];
         if (ca >= 0) {
           __threadfence();
-          merge_rows(a, ut, t, r, ca, cb, up);
+          merge_rows(a, ut, t, r, ca, cb, up, e_cur);
         }
       }
       if (sg.tail) tail_seen = true;
@@ -711,36 +881,46 @@ bool plan(int B, int L, int heads, int P, bool split, AttnArgs* a) {
   } else {
     a->G = (int)(U < sms ? U : sms);
   }
+  a->skip_load = -1;
   return true;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// The scratch buffer: the per-(batch, head) maxima of |V|, then (split schedule) the
+// per-(tail unit, query tile) counters and the partial records.  The maxima and the
+// counters must be zero when a launch starts.
+size_t vmax_bytes(int B, int heads) { return align256((size_t)B * heads * sizeof(unsigned)); }
+size_t counter_bytes(const AttnArgs& a) {
+  return a.split ? align256((size_t)2 * (a.U - a.W * a.G) * sizeof(int)) : 0;
+}
+size_t record_bytes(const AttnArgs& a) {
+  return a.split ? (size_t)(a.G + (a.U - a.W * a.G)) * REC_BYTES : 0;
 }
 
 }  // namespace
 
-// The partials buffer: the per-(tail unit, query tile) counters, then the records.
-static size_t counter_bytes(const AttnArgs& a) {
-  return ((size_t)2 * (a.U - a.W * a.G) * sizeof(int) + 255) / 256 * 256;
+size_t tc_attention_scratch_bytes(int B, int L, int heads, int P, bool split) {
+  AttnArgs a;
+  if (!plan(B, L, heads, P, split, &a)) return 0;
+  return vmax_bytes(B, heads) + counter_bytes(a) + record_bytes(a);
 }
 
-size_t tc_attention_partial_bytes(int B, int L, int heads, int P) {
+int tc_attention_zero_ints(int B, int L, int heads, int P, bool split) {
   AttnArgs a;
-  if (!plan(B, L, heads, P, true, &a) || !a.split) return 0;
-  return counter_bytes(a) + (size_t)(a.G + (a.U - a.W * a.G)) * REC_BYTES;
-}
-
-int tc_attention_counters(int B, int L, int heads, int P) {
-  AttnArgs a;
-  if (!plan(B, L, heads, P, true, &a) || !a.split) return 0;
-  return 2 * (a.U - a.W * a.G);
+  if (!plan(B, L, heads, P, split, &a)) return 0;
+  return (int)((vmax_bytes(B, heads) + counter_bytes(a)) / sizeof(int));
 }
 
 int launch_tc_attention(const void* q, const void* kf, const void* vf, const void* ks,
-                        const void* vs, void* o, int B, int L, int heads, int P, void* partials,
-                        size_t partial_bytes, bool counters_zeroed, int* status,
-                        long long wait_limit, cudaStream_t s) {
+                        const void* vs, void* o, int B, int L, int heads, int P, bool split,
+                        void* scratch, size_t scratch_bytes, bool scratch_zeroed,
+                        bool vmax_ready, int* status, long long wait_limit, int skip_load,
+                        cudaStream_t s) {
   AttnArgs a;
-  if (!plan(B, L, heads, P, partials != nullptr, &a)) return DPP_ERR_SHAPE;
-  if (a.split && partial_bytes < counter_bytes(a) + (size_t)(a.G + (a.U - a.W * a.G)) * REC_BYTES)
-    return DPP_ERR_ARG;
+  if (!plan(B, L, heads, P, split, &a)) return DPP_ERR_SHAPE;
+  const size_t vb = vmax_bytes(B, heads), cb = counter_bytes(a);
+  if (!scratch || scratch_bytes < vb + cb + record_bytes(a)) return DPP_ERR_ARG;
   const int C = heads * D;
   int rc = set_attn_smem();
   if (rc) return rc;
@@ -750,16 +930,32 @@ int launch_tc_attention(const void* q, const void* kf, const void* vf, const voi
       !make_map3(&mvs, vs, L, B, C, a.g))
     return DPP_ERR_CUDA;
   a.o = static_cast<__nv_bfloat16*>(o);
+  unsigned* vmax = static_cast<unsigned*>(scratch);
+  a.vmax = vmax;
   if (a.split) {
-    a.cnt = static_cast<int*>(partials);
-    a.part = static_cast<uint8_t*>(partials) + counter_bytes(a);
-    if (!counters_zeroed && cudaMemsetAsync(a.cnt, 0, counter_bytes(a), s) != cudaSuccess)
-      return DPP_ERR_CUDA;
+    a.cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(scratch) + vb);
+    a.part = static_cast<uint8_t*>(scratch) + vb + cb;
   }
+  if (!scratch_zeroed && cudaMemsetAsync(scratch, 0, vb + cb, s) != cudaSuccess)
+    return DPP_ERR_CUDA;
   a.status = status;
   a.wait_limit = wait_limit;
-  const cudaError_t e = dpp_host::launch_pdl(tc_attn_kernel, dim3(a.G), dim3(ATTN_THREADS),
-                                             ATTN_SMEM, s, mq, mkf, mks, mvf, mvs, a);
+  a.skip_load = skip_load;
+  // max |V| per (batch, head): about 2.5 blocks of 256 per SM
+  const int want = 2 * dpp_host::sm_count() * 5 / 2 / (B * heads);
+  const int chunks = want < 1 ? 1 : want;
+  int rows = (L + chunks - 1) / chunks;
+  rows = (rows + 31) / 32 * 32;
+  const dim3 vgrid((unsigned)((L + rows - 1) / rows), (unsigned)heads, (unsigned)B);
+  cudaError_t e = cudaSuccess;
+  if (!vmax_ready)
+    e = dpp_host::launch_pdl(vrange_kernel, vgrid, dim3(256), 0, s,
+                             static_cast<const __nv_bfloat16*>(vf),
+                             static_cast<const __nv_bfloat16*>(vs), L, heads, rows,
+                             P > 1 && vs != vf ? 1 : 0, vmax);
+  if (e != cudaSuccess) return DPP_ERR_CUDA;
+  e = dpp_host::launch_pdl(tc_attn_kernel, dim3(a.G), dim3(ATTN_THREADS), ATTN_SMEM, s, mq, mkf,
+                           mks, mvf, mvs, a);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
 

@@ -64,6 +64,7 @@ struct GemmArgs {
   int ncols;
   int* status;
   long long wait_limit;
+  long long skip_load;  // test hook: the producer never loads this K slice (-1: none)
   // implicit conv
   int H, W, Cin, Hp, cin_blocks, boxes, box_px;
   // conv with GroupNorm applied to the in-band rows of A (raw x): [B][P][3][Cin] fp32
@@ -77,6 +78,10 @@ struct GemmArgs {
   void* rfx_out[2];
   int8_t* rfx_codes[2];
   float* rfx_scales[2];
+  // linear with a three-way split output: max |out| of the third output (V) per (batch of
+  // vmax_L rows, 64-column head) into vmax as fp32 bits by atomicMax, or NULL
+  unsigned* vmax;
+  int vmax_L, vmax_heads;
 };
 
 // What the producer fetched into a stage, for the GroupNorm warps: the boxes' first
@@ -263,6 +268,7 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
             ok = false;
             break;
           }
+          if (g == args.skip_load) continue;  // test hook: this slice never lands
           uint8_t* a_dst = smem + s * C::STAGE_BYTES;
           uint8_t* b_dst = a_dst + C::A_BYTES;
           if (GNF) {  // the note first: the arrive below releases it to the waiters
@@ -318,8 +324,9 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
       if (*abort_flag) {  // wait for own copies still in flight before the CTA may exit
         const long long first = g > STAGES ? g - STAGES : 0;
         for (long long q = first; q < g; ++q)
-          ptx::mbar_wait(&full[q % STAGES], (uint32_t)((q / STAGES) & 1), kDrainWaitLimit,
-                         nullptr);
+          if (q != args.skip_load)
+            ptx::mbar_wait(&full[q % STAGES], (uint32_t)((q / STAGES) & 1), kDrainWaitLimit,
+                           nullptr);
       }
     }
   } else if (warp == 1) {
@@ -492,6 +499,21 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
 #pragma unroll
           for (int i = 0; i < 4; ++i) d4[i] = pk[i];
         }
+        if (!CONV && which == 2 && args.vmax) {  // max |V| of these 32 columns (one head)
+          uint32_t m = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t w4[4] = {pk[i].x, pk[i].y, pk[i].z, pk[i].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) m = max(m, max(w4[e] & 0x7FFFu, (w4[e] >> 16) & 0x7FFFu));
+          }
+          m = __reduce_max_sync(0xffffffffu, row < args.M ? m : 0u);
+          if (lane == 0 && m) {  // the warp's 32 rows lie in one batch (L % 128 == 0)
+            const long long r0 = (long long)mt * BM + quarter * 32;
+            atomicMax(args.vmax + (r0 / args.vmax_L) * args.vmax_heads + (col0 + ch * 32) / 64,
+                      m << 16);
+          }
+        }
       }
       // accumulator drained: the MMA warp may reuse it
       ptx::tc_fence_before();
@@ -617,7 +639,8 @@ bool tc_conv_gn_supported(int H, int W, int P) {
 }
 
 int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2, long long M,
-                     int N, int K, int* status, long long wait_limit, cudaStream_t s) {
+                     int N, int K, int* status, long long wait_limit, cudaStream_t s,
+                     unsigned* vmax, int vmax_L, int vmax_heads) {
   if (M % BM || N % 128 || K % BK) return DPP_ERR_SHAPE;
   const int ncols = o1 ? N / 3 : N;
   const int bn = pick_bn(N, ncols, K / BK);
@@ -635,6 +658,11 @@ int launch_tc_linear(const void* a, const void* w, void* o0, void* o1, void* o2,
   g.ncols = ncols;
   g.status = status;
   g.wait_limit = wait_limit;
+  g.skip_load = dpp_host::skip_load_from_env("linear");
+  if (vmax && (!o2 || vmax_L % BM || ncols % 64)) return DPP_ERR_SHAPE;
+  g.vmax = vmax;
+  g.vmax_L = vmax_L;
+  g.vmax_heads = vmax_heads;
   return dispatch<false, false>(bn, ta, ta, tb, g, s);
 }
 
@@ -658,6 +686,7 @@ int launch_tc_linear_refresh(const void* a, const void* w, void* o0, void* o1, v
   g.ncols = ncols;
   g.status = status;
   g.wait_limit = wait_limit;
+  g.skip_load = dpp_host::skip_load_from_env("linear");
   const long long blc = M * ncols;  // elements of K (and of V): V's codes follow K's
   g.rfx_stale[0] = k_stale; g.rfx_stale[1] = v_stale;
   g.rfx_out[0] = k_out; g.rfx_out[1] = v_out;
@@ -691,6 +720,7 @@ int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int
   g.out[0] = out; g.ncols = Cout;
   g.status = status;
   g.wait_limit = wait_limit;
+  g.skip_load = dpp_host::skip_load_from_env("conv");
   g.H = H; g.W = W; g.Cin = Cin; g.Hp = H / P; g.cin_blocks = Cin / BK;
   g.boxes = BM / box_px;
   g.box_px = box_px;

@@ -88,11 +88,14 @@ def test_workspace_layout_sizes(lib):
     assert lo.y == lo.gn_params                          # no parameters without fuse_gn
     lf = dpp.workspace_layout(_params(fuse_gn=1))
     assert lf.y - lf.gn_params >= 2 * 4 * 3 * 640 * 4   # [B, P, 3, C] fp32 parameters
-    # 320 attention units on (without a GPU, the library assumes) 152 SMs: one round of
-    # 152 whole units, the other 168 shared; two counters per shared unit (1536 bytes
-    # with padding), then 152 + 168 partial records of 34816 bytes
-    part = dpp.attention_partials_size(2, 4096, 10, 4)
-    assert part == 1536 + (152 + 168) * 34816 or torch.cuda.is_available()
+    # the maxima of |V| per (batch, head) (20 words, 256 bytes with padding); then 320
+    # attention units on (without a GPU, the library assumes) 152 SMs: one round of 152
+    # whole units, the other 168 shared; two counters per shared unit (1536 bytes with
+    # padding), then 152 + 168 partial records of 34816 bytes
+    part = dpp.attention_scratch_size(2, 4096, 10, 4, split=True)
+    assert part == 256 + 1536 + (152 + 168) * 34816 or torch.cuda.is_available()
+    assert dpp.attention_scratch_size(2, 4096, 10, 4, split=False) == 256
+    assert dpp.attention_scratch_size(2, 4096, 10, 4, dtype=dpp.F32) == 0
     assert lo.attn_partial_bytes == part and lo.total >= lo.attn_partial + part
     n, nb = dpp.message_sizes(prm)
     blc = 2 * 4096 * 640
@@ -142,20 +145,20 @@ def test_host_checks_without_launch(lib):
     # bf16: W a multiple of 8 and H*W a multiple of 128 (row segments of gcd(W, 128))
     assert lib.halo_conv3x3(a, a, a, a, 1, 16, 44, 64, 128, 2, dpp.BF16, None, None) == 2
     assert lib.halo_conv3x3(a, a, a, a, 1, 3, 40, 64, 128, 3, dpp.BF16, None, None) == 2
-    assert lib.stale_kv_attention(a, a, a, a, a, a, 1, 1024, 2, 32, 2, dpp.BF16, None, None) == 2
-    assert lib.stale_kv_attention(a, a, a, a, a, a, 1, 1000, 2, 64, 3, dpp.BF16, None, None) == 2
-    assert lib.stale_kv_attention(a, a, a, a, a, vp(8), 1, 1024, 2, 64, 2, dpp.BF16, None,
-                                  None) == 3
-    # split schedule: a missing or short partials buffer is refused before any launch
-    need = lib.dpp_attention_partials_size(1, 1024, 2, 64, 4, dpp.BF16)
-    assert need > 0
-    assert lib.stale_kv_attention_split(a, a, a, a, a, a, 1, 1024, 2, 64, 4, dpp.BF16, None, 0,
-                                        None, None) == 9
-    assert lib.stale_kv_attention_split(a, a, a, a, a, a, 1, 1024, 2, 64, 4, dpp.BF16, a,
-                                        need - 1, None, None) == 9
-    assert lib.stale_kv_attention_split(a, a, a, a, a, a, 1, 1024, 2, 64, 4, dpp.BF16, vp(264),
-                                        need, None, None) == 3
-    assert lib.dpp_attention_partials_size(1, 1000, 2, 64, 3, dpp.BF16) == 0  # invalid shape
+    assert lib.stale_kv_attention(a, a, a, a, a, a, 1, 1024, 2, 32, 2, dpp.BF16, a, 4096, None,
+                                  None) == 2
+    assert lib.stale_kv_attention(a, a, a, a, a, a, 1, 1000, 2, 64, 3, dpp.BF16, a, 4096, None,
+                                  None) == 2
+    assert lib.stale_kv_attention(a, a, a, a, a, vp(8), 1, 1024, 2, 64, 2, dpp.BF16, a, 4096,
+                                  None, None) == 3
+    # a missing or short scratch buffer is refused before any launch, for both schedules
+    for fn, split in ((lib.stale_kv_attention, 0), (lib.stale_kv_attention_split, 1)):
+        need = lib.dpp_attention_scratch_size(1, 1024, 2, 64, 4, dpp.BF16, split)
+        assert need > 0
+        assert fn(a, a, a, a, a, a, 1, 1024, 2, 64, 4, dpp.BF16, None, 0, None, None) == 9
+        assert fn(a, a, a, a, a, a, 1, 1024, 2, 64, 4, dpp.BF16, a, need - 1, None, None) == 9
+        assert fn(a, a, a, a, a, a, 1, 1024, 2, 64, 4, dpp.BF16, vp(264), need, None, None) == 3
+    assert lib.dpp_attention_scratch_size(1, 1000, 2, 64, 3, dpp.BF16, 1) == 0  # invalid shape
     prm = _params()
     w = dpp.LayerWeights()
     st = dpp.LayerState()

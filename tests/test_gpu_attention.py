@@ -19,10 +19,7 @@ def _attn_gpu(q, kf, vf, ks, vs, heads, P, split=False):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     args = (q.cuda(), kf.cuda(), vf.cuda(), ks.cuda(), vs.cuda(), o, heads, P)
     if split:
-        B, L, _ = q.shape
-        n = dpp.attention_partials_size(B, L, heads, P, dpp.dtype_code(q))
-        part = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda") if n else None
-        dpp.stale_kv_attention_split(*args, partials=part, dev_status=st)
+        dpp.stale_kv_attention_split(*args, dev_status=st)
     else:
         dpp.stale_kv_attention(*args, dev_status=st)
     torch.cuda.synchronize()
@@ -82,15 +79,21 @@ def test_attention_sdxl3840_sampled_rows(split):
     assert rel_err(np64(o)[:, rows], ref) < TOL_BF16
 
 
+@pytest.mark.parametrize("rows", ["all", "alternating"])
 @pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("P", [1, 2])
-def test_attention_late_large_scores_rescale(P, split):
+def test_attention_late_large_scores_rescale(P, split, rows):
     """Scores in a late key tile far above those of the first tiles: the running
-    reference maximum must move (O and the row sum rescaled) and the result still
-    matches the oracle."""
+    reference maximum must move (O and the row sum rescaled, P recomputed) and the
+    result still matches the oracle.  rows="alternating": the jump happens only for
+    every other query row (the others see the same keys as very low scores), so rows of
+    one warp take different paths."""
     B, L, heads = 1, 1024, 1
     g = torch.Generator().manual_seed(11)
-    q = (0.5 + 0.05 * torch.randn(B, L, 64, generator=g)).to(torch.bfloat16)
+    q = (0.5 + 0.05 * torch.randn(B, L, 64, generator=g))
+    if rows == "alternating":
+        q[:, 1::2] *= -1.0
+    q = q.to(torch.bfloat16)
     k = (0.1 * torch.randn(B, L, 64, generator=g))
     k[:, 640:768] += 3.0          # tile 5: scores ~ 0.5*3*64/8 = 12 above the rest
     k[:, 900:910] += 6.0          # a few even larger keys later on
@@ -115,3 +118,27 @@ def test_attention_split_deterministic_and_close_to_whole_units():
     o0 = _attn_gpu(q, kf, vf, ks, vs, heads, P, False)
     assert torch.equal(o1, o2)
     assert rel_err(np64(o1), np64(o0)) < TOL_BF16
+
+
+@pytest.mark.parametrize("split", [False, True])
+@pytest.mark.parametrize("vscale", [1e4, 1e-5, 1e6, 1e-30, "mixed"])
+def test_attention_v_outside_fp16_range(vscale, split):
+    """P.V runs in fp16, whose full-precision range is [2^-14, 65504].  V at scale 1e4
+    (max near 4.5e4), 1e6 (beyond fp16), 1e-5 and 1e-30 (fp16 subnormal or zero without
+    scaling), and per-head mixtures of those, all within the bf16 bound: the kernel
+    scales V by a power of two per (batch, head) and removes it from O."""
+    B, L, heads, P = 2, 1024, 4, 4
+    q, kf, vf, ks, vs = synth.attention_inputs(B, L, heads, 64, "bf16", seed=77)
+    if vscale == "mixed":
+        f = torch.tensor([1e4, 1e-5, 1.0, 3e5], dtype=torch.float32).repeat_interleave(64)
+    else:
+        f = torch.full((heads * 64,), float(vscale))
+    vf = (vf.float() * f).to(torch.bfloat16)
+    vs = (vs.float() * f).to(torch.bfloat16)
+    assert torch.isfinite(vf.float()).all() and vf.float().abs().max() > 0
+    o = _attn_gpu(q, kf, vf, ks, vs, heads, P, split)
+    ref = oracle.stale_kv_attention(*(np64(t) for t in (q, kf, vf, ks, vs)), heads, P, "bf16")
+    for h in range(heads):  # each head on its own scale
+        cs = slice(h * 64, (h + 1) * 64)
+        err = rel_err(np64(o)[..., cs], ref[..., cs])
+        assert err < TOL_BF16, (h, err)

@@ -84,18 +84,3 @@ def test_conv_vae_size_banded_equals_unbanded_and_oracle_rows():
     assert rel_err(np64(out)[:, rows], ref) < TOL_BF16
     ref1 = oracle.halo_conv3x3(np64(yf), np64(yf), np64(w), 1, "bf16", rows=rows)
     assert rel_err(np64(unbanded)[:, rows], ref1) < TOL_BF16
-
-
-def test_conv_timeout_path_reports_status(monkeypatch):
-    """Every in-kernel wait is bounded: with the bound forced to 0 the kernel gives
-    up, reports DPP_ERR_TIMEOUT in the status word and returns (context usable)."""
-    monkeypatch.setenv("DPP_DEBUG_WAIT_LIMIT", "0")
-    yf, ys, w = synth.conv_inputs(1, 16, 64, 128, 128, "bf16", seed=1)
-    out = torch.empty(1, 16, 64, 128, dtype=torch.bfloat16, device="cuda")
-    st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    dpp.halo_conv3x3(yf.cuda(), ys.cuda(), w.cuda(), out, 4, dev_status=st)
-    torch.cuda.synchronize()
-    assert st.item() in (0, 6)   # a wait may still succeed on its one try
-    monkeypatch.delenv("DPP_DEBUG_WAIT_LIMIT")
-    ok = _conv_gpu(yf, ys, w, 4)  # the context is still usable
-    assert torch.isfinite(ok.float()).all()

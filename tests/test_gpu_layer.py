@@ -367,3 +367,40 @@ def test_layer_message_keeps_rank_copies_identical(name, dbuf, frx):
             for k in c:
                 assert torch.equal(c[k], state[k]), (i, r, k)
     assert state["k_stale"].float().abs().sum().item() > 0  # a non-trivial state
+
+
+@pytest.mark.parametrize("vshift", [17, -20])
+def test_layer_v_outside_fp16_range(vshift):
+    """The V projection weights scaled by 2^17 (V near 1e4..1e5, beyond fp16's 65504) or
+    2^-20 (V in fp16's subnormal range): the layer step takes max |V| per (batch, head)
+    from the projection's epilogue (fresh V) and the GroupNorm pass (stale V) and scales
+    V by a power of two inside the attention.  A synchronous then a stale step; the
+    attention stage on the GPU's own Q, K, V and the state within the bf16 bound."""
+    cfg = CFGS["small_bf16"]
+    wts = synth.layer_weights(cfg, seed=4, affine=True)
+    C = cfg.C
+    w = wts["w_qkv"].clone()
+    w[2 * C:] = (w[2 * C:].float() * 2.0 ** vshift).to(w.dtype)
+    wts["w_qkv"] = w
+    wn = {k: np64(v) for k, v in wts.items()}
+    x, x_prev = synth.layer_inputs(cfg, seed=4)
+    prm = _params(cfg)
+    state, ws = dpp.alloc_layer(prm)
+    wd = {k: t.cuda() for k, t in wts.items()}
+    out = torch.empty(cfg.B, cfg.H, cfg.W, cfg.C, dtype=torch.bfloat16, device="cuda")
+    dpp.patch_layer_step(prm, wd, state, x_prev.cuda(), out, dpp.SYNC, ws)
+    assert dpp.read_device_status(ws) == 0
+    v0 = {k: np64(t) for k, t in dpp.workspace_views(prm, ws).items()}
+    o_sync = oracle.stale_kv_attention(v0["q"], v0["k"], v0["v"], v0["k"], v0["v"], cfg.heads,
+                                       cfg.P, "bf16")
+    assert rel_err(v0["o"], o_sync) < TOL_BF16
+    old = {k: np64(state[k]) for k in ("k_stale", "v_stale")}
+    assert np.abs(old["v_stale"]).max() > 65504 if vshift > 0 else np.abs(old["v_stale"]).max() < 2 ** -10
+    dpp.patch_layer_step(prm, wd, state, x.cuda(), out, dpp.STALE, ws)
+    assert dpp.read_device_status(ws) == 0
+    v1 = {k: np64(t) for k, t in dpp.workspace_views(prm, ws).items()}
+    B, L = cfg.B, cfg.L
+    o = oracle.stale_kv_attention(v1["q"], v1["k"], v1["v"], old["k_stale"].reshape(B, L, C),
+                                  old["v_stale"].reshape(B, L, C), cfg.heads, cfg.P, "bf16")
+    assert rel_err(v1["o"], o) < TOL_BF16
+    assert rel_err(np64(out).reshape(B, L, C), oracle.linear(v1["o"], wn["w_o"], "bf16")) < TOL_BF16
