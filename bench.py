@@ -33,9 +33,19 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "patch-layer steps/s; attention TFLOP/s & refresh GB/s as % of GB300 roofline"
-# dram__bytes_read.sum + dram__bytes_write.sum of one SDXL-1024 attention launch from an
-# ncu capture of the current kernel version (profiles/tc_attn_kernel_sdxl.md)
-ATTN_TRAFFIC_BYTES = 52.515072e6 + 1.034496e6
+# dram__bytes_read.sum + dram__bytes_write.sum per launch, from ncu captures of the
+# current kernel versions (summaries in profiles/); None where no capture of the current
+# version exists.
+TRAFFIC = {
+    "attention_sdxl1024_step": None,
+    "attention_sdxl3840": None,
+    "conv_sdxl1024_step": None,
+    "conv_vae_1x256x256x512": None,
+    "conv_sdxl3840_latent_step": None,
+    "refresh_sweep_200MiB": None,
+    "refresh_2x256x256x640_step": None,
+    "groupnorm_2x240x240x640_step": None,
+}
 WORKLOAD = "sdxl1024_mid_b2_64x64_c640_p4_bf16"
 
 
@@ -203,6 +213,25 @@ def whole_job_rate(steps: int, world: int, max_total_ms: float) -> float:
     return world * steps / (max_total_ms / 1e3)
 
 
+def _roof(name, kernel, bound, work, ms, peaks, algorithmic):
+    """One roofline row: algorithmic work per launch / the event-timed duration, against
+    the measured burst peak (these kernels are timed in short runs), with the sustained
+    tensor ratio beside it; traffic = ncu DRAM bytes per launch of the current version."""
+    if bound == "hbm":
+        ach = work / (ms * 1e-3) / 1e9
+        row = {"name": name, "kernel": kernel, "bound": "hbm", "achieved": ach,
+               "peak": peaks["hbm"], "unit": "GB/s", "frac": ach / peaks["hbm"],
+               "peak_kind": f"HBM copy bandwidth, {peaks['src']}"}
+    else:
+        ach = work / (ms * 1e-3) / 1e12
+        row = {"name": name, "kernel": kernel, "bound": "tensor", "achieved": ach,
+               "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": ach / peaks["bf16"],
+               "peak_kind": f"bf16 dense burst, {peaks['src']}",
+               "frac_of_sustained": ach / peaks["bf16_sus"]}
+    row.update({"traffic": TRAFFIC.get(name), "ms": ms, "algorithmic": algorithmic})
+    return row
+
+
 def _layer_setup(dev, fuse_gn=False):
     import torch
 
@@ -299,7 +328,9 @@ def run_gpu(args):
     qkv_flop = 2.0 * B * L * C * 3 * C
     o_flop = 2.0 * B * L * C * C
     act = B * L * C
-    gn_bytes = 3 * act * 2             # read x (stats), read x + write y (apply)
+    # read x (stats), read x + write y (apply), and the stale V read on the way for the
+    # attention's per-(batch, head) V range
+    gn_bytes = 4 * act * 2
     halo_elems = B * (P - 1) * 2 * cfg.W * C
     refresh_elems = 2 * act + halo_elems
     refresh_bytes = 7.03125 * refresh_elems
@@ -318,13 +349,24 @@ def run_gpu(args):
             v["frac_hbm"] = v["GB/s"] / peaks["hbm"]
         else:
             v["frac_bf16_sustained"] = v["TFLOP/s"] / peaks["bf16_sus"]
-    roofline = {"kernel": "stale_kv_attention (tc_attn_kernel)", "bound": "tensor",
-                "achieved": attn_tfs, "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
-                "frac": attn_tfs / peaks["bf16_sus"], "traffic": ATTN_TRAFFIC_BYTES,
-                "traffic_note": "dram read+write bytes per launch (ncu); algorithmic 62.9e6 "
-                                "(O writes stay in L2)",
-                "peak_kind": f"bf16 dense sustained, {peaks['src']}",
-                "algorithmic": f"4*B*heads*L^2*d = {attn_flop:.4g} FLOP per launch"}
+    roofline = _roof("attention_sdxl1024_step", "tc_attn_kernel (stale_kv_attention_split)",
+                     "tensor", attn_flop, avg["attention"], peaks,
+                     f"4*B*heads*L^2*d = {attn_flop:.4g} FLOP per launch (B=2, L=4096, 10 heads)")
+    rows = [dict(roofline),
+            _roof("conv_sdxl1024_step", "tc_gemm_kernel<conv> (halo_conv3x3)", "tensor",
+                  conv_flop, avg["halo_conv"], peaks,
+                  f"2*B*H*W*C*9*C = {conv_flop:.4g} FLOP (2x64x64, 640->640)"),
+            _roof("qkv_proj_sdxl1024_step", "tc_gemm_kernel<linear>", "tensor", qkv_flop,
+                  avg["qkv_proj"], peaks, f"2*M*3C*C = {qkv_flop:.4g} FLOP"),
+            _roof("out_proj_sdxl1024_step", "tc_gemm_kernel<linear>", "tensor", o_flop,
+                  avg["out_proj"], peaks, f"2*M*C*C = {o_flop:.4g} FLOP"),
+            _roof("groupnorm_sdxl1024_step", "gn_stats_kernel + gn_apply_kernel", "hbm",
+                  gn_bytes, avg["groupnorm"], peaks,
+                  f"8 B per element x {act} = {gn_bytes:.4g} B: x read twice, y written, stale V "
+                  "read for the attention's V range (latency-bound at 42 MB)"),
+            _roof("refresh_sdxl1024_step", "refresh_kernel", "hbm", refresh_bytes,
+                  avg["state_update"], peaks,
+                  f"7.03125 B per element x {refresh_elems} = {refresh_bytes:.4g} B")]
 
     # End to end through the public API with host buffers (pinned), copies timed.
     # (1) latency: each step alone -- H2D of its input, the step, D2H of its output.
@@ -412,16 +454,44 @@ def run_gpu(args):
     }
     line["clocks"] = clocks.summary()
     if not args.no_secondary:
-        line["secondary"] = {"attention_sdxl3840": measure_attention_3840(dev, peaks),
-                             "refresh_sweep": measure_refresh_sweep(dev, peaks),
-                             "layer_2x256x256x640_p8": measure_large_layer(dev, peaks),
-                             "layer_sdxl3840_2x240x240x640_p8": measure_large_layer(
-                                 dev, peaks, H=240, W=240),
-                             "halo_conv_vae": measure_vae_conv(dev, peaks),
+        a3840 = measure_attention_3840(dev, peaks)
+        sweep = measure_refresh_sweep(dev, peaks)
+        big = measure_large_layer(dev, peaks)
+        lat = measure_large_layer(dev, peaks, H=240, W=240)
+        vae = measure_vae_conv(dev, peaks)
+        line["secondary"] = {"attention_sdxl3840": a3840, "refresh_sweep": sweep,
+                             "layer_2x256x256x640_p8": big,
+                             "layer_sdxl3840_2x240x240x640_p8": lat,
+                             "halo_conv_vae": vae,
+                             "tiny_f32_step": measure_tiny_f32(dev),
                              "otil_exchange_2x4x128x128_p4": measure_otil(dev),
                              "layer_fusions": measure_fusions(dev)}
+        rows += [
+            _roof("attention_sdxl3840", "tc_attn_kernel (stale_kv_attention_split)", "tensor",
+                  a3840["flop_per_launch"], a3840["ms_mean"], peaks,
+                  "4*B*heads*L^2*d, B=2, L=57600, 10 heads, P=8 (standalone launches)"),
+            _roof("conv_vae_1x256x256x512", "tc_gemm_kernel<conv>", "tensor",
+                  vae["flop_per_launch"], vae["ms_mean"], peaks,
+                  "2*H*W*C*9*C, 1x256x256, 512->512, P=8 (standalone, L2 flushed)"),
+            _roof("conv_sdxl3840_latent_step", "tc_gemm_kernel<conv, wrapping segments>",
+                  "tensor", lat["conv_flop"], lat["stage_ms"]["halo_conv"], peaks,
+                  "2*B*H*W*C*9*C, 2x240x240, 640->640, P=8 (W=240: 16-pixel row segments)"),
+            _roof("refresh_sweep_200MiB", "refresh_kernel", "hbm", sweep["bytes_per_launch"],
+                  sweep["ms_mean"], peaks,
+                  "7.03125 B per element x 104988672 (standalone, L2 flushed)"),
+            _roof("refresh_2x256x256x640_step", "refresh_kernel", "hbm", big["refresh_bytes"],
+                  big["stage_ms"]["state_update"], peaks,
+                  "7.03125 B per element x (K, V, halo rows) of a 2x256x256x640 P=8 step"),
+            _roof("groupnorm_2x240x240x640_step", "gn_stats_kernel + gn_apply_kernel", "hbm",
+                  lat["groupnorm_bytes"], lat["stage_ms"]["groupnorm"], peaks,
+                  "8 B per element x 2x240x240x640 (stats read, apply read + write, stale V "
+                  "read for the attention's V range)"),
+        ]
+    line["roofline"]["kernels"] = rows
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_budget_s)
+        if not args.no_oracle_plan:
+            line["cpu_baseline"]["plan"] = cpu_oracle_plan()
     if ws_n > 1:
         tdist.barrier()
         tdist.destroy_process_group()
@@ -554,6 +624,37 @@ def measure_vae_conv(dev, peaks, iters=5):
             "launches": iters}
 
 
+def measure_tiny_f32(dev, iters=50):
+    """The tiny fp32 workload's layer step on the GPU (1x32x32x64, P=2, G=8, one head,
+    fp32 SIMT kernels): steps/s of back-to-back STALE steps with refresh."""
+    import torch
+
+    import stale_activations_gb300 as dpp
+    import synth
+    cfg = synth.TINY_F32
+    prm = dpp.make_params(cfg.B, cfg.H, cfg.W, cfg.C, cfg.P, cfg.G, cfg.heads, dpp.F32,
+                          refresh=True, eps=cfg.eps)
+    wts = {k: v.to(dev) for k, v in synth.layer_weights(cfg, seed=0).items()}
+    x, x_prev = (t.to(dev) for t in synth.layer_inputs(cfg, seed=0))
+    state, ws = dpp.alloc_layer(prm, device=dev)
+    out = torch.empty_like(x)
+    dpp.patch_layer_step(prm, wts, state, x_prev, out, dpp.SYNC, ws)
+    for _ in range(5):
+        dpp.patch_layer_step(prm, wts, state, x, out, dpp.STALE, ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(iters):
+        dpp.patch_layer_step(prm, wts, state, x, out, dpp.STALE, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    if dpp.read_device_status(ws) != 0:
+        raise RuntimeError("device status set in the tiny fp32 steps")
+    ms = e0.elapsed_time(e1) / iters
+    return {"workload": cfg.name, "ms_per_step": ms, "steps/s": 1e3 / ms,
+            "note": "back-to-back steps, launch-bound at this size"}
+
+
 def measure_otil(dev, iters=20):
     """The OTIL exchange alone at the pages' noise-prediction shape: [2, 4, 128, 128]
     bf16, P = 4 ranks, 8 x 32 sub-blocks (K = 16 per band), k = 4 sent per rank and
@@ -678,17 +779,19 @@ def measure_large_layer(dev, peaks, iters=3, H=256, W=256):
            for k, n in enumerate(dpp.STAGES)}
     act = B * H * W * C
     L = H * W
-    gn_gbs = 3 * act * 2 / (avg["groupnorm"] * 1e-3) / 1e9
+    gn_gbs = 4 * act * 2 / (avg["groupnorm"] * 1e-3) / 1e9
     ref_bytes = 7.03125 * (2 * act + B * (P - 1) * 2 * W * C)
     ref_gbs = ref_bytes / (avg["state_update"] * 1e-3) / 1e9
     attn_tfs = 4.0 * B * heads * L * L * 64 / (avg["attention"] * 1e-3) / 1e12
     conv_tfs = 2.0 * B * L * C * 9 * C / (avg["halo_conv"] * 1e-3) / 1e12
     step_ms = sum(avg.values())
-    return {"ms_per_step": step_ms, "stage_ms": avg,
+    return {"ms_per_step": step_ms, "stage_ms": avg, "groupnorm_bytes": 4 * act * 2,
+            "refresh_bytes": ref_bytes, "conv_flop": 2.0 * B * L * C * 9 * C,
             "groupnorm_GB/s": gn_gbs, "groupnorm_frac_hbm": gn_gbs / peaks["hbm"],
             "refresh_GB/s": ref_gbs, "refresh_frac_hbm": ref_gbs / peaks["hbm"],
             "attention_TFLOP/s": attn_tfs, "conv_TFLOP/s": conv_tfs,
-            "note": "GroupNorm algorithmic bytes 6 B/elem (stats read, apply read+write)"}
+            "note": "GroupNorm algorithmic bytes 8 B/elem (stats read, apply read+write, stale V "
+                    "read for the attention's V range)"}
 
 
 # ------------------------------------------------------------------ CPU oracle (reference arm)
@@ -730,6 +833,102 @@ def cpu_baseline(budget_s: float):
                       f"threads + C refresh), {el:.1f} s"}
 
 
+def _oracle_plan_child(threads: str):
+    """Runs in a fresh process whose BLAS/OpenMP thread counts the parent set: times the
+    oracle on each of the five workloads (bounded samples where a full run takes minutes)
+    and prints one JSON object."""
+    import numpy as np
+
+    import oracle
+    import synth
+    out = {"threads": threads}
+
+    def np64(t):
+        return t.double().numpy()
+
+    # tiny fp32 layer step, in full
+    cfg = synth.TINY_F32
+    wn = {k: np64(v) for k, v in synth.layer_weights(cfg, seed=0).items()}
+    x, xp = synth.layer_inputs(cfg, seed=0)
+    st = oracle.empty_state(cfg.B, cfg.H, cfg.W, cfg.C, cfg.P, cfg.G)
+    _, st, _, _ = oracle.patch_layer_step(np64(xp), st, wn, cfg.P, cfg.G, cfg.heads, cfg.eps,
+                                          "f32", oracle.SYNC)
+    n, t0 = 0, time.perf_counter()
+    while n < 20 and (n == 0 or time.perf_counter() - t0 < 2.0):
+        oracle.patch_layer_step(np64(x), st, wn, cfg.P, cfg.G, cfg.heads, cfg.eps, "f32",
+                                oracle.STALE)
+        n += 1
+    el = time.perf_counter() - t0
+    out["tiny_f32_step"] = {"value": n / el, "unit": "steps/s", "s": el,
+                            "sample": f"{n} full STALE steps with refresh"}
+    # the SDXL-1024 layer step: timed in the parent with all cores; one step here with one
+    if threads == "1":
+        case = _oracle_case()
+        t0 = time.perf_counter()
+        _oracle_step(case)
+        el = time.perf_counter() - t0
+        out["sdxl1024_step"] = {"value": 1 / el, "unit": "steps/s", "s": el,
+                                "sample": "one full STALE step with refresh"}
+    # SDXL-3840 attention: 256 query rows per (patch, head), keys and values in full, then
+    # extrapolated to all 2 x 57600 rows of all 10 heads (rows are independent)
+    B, L, heads, P = 2, 57600, 10, 8
+    hs = heads if threads != "1" else 1  # one head on one thread (extrapolated over heads)
+    Lp = L // P
+    rng = np.random.default_rng(0)
+    rows = np.sort(np.concatenate([p * Lp + rng.choice(Lp, 256, replace=False)
+                                   for p in range(P)]))
+    gen = [oracle.to_storage(np64(synth.normal((1, L, hs * 64), 0, t)), "bf16")
+           for t in ("q", "k", "v", "k_noise", "v_noise")]
+    t0 = time.perf_counter()
+    oracle.stale_kv_attention(gen[0], gen[1], gen[2], gen[3], gen[4], hs, P, "bf16", rows=rows)
+    el = time.perf_counter() - t0
+    scale = (B * L * heads) / (len(rows) * hs)
+    flop = 4.0 * B * heads * L * L * 64
+    out["sdxl3840_attention"] = {
+        "value": flop / (el * scale) / 1e12, "unit": "TFLOP/s", "s": el,
+        "s_per_launch_extrapolated": el * scale,
+        "sample": f"{len(rows)} query rows (256 per patch) x {hs} head(s) of batch 0 over all "
+                  f"57600 keys; extrapolated x{scale:.0f} to the full launch (rows independent)"}
+    # VAE-sized halo conv, in full
+    yf, ys, w = synth.conv_inputs(1, 256, 256, 512, 512, "bf16", seed=0)
+    a, b, c = np64(yf), np64(ys), np64(w)
+    t0 = time.perf_counter()
+    oracle.halo_conv3x3(a, b, c, 8, "bf16")
+    el = time.perf_counter() - t0
+    out["vae_conv_1x256x256x512"] = {"value": 2.0 * 65536 * 512 * 9 * 512 / el / 1e12,
+                                     "unit": "TFLOP/s", "s": el, "sample": "one full conv"}
+    # 200 MiB refresh sweep, in full (exact fp32 C code, OpenMP over blocks)
+    f, s_ = synth.refresh_sweep_inputs(seed=0)
+    f64, s64 = np64(f), np64(s_)
+    del f, s_
+    t0 = time.perf_counter()
+    oracle.refresh_residual(f64, s64, "bf16")
+    el = time.perf_counter() - t0
+    out["refresh_sweep_200MiB"] = {"value": 7.03125 * f64.size / el / 1e9, "unit": "GB/s",
+                                   "s": el, "sample": "one full sweep (104988672 elements)"}
+    print(json.dumps(out))
+
+
+def cpu_oracle_plan():
+    """The oracle on this host's cores for the five workloads, with every core and with
+    one thread (BLAS and OpenMP thread counts fixed before numpy loads, in a fresh
+    process each)."""
+    import subprocess
+    res = {"nproc": os.cpu_count()}
+    for threads in ("all", "1"):
+        env = dict(os.environ)
+        if threads == "1":
+            env.update(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-plan-child",
+                            threads], env=env, capture_output=True, text=True, timeout=900)
+        if r.returncode != 0:
+            res[threads] = {"error": r.stderr.strip().splitlines()[-1:]}
+            continue
+        res["all_cores" if threads == "all" else "single_thread"] = json.loads(
+            r.stdout.strip().splitlines()[-1])
+    return res
+
+
 def run_reference(args):
     ws_n, rank, _ = _dist()
     if rank != 0:
@@ -767,7 +966,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the standalone SDXL-3840 attention and refresh-sweep lines")
+    ap.add_argument("--no-oracle-plan", action="store_true",
+                    help="skip the oracle timings of the five workloads on the host cores")
+    ap.add_argument("--oracle-plan-child", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_plan_child:
+        _oracle_plan_child(args.oracle_plan_child)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -404,7 +404,8 @@ int dpp_otil_step(const dpp_otil_params* prm, const void* fresh, void* views, ui
 int dpp_otil_finalize(const dpp_otil_params* prm, const void* fresh, void* views,
                       uint8_t* visited, int reset, void* stream);
 
-/* Number of kernels one patch_layer_step launches for these params and mode. */
+/* Number of kernels one patch_layer_step launches for these params and mode (with
+ * fuse_refresh counted as in effect, i.e. for a state with the second set). */
 int dpp_layer_kernel_count(const dpp_layer_params* prm, int mode);
 
 #ifdef __cplusplus

@@ -325,6 +325,9 @@ int64_t dpp_message_blocks(const dpp_layer_params* p) {
 int dpp_layer_kernel_count(const dpp_layer_params* p, int mode) {
   if (check_layer(p)) return -1;
   int n = 2 /* gn */ + 1 /* conv */ + 1 /* qkv */ + 1 /* attention */ + 1 /* out proj */;
+  // the attention's separate max |V| pass, when the GroupNorm and projection kernels do
+  // not take it on the way (fuse_gn; fuse_refresh with a second state set)
+  if (p->dtype == DPP_BF16 && (p->fuse_gn || p->fuse_refresh)) n += 1;
   if (mode == DPP_STALE && p->refresh) {
     // a launch per full table of segments, and always a last one (it also copies
     // the GroupNorm sums)

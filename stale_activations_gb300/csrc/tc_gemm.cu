@@ -12,11 +12,15 @@
 // Halo conv staging ("Benchmarking DistVAE", Glossary: the halo rows a sharded
 // convolution needs; "OTIL for SDXL on 4x L40S", item 3: the conv halo buffers
 // are stale): for tap (di, dj) the A slice of an M tile is the tile's pixels
-// shifted by (di, dj), fetched as row segments of gcd(W, 128) pixels with a 4-D
-// tensor map over the NHWC map.  A segment whose source row is inside its own
-// row's band comes from the fresh map, one whose source row is the neighbouring
-// band's (the halo) from the stale map, and the TMA zero fill of out-of-range
-// rows/columns is the convolution's zero padding.
+// shifted by (di, dj), fetched as row segments with a 4-D tensor map over the NHWC
+// map.  A segment whose source row is inside its own row's band comes from the fresh
+// map, one whose source row is the neighbouring band's (the halo) from the stale map,
+// and the TMA zero fill of out-of-range rows/columns is the convolution's zero padding.
+// Three tilings of the pixels (AMODE): 128 consecutive pixels as whole rows or one
+// segment (W a multiple of 128, or 128 a multiple of W); 128 consecutive pixels as
+// segments of gcd(W, 128) pixels that wrap across rows; or, when W has a divisor tp in
+// [112, 128] (tp = 120 for the SDXL-3840 latent's W = 240), tp pixels of one row per
+// tile -- one box per tap, the MMA's last 128 - tp rows never stored.
 //
 // Two opt-in variants: GNF (the conv's A is raw x; warps 6-9 apply GroupNorm to the
 // landed in-band segments before the MMA reads a stage) and RFX (the Q/K/V projection
@@ -182,7 +186,7 @@ __device__ __forceinline__ void refresh_row(uint32_t t_row, __nv_bfloat16* dst, 
 // RFX (linear, 128-wide tiles): a K or V tile row is exactly one 128-element refresh
 // block, so the epilogue thread that stores a row of fresh K or V also quantises its
 // residual against the stale row and writes the refreshed row, the codes and the scale.
-template <bool CONV, int BN, bool GNF, bool RFX = false, bool WRAP = false>
+template <bool CONV, int BN, bool GNF, bool RFX = false, int AMODE = 0>
 __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
@@ -247,7 +251,12 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
         const long long m0 = (long long)mt * BM;
         const int n0 = nt * BN;
         int b = 0, r = 0, c0 = 0;
-        if (CONV) {
+        if (CONV && AMODE == 2) {  // a tile is box_px pixels of one row (rows padded)
+          const int tpr = args.W / args.box_px, R = mt / tpr;
+          b = R / args.H;
+          r = R - b * args.H;
+          c0 = (mt - R * tpr) * args.box_px;
+        } else if (CONV) {
           const long long hw = (long long)args.H * args.W;
           b = (int)(m0 / hw);
           const int rem = (int)(m0 - (long long)b * hw);
@@ -281,7 +290,10 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
             }
             note[s] = StageNote{c0 + tap % 3 - 1, (int)fresh};
           }
-          ptx::mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          // padded row tiles: only box_px of the 128 A rows are loaded (the MMA rows past
+          // them compute values that the epilogue never stores)
+          ptx::mbar_arrive_expect_tx(
+              &full[s], AMODE == 2 ? (uint32_t)(args.box_px * 128 + C::B_BYTES) : C::STAGE_BYTES);
           if (CONV) {
             const int tap = kb / args.cin_blocks;
             const int cb = kb - tap * args.cin_blocks;
@@ -290,7 +302,7 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
             // segment (box_px divides W).  Whole rows (box_px == W) or one box per tile
             // (W a multiple of 128): box bx is row r + bx from column c0; with WRAP the
             // segments wrap across rows.
-            if (!WRAP) {
+            if (AMODE != 1) {
               for (int bx = 0; bx < args.boxes; ++bx) {
                 const int rk = r + bx;   // image row of this box's pixels
                 const int rr = rk + di;  // source row
@@ -470,7 +482,13 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
       }
       ptx::tc_fence_after();
       const int mt = tile / args.n_tiles, nt = tile - mt * args.n_tiles;
-      const long long row = (long long)mt * BM + quarter * 32 + lane;
+      long long row = (long long)mt * BM + quarter * 32 + lane;
+      bool row_ok = row < args.M;
+      if (CONV && AMODE == 2) {  // pixel c0 + local of image row R
+        const int tpr = args.W / args.box_px, R = mt / tpr, local = quarter * 32 + lane;
+        row = (long long)R * args.W + (long long)(mt - R * tpr) * args.box_px + local;
+        row_ok = local < args.box_px;
+      }
       const int n0 = nt * BN;
       const int which = n0 / args.ncols;
       const int col0 = n0 - which * args.ncols;
@@ -480,7 +498,7 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(obase) + row * args.ncols + col0;
       const uint32_t t_base = tmem + ab * BN + ((uint32_t)(quarter * 32) << 16);
       const bool rfx_row = RFX && which > 0;
-      if (rfx_row) refresh_row(t_base, dst, row < args.M, which == 1, args, row * args.ncols + col0);
+      if (rfx_row) refresh_row(t_base, dst, row_ok, which == 1, args, row * args.ncols + col0);
 #pragma unroll 1
       for (int ch = 0; ch < (rfx_row ? 0 : BN / 32); ++ch) {
         uint32_t v[32];
@@ -494,7 +512,7 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
           pk[i].z = pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
           pk[i].w = pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
         }
-        if (row < args.M) {
+        if (row_ok) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) d4[i] = pk[i];
@@ -507,7 +525,7 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
 #pragma unroll
             for (int e = 0; e < 4; ++e) m = max(m, max(w4[e] & 0x7FFFu, (w4[e] >> 16) & 0x7FFFu));
           }
-          m = __reduce_max_sync(0xffffffffu, row < args.M ? m : 0u);
+          m = __reduce_max_sync(0xffffffffu, row_ok ? m : 0u);
           if (lane == 0 && m) {  // the warp's 32 rows lie in one batch (L % 128 == 0)
             const long long r0 = (long long)mt * BM + quarter * 32;
             atomicMax(args.vmax + (r0 / args.vmax_L) * args.vmax_heads + (col0 + ch * 32) / 64,
@@ -560,12 +578,12 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
   return r == CUDA_SUCCESS;
 }
 
-template <bool CONV, int BN, bool GNF, bool RFX = false, bool WRAP = false>
+template <bool CONV, int BN, bool GNF, bool RFX = false, int AMODE = 0>
 int prepare() {
   static std::once_flag once;
   static int rc = DPP_OK;
   std::call_once(once, [] {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<CONV, BN, GNF, RFX, WRAP>,
+    if (cudaFuncSetAttribute(tc_gemm_kernel<CONV, BN, GNF, RFX, AMODE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<BN>::SMEM) != cudaSuccess)
       rc = DPP_ERR_CUDA;
@@ -590,29 +608,29 @@ int pick_bn(int N, int ncols, int nkb) {
 
 constexpr int mma_n(int bn) { return bn > 256 ? bn / 2 : bn; }
 
-template <bool CONV, int BN, bool GNF, bool RFX = false, bool WRAP = false>
+template <bool CONV, int BN, bool GNF, bool RFX = false, int AMODE = 0>
 int launch(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, GemmArgs g,
            cudaStream_t s) {
-  int rc = prepare<CONV, BN, GNF, RFX, WRAP>();
+  int rc = prepare<CONV, BN, GNF, RFX, AMODE>();
   if (rc) return rc;
   g.n_tiles = g.N / BN;
   const long long ntiles = (long long)g.m_tiles * g.n_tiles;
   const int grid = (int)(ntiles < dpp_host::sm_count() ? ntiles : dpp_host::sm_count());
   const cudaError_t e =
-      dpp_host::launch_pdl(tc_gemm_kernel<CONV, BN, GNF, RFX, WRAP>, dim3(grid),
+      dpp_host::launch_pdl(tc_gemm_kernel<CONV, BN, GNF, RFX, AMODE>, dim3(grid),
                            dim3(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS), Cfg<BN>::SMEM, s, ta, ta2,
                            tb, g);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
 
-template <bool CONV, bool GNF, bool WRAP = false>
+template <bool CONV, bool GNF, int AMODE = 0>
 int dispatch(int bn, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
              const GemmArgs& g, cudaStream_t s) {
   switch (bn) {
-    case 320: return launch<CONV, 320, GNF, false, WRAP>(ta, ta2, tb, g, s);
-    case 256: return launch<CONV, 256, GNF, false, WRAP>(ta, ta2, tb, g, s);
-    case 160: return launch<CONV, 160, GNF, false, WRAP>(ta, ta2, tb, g, s);
-    case 128: return launch<CONV, 128, GNF, false, WRAP>(ta, ta2, tb, g, s);
+    case 320: return launch<CONV, 320, GNF, false, AMODE>(ta, ta2, tb, g, s);
+    case 256: return launch<CONV, 256, GNF, false, AMODE>(ta, ta2, tb, g, s);
+    case 160: return launch<CONV, 160, GNF, false, AMODE>(ta, ta2, tb, g, s);
+    case 128: return launch<CONV, 128, GNF, false, AMODE>(ta, ta2, tb, g, s);
     default: return DPP_ERR_SHAPE;
   }
 }
@@ -703,6 +721,19 @@ int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int
   if (!bn) return DPP_ERR_SHAPE;
   int box_px = 128;  // gcd(W, 128)
   while (W % box_px) box_px >>= 1;
+  // When gcd(W, 128) is small (e.g. 16 for the SDXL-3840 latent's W = 240) a 128-pixel
+  // tile would need many short row segments per tap; instead a tile is the largest
+  // divisor tp <= 128 of W (120 for W = 240) pixels of one row -- one box per tap -- with
+  // the MMA's last 128 - tp rows unused, when that wastes at most 1/8 of the rows.
+  int amode = box_px == W || box_px == 128 ? 0 : 1;
+  if (amode == 1 && !gn_par) {
+    int tp = 128;
+    while (W % tp) --tp;
+    if (tp >= 112) {
+      amode = 2;
+      box_px = tp;
+    }
+  }
   if (gn_par && !tc_conv_gn_supported(H, W, P)) return DPP_ERR_SHAPE;
   CUtensorMap tf, ts, tw;
   const uint64_t dy[4] = {(uint64_t)Cin, (uint64_t)W, (uint64_t)H, (uint64_t)B};
@@ -716,21 +747,22 @@ int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int
     return DPP_ERR_CUDA;
   GemmArgs g{};
   g.M = (long long)B * H * W; g.N = Cout; g.K = K; g.nkb = K / BK;
-  g.m_tiles = (int)(g.M / BM);
+  g.m_tiles = amode == 2 ? B * H * (W / box_px) : (int)(g.M / BM);
   g.out[0] = out; g.ncols = Cout;
   g.status = status;
   g.wait_limit = wait_limit;
   g.skip_load = dpp_host::skip_load_from_env("conv");
   g.H = H; g.W = W; g.Cin = Cin; g.Hp = H / P; g.cin_blocks = Cin / BK;
-  g.boxes = BM / box_px;
+  g.boxes = amode == 2 ? 1 : BM / box_px;
   g.box_px = box_px;
   g.gn_par = gn_par;
   g.P = P;
   if (gn_par) return dispatch<true, true>(bn, tf, ts, tw, g, s);
-  // segments that wrap across rows get their own kernel, so that the common shapes keep
-  // the simpler producer (the branch alone cost the SDXL-1024 conv 7%)
-  return box_px == W || box_px == 128 ? dispatch<true, false>(bn, tf, ts, tw, g, s)
-                                      : dispatch<true, false, true>(bn, tf, ts, tw, g, s);
+  // each A staging mode is its own kernel instantiation, so that the common shapes keep
+  // the simplest producer (a run-time branch alone cost the SDXL-1024 conv 7%)
+  return amode == 0 ? dispatch<true, false>(bn, tf, ts, tw, g, s)
+         : amode == 1 ? dispatch<true, false, 1>(bn, tf, ts, tw, g, s)
+                      : dispatch<true, false, 2>(bn, tf, ts, tw, g, s);
 }
 
 }  // namespace dpp
