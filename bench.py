@@ -555,7 +555,7 @@ def measure_attention_3840(dev, peaks, iters=5):
     return {"ms_mean": ms_mean, "ms_min": ms_min, "TFLOP/s": tfs,
             "frac_of_burst_bf16": tfs / peaks["bf16"], "peak_burst": peaks["bf16"],
             "frac_of_sustained_bf16": tfs / peaks["bf16_sus"], "flop_per_launch": flop,
-            "launches": iters, "schedule": "split (attention + merge kernel)",
+            "launches": iters, "schedule": "split (cut units merged inside the attention kernel)",
             "whole_units": {"ms_mean": res[False][0], "TFLOP/s": res[False][2]},
             "note": "back-to-back launches, inputs > L2"}
 

@@ -34,10 +34,6 @@
  *     word is already 0) and returns early, leaving its output incomplete.
  *     The environment variable DPP_DEBUG_WAIT_LIMIT (read at each call)
  *     overrides the wait bound; 0 makes every such wait give up at once.
- *   - DPP_DEBUG_REFRESH_FORM (read at each call): 1 or 2 selects which of the two
- *     equivalent forms of the residual quantiser the refresh kernel runs (with a
- *     branch per element, or branch-free); both give the same bits, and the default
- *     picks the faster one for the call.  For tests that run each form on one input.
  *   - DPP_DEBUG_SKIP_LOAD=<kind>:<i> (read at each call; kind attn, conv or linear):
  *     every CTA of the attention kernel, of the conv's GEMM or of the projections'
  *     GEMM leaves its i-th K/V tile or K slice unloaded, so its bounded waits give up

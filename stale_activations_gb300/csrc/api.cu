@@ -34,13 +34,6 @@ int skip_load_from_env(const char* kind) {
   return v < 0 ? -1 : v;
 }
 
-int refresh_form_from_env() {
-  const char* s = getenv("DPP_DEBUG_REFRESH_FORM");
-  if (!s || !*s) return 0;
-  const int v = atoi(s);
-  return v == 1 || v == 2 ? v : 0;
-}
-
 int sm_count() {
   static std::mutex mu;
   static int cached[64] = {0};

@@ -68,10 +68,6 @@ namespace dpp_host {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 long long wait_limit_from_env();  // DPP_DEBUG_WAIT_LIMIT, else the default
-// DPP_DEBUG_REFRESH_FORM: 1 = the quantiser with a branch per element, 2 = the branch-free
-// one, anything else = the default choice (both forms give the same bits; the variable
-// lets the tests run each form on the same inputs)
-int refresh_form_from_env();
 // DPP_DEBUG_SKIP_LOAD=<kind>:<i> (kind "attn", "conv" or "linear"): a test hook that makes the TMA
 // producer of every CTA of that kernel kind leave its i-th load unissued, so that the
 // kernel's bounded waits give up and report DPP_ERR_TIMEOUT; -1 when unset

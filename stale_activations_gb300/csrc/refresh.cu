@@ -110,7 +110,7 @@ __device__ __forceinline__ void start_block(const RefreshTable& tab, long long g
   v.live = true;
 }
 
-template <typename T, bool PER_ELEM>
+template <typename T>
 __device__ __forceinline__ void finish_block(const VecBlock& v, int sub, unsigned hmask) {
   float f[8], sv[8], d[8];
   unpack8<T>(v.fr, f);
@@ -123,12 +123,7 @@ __device__ __forceinline__ void finish_block(const VecBlock& v, int sub, unsigne
   const QuantBlock qb = quant_block(a);
   if (sub == 0) *v.scale = qb.s;
   float tm[8], nv[8];
-  if (PER_ELEM) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) tm[i] = quant_elem(qb, d[i], sv[i], nv[i]);
-  } else {
-    quant8(qb, d, sv, tm, nv);
-  }
+  quant8(qb, d, sv, tm, nv);
   store8<T>(static_cast<T*>(v.out), nv);
   __stcs(reinterpret_cast<uint2*>(v.codes), pack_codes(tm));
 }
@@ -137,10 +132,7 @@ __device__ __forceinline__ void finish_block(const VecBlock& v, int sub, unsigne
 // finishing either block, to keep more bytes in flight per thread.  Blocks that are
 // ragged (the last of a segment) or in a misaligned segment are refreshed by a
 // second, scalar pass, so that the streaming loop holds no call.
-// PER_ELEM: the quantiser with a branch per element (faster on long streams such as the
-// 200 MiB sweep), else the branch-free one (faster inside the layer step, where the
-// refresh shares the SMs with the output projection); both give the same bits.
-template <typename T, bool PER_ELEM>
+template <typename T>
 __global__ void __launch_bounds__(256, 4) refresh_kernel(const __grid_constant__ RefreshTable tab) {
   const int lane = threadIdx.x & 31;
   const int sub = lane & 15;
@@ -158,8 +150,8 @@ __global__ void __launch_bounds__(256, 4) refresh_kernel(const __grid_constant__
     VecBlock v0, v1;
     start_block<T>(tab, gb, total, seg, sub, v0);
     start_block<T>(tab, gb + stride, total, seg, sub, v1);
-    if (v0.live) finish_block<T, PER_ELEM>(v0, sub, hmask);
-    if (v1.live) finish_block<T, PER_ELEM>(v1, sub, hmask);
+    if (v0.live) finish_block<T>(v0, sub, hmask);
+    if (v1.live) finish_block<T>(v1, sub, hmask);
   }
   // scalar pass: every block of a misaligned segment, the ragged last block of others
   for (int k = 0; k < tab.nseg; ++k) {
@@ -184,22 +176,11 @@ int launch_refresh(const RefreshTable& tab, int dtype, cudaStream_t stream) {
   long long want = (total + groups_per_cta - 1) / groups_per_cta;
   const long long cap = (long long)dpp_host::sm_count() * 4;  // 4 resident CTAs of 256 per SM
   const int grid = (int)(want < 1 ? 1 : want < cap ? want : cap);  // >= 1 for the side copy
-  // measured: the per-element form for a refresh of its own (4.94 -> 5.08 TB/s on the
-  // 200 MiB sweep), the branch-free form beside the layer's output projection
-  const int form = dpp_host::refresh_form_from_env();
-  const bool per_elem = form == 1 ? true : form == 2 ? false : !tab.early;
-  using dpp_host::launch_pdl;
-  cudaError_t e;
-  if (dtype == DPP_BF16)
-    e = per_elem ? launch_pdl(refresh_kernel<__nv_bfloat16, true>, dim3(grid), dim3(threads), 0,
-                              stream, tab)
-                 : launch_pdl(refresh_kernel<__nv_bfloat16, false>, dim3(grid), dim3(threads), 0,
-                              stream, tab);
-  else
-    e = per_elem ? launch_pdl(refresh_kernel<float, true>, dim3(grid), dim3(threads), 0, stream,
-                              tab)
-                 : launch_pdl(refresh_kernel<float, false>, dim3(grid), dim3(threads), 0, stream,
-                              tab);
+  const cudaError_t e =
+      dtype == DPP_BF16
+          ? dpp_host::launch_pdl(refresh_kernel<__nv_bfloat16>, dim3(grid), dim3(threads), 0,
+                                 stream, tab)
+          : dpp_host::launch_pdl(refresh_kernel<float>, dim3(grid), dim3(threads), 0, stream, tab);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? DPP_OK : DPP_ERR_CUDA;
 }
 

@@ -83,6 +83,10 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_KV = 4 * TILE_BYTES;
 constexpr int OFF_BAR = OFF_KV + KV_STAGES * 2 * TILE_BYTES;
 constexpr int ATTN_SMEM = OFF_BAR + 512 + 1024;
+// The first step of every CTA's tail run, tail_bound(c) for c = 0..G (split schedule), in
+// static shared memory (a fixed address: no register holds a pointer to it).
+constexpr int MAX_G = 159;
+static_assert(ATTN_SMEM + (MAX_G + 1) * 4 <= 227 * 1024, "shared memory per CTA");
 static_assert(ATTN_SMEM <= 227 * 1024, "shared memory per CTA");
 constexpr float kScaleLog2 = 0.18033688011112042f;  // log2(e) / sqrt(64)
 // A key tile whose probabilities (against the row's reference maximum) sum to 2^15 or
@@ -102,6 +106,7 @@ struct AttnArgs {
   int W;            // split: whole units per CTA (c, c+G, ...); 0 otherwise
   int split;        // 1: units W*G .. U-1 are shared key tile by key tile
   long long tailT;  // split: their (unit, key tile) steps
+  int tq, tr;       // tailT = tq * G + tr (tail_bound(c) = c tq + c tr / G in 32 bits)
   __nv_bfloat16* o;
   uint8_t* part;    // split: G + (U - W*G) partial records
   const unsigned* vmax;  // [B*heads] fp32 bits of max |V| over the fresh and stale V
@@ -136,6 +141,17 @@ __host__ __device__ __forceinline__ long long tail_bound(long long c, const Attn
 // The CTA whose tail run contains step s (ranges may be empty when tailT < G).
 __host__ __device__ __forceinline__ int tail_cta(long long s, const AttnArgs& a) {
   return (int)(((s + 1) * a.G - 1) / a.tailT);
+}
+
+// The same from the CTA's table tb[c] = tail_bound(c) (no 64-bit divisions on the merge
+// path): the largest c < G with tb[c] <= s.
+__device__ __forceinline__ int tail_cta_tb(const int* tb, long long s, int G) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tb[mid] <= s) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 
 __device__ __forceinline__ Sched make_sched(const AttnArgs& a) {
@@ -201,8 +217,10 @@ __host__ __device__ __forceinline__ UnitPos unit_pos(int u, const AttnArgs& a) {
 // range: e = 0 when max|V| lies in [2^-6, 2^15); otherwise 14 - floor(log2 max|V|), so
 // that the scaled maximum lies in [2^14, 2^15), clamped to [-125, 125] (only |V| below
 // 2^-111 then keeps some fp16 subnormals).  An all-zero V gets 0.
-__device__ __forceinline__ int v_exponent(const AttnArgs& a, int b, int h) {
-  const unsigned bits = __ldg(a.vmax + b * a.heads + h);
+__device__ __forceinline__ unsigned vmax_bits(const AttnArgs& a, int b, int h) {
+  return __ldg(a.vmax + b * a.heads + h);
+}
+__device__ __forceinline__ int v_exponent(unsigned bits) {
   const float amax = __uint_as_float(bits);
   if (bits == 0 || (amax >= 0.015625f && amax < 32768.0f)) return 0;
   const int E = (int)(bits >> 23) - 127;  // floor(log2 amax); a subnormal amax gives -127
@@ -256,50 +274,46 @@ __device__ __forceinline__ void store_f16x16(uint4* d4, const uint32_t (&o)[16],
 
 // Merges the pieces of tail unit ut for row r of query tile t: records of CTAs
 // ca..cb (those with a non-empty run), in that order.  With pieces i = (m_i, l_i,
-// O_i/l_i): M = max m_i, w_i = l_i 2^(m_i - M), o = sum_i w_i (O_i/l_i) / sum_i w_i,
-// times 2^-e (the records hold O in V's scaled units).
+// O_i/l_i), in one pass with a running maximum M: each piece rescales the sums so far by
+// 2^(M_old - M) and adds w_i = l_i 2^(m_i - M); o = sum_i w_i (O_i/l_i) / sum_i w_i,
+// times 2^-e (the records hold O in V's scaled units).  One round trip to L2 per piece.
 // The records were written by other SMs: read through L2 (ld.global.cg).
-__device__ __forceinline__ void merge_rows(const AttnArgs& a, int ut, int t, int r, int ca, int cb,
-                                           const UnitPos& up, int e) {
+__device__ __forceinline__ void merge_rows(const AttnArgs& a, const int* tb, int ut, int t,
+                                           int r, int ca, int cb, const UnitPos& up, int e) {
+  const int row_in_patch = up.q0 + t * QT + r;
+  if (row_in_patch >= a.Lp) return;
   const long long s_a = (long long)ut * a.nkt;
-  auto record = [&](int c, long long b0) -> const uint8_t* {
-    // a CTA's first tail segment, or the last one of the CTA that started before the unit
-    return a.part + (size_t)((c == ca && b0 != s_a) ? a.G + ut : c) * REC_BYTES;
-  };
-  float M = -INFINITY;
-  for (int c = ca; c <= cb; ++c) {
-    const long long b0 = tail_bound(c, a);
-    if (b0 == tail_bound(c + 1, a)) continue;  // empty run
-    M = fmaxf(M, __ldcg(reinterpret_cast<const float*>(record(c, b0) + REC_M) + t * QT + r));
-  }
+  const size_t row = (size_t)(t * QT + r);
+  float M = -INFINITY, wsum = 0.f;
   float acc[D];
 #pragma unroll
   for (int d = 0; d < D; ++d) acc[d] = 0.f;
-  float wsum = 0.f;
   for (int c = ca; c <= cb; ++c) {
-    const long long b0 = tail_bound(c, a);
-    if (b0 == tail_bound(c + 1, a)) continue;
-    const uint8_t* base = record(c, b0);
-    const float m = __ldcg(reinterpret_cast<const float*>(base + REC_M) + t * QT + r);
-    const float w = __ldcg(reinterpret_cast<const float*>(base + REC_L) + t * QT + r) * exp2f(m - M);
-    wsum += w;
-    const uint4* src = reinterpret_cast<const uint4*>(base + ((size_t)(t * QT + r) * D) * 2);
+    const int b0 = tb[c];
+    if (b0 == tb[c + 1]) continue;  // empty run
+    // a CTA's first tail segment, or the last one of the CTA that started before the unit
+    const uint8_t* base = a.part + (size_t)((c == ca && b0 != s_a) ? a.G + ut : c) * REC_BYTES;
+    const float m = __ldcg(reinterpret_cast<const float*>(base + REC_M) + row);
+    const float l = __ldcg(reinterpret_cast<const float*>(base + REC_L) + row);
+    const uint4* src = reinterpret_cast<const uint4*>(base + row * D * 2);
     uint4 u[D / 8];
 #pragma unroll
     for (int q = 0; q < D / 8; ++q) u[q] = __ldcg(src + q);
+    const float mn = fmaxf(M, m);
+    const float sc = exp2f(M - mn), w = l * exp2f(m - mn);
+    M = mn;
+    wsum = fmaf(wsum, sc, w);
 #pragma unroll
     for (int q = 0; q < D / 8; ++q) {
       const uint32_t hw[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[k]));
-        acc[8 * q + 2 * k] = fmaf(w, f.x, acc[8 * q + 2 * k]);
-        acc[8 * q + 2 * k + 1] = fmaf(w, f.y, acc[8 * q + 2 * k + 1]);
+        acc[8 * q + 2 * k] = fmaf(w, f.x, acc[8 * q + 2 * k] * sc);
+        acc[8 * q + 2 * k + 1] = fmaf(w, f.y, acc[8 * q + 2 * k + 1] * sc);
       }
     }
   }
-  const int row_in_patch = up.q0 + t * QT + r;
-  if (row_in_patch >= a.Lp) return;
   __nv_bfloat16* dst =
       a.o + ((long long)up.b * a.L + up.patch0 + row_in_patch) * (long long)(a.heads * D) + up.h * D;
   const float inv = pow2(-e) / wsum;
@@ -434,6 +448,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  __shared__ int tb[MAX_G + 1];  // tail_bound(c) < 2^31: the plan limits tiles x key tiles
+  for (int c = threadIdx.x; c <= a.G && c <= MAX_G; c += blockDim.x) tb[c] = c * a.tq + c * a.tr / a.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -636,8 +652,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       for (int v = 0; v < sc.nsteps && ok;) {
         const Seg sg = seg_at(sc, v, a);
         const UnitPos up = unit_pos(sg.u, a);
-        const int e = v_exponent(a, up.b, up.h);
-        const float scale = pow2(e);
+        const float scale = pow2(v_exponent(vmax_bits(a, up.b, up.h)));
         for (const int vend = v + sg.len; v < vend; ++v) {
           const int st = v % KV_STAGES;
           if (!wait_or_abort(&bars->v_full[st], (v / KV_STAGES) & 1, a, bars)) {
@@ -684,7 +699,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       const Seg sg = seg_at(sc, v, a);
       const int vbeg = v, vend = v + sg.len;
       const UnitPos up = unit_pos(sg.u, a);
-      const int e_cur = v_exponent(a, up.b, up.h);
+      const int e_cur = v_exponent(vmax_bits(a, up.b, up.h));
       float m_ref = -INFINITY, l = 0.f;
       for (int j = sg.j0; v < vend; ++v, ++j) {
         // S_t(v) ready (the MMA thread issues it before P_t(v-1) V(v-1), which may still
@@ -795,9 +810,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           if (wait_or_abort(&bars->rec_done[t], pieces & 1, a, bars)) {
             __threadfence();
             const long long s_a = (long long)ut * a.nkt;
-            const int ca = tail_cta(s_a, a), cb = tail_cta(s_a + a.nkt - 1, a);
+            const int ca = tail_cta_tb(tb, s_a, a.G), cb = tail_cta_tb(tb, s_a + a.nkt - 1, a.G);
             int np = 0;
-            for (int c = ca; c <= cb; ++c) np += tail_bound(c, a) != tail_bound(c + 1, a);
+            for (int c = ca; c <= cb; ++c) np += tb[c] != tb[c + 1];
             const bool last = atomicAdd(&a.cnt[2 * ut + t], 1) == np - 1;
             if (last) atomicExch(&a.cnt[2 * ut + t], 0);  // all arrived: ready for the next call
             from = last ? ca : -1;
@@ -812,7 +827,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         const int ca = bars->merge_from[t], cb = bars->merge_to[t];
         if (ca >= 0) {
           __threadfence();
-          merge_rows(a, ut, t, r, ca, cb, up, e_cur);
+          merge_rows(a, tb, ut, t, r, ca, cb, up, e_cur);
         }
       }
       if (sg.tail) tail_seen = true;
@@ -866,7 +881,8 @@ bool plan(int B, int L, int heads, int P, bool split, AttnArgs* a) {
   const int sms = dpp_host::sm_count();
   if (split) {
     const long long T = U * a->nkt;
-    a->G = (int)(T < sms ? T : sms);
+    const int gmax = sms < MAX_G ? sms : MAX_G;  // the CTAs' table of tail runs
+    a->G = (int)(T < gmax ? T : gmax);
     a->W = a->U / a->G;
     // The last full round joins the leftover units in the shared tail: each CTA's
     // tail run is then longer than a unit, so a cut unit has at most two pieces
@@ -881,6 +897,8 @@ bool plan(int B, int L, int heads, int P, bool split, AttnArgs* a) {
   } else {
     a->G = (int)(U < sms ? U : sms);
   }
+  a->tq = (int)(a->tailT / a->G);
+  a->tr = (int)(a->tailT % a->G);
   a->skip_load = -1;
   return true;
 }

@@ -10,6 +10,8 @@ ties to even, clamped to +-127.  Inputs that a random draw almost never produces
     whose quotients sit within an ulp of the half-integer;
   * clamp edge: several elements at +-a, where the rounded scale makes |a/s| a hair
     above or below 127;
+  * scales just above and just below 2^-96, with ties (a kernel may form the quotient
+    differently on the two sides of such a threshold);
   * subnormal scales: a block maximum so small that a/127 is an fp32 subnormal, with
     ties constructed there too.
 
@@ -140,6 +142,22 @@ def edge_blocks(dtype: str, seed: int = 0):
         if min(found.values()) >= 2:
             break
     assert min(found.values()) >= 1
+    # scales just above and just below 2^-96 (not powers of two), with ties
+    t96 = F32(2.0 ** -96)
+    side = {True: None, False: None}
+    for a in _bf16_grid(float(F32(120.0) * t96), float(F32(134.0) * t96)):
+        s = F32(a / F32(127.0))
+        if (s.view(np.uint32) & 0x7FFFFF) == 0:
+            continue
+        key = bool(s >= t96)
+        if side[key] is None or abs(float(s) - float(t96)) < abs(float(side[key][1]) - float(t96)):
+            side[key] = (a, s)
+    for key in (True, False):
+        a, s = side[key]
+        fr, st = _tie_pairs_f32(s, ks, rng) if dtype == "f32" else _tie_pairs_bf16(s, ks, rng)
+        assert fr.size > 0
+        blocks.append(_block(a, fr, st, rng, dtype))
+        what.append(f"scale {'>=' if key else '<'} 2^-96, a={float(a):.6g}, {fr.size} tie elements")
     # subnormal scales (a / 127 below FLT_MIN), with ties constructed there too
     for amax in (1.0e-37, 3.0e-38, 1.0e-36):
         a = F32(amax) if dtype == "f32" else _bf16_round(F32(amax))[()]

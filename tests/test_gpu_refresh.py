@@ -99,17 +99,16 @@ def test_apply_residual_matches_oracle_bitexact(dtype, n):
     np.testing.assert_array_equal(np64(copy), en)
 
 
-@pytest.mark.parametrize("form", ["1", "2"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_refresh_edge_blocks_bitexact(dtype, form, monkeypatch):
+def test_refresh_edge_blocks_bitexact(dtype):
     """Blocks at the quantiser's edges (tests/refresh_edges.py): half-integer quotients
     with scales that are not powers of two and their neighbours, |a/s| just above and
-    below 127, subnormal scales.  Each form of the kernel's quantiser (form 1: a branch
-    per element, form 2: branch-free), and the scalar pass on a ragged copy of the first
-    blocks, give the oracle's codes, scales and refreshed values bit for bit; the
-    receiver's apply of the oracle's message gives its refreshed buffer."""
+    below 127, scales just above and below 2^-96 (where the kernel switches from its
+    division-free quotient to the IEEE division) and subnormal scales.  The streaming
+    loop, and the scalar pass on a ragged copy of the first blocks, give the oracle's
+    codes, scales and refreshed values bit for bit; the receiver's apply of the oracle's
+    message gives its refreshed buffer."""
     from tests.refresh_edges import edge_blocks
-    monkeypatch.setenv("DPP_DEBUG_REFRESH_FORM", form)
     f64, s64, _ = edge_blocks(dtype)
     f64 = np.concatenate([f64, f64[:200]])
     s64 = np.concatenate([s64, s64[:200]])
