@@ -38,17 +38,17 @@ METRIC = "patch-layer steps/s; attention TFLOP/s & refresh GB/s as % of GB300 ro
 # (its summary is under profiles/); None where no capture of the current version
 # exists.  Writes that are still in L2 when a kernel ends are not counted by the capture.
 TRAFFIC = {
-    "attention_sdxl1024_step": 52.53e6,
+    "attention_sdxl1024_step": None,
     "conv_sdxl1024_step": 18.89e6,
     "qkv_proj_sdxl1024_step": 12.97e6,
     "out_proj_sdxl1024_step": 11.33e6,
     "groupnorm_sdxl1024_step": 31.59e6,
-    "refresh_sdxl1024_step": 43.94e6,
-    "attention_sdxl3840": 1014.4e6,
+    "refresh_sdxl1024_step": None,
+    "attention_sdxl3840": None,
     "conv_vae_1x256x256x512": 94.26e6,
     "conv_sdxl3840_latent_step": 266.3e6,
-    "refresh_sweep_200MiB": 683.0e6,
-    "refresh_2x256x256x640_step": 1153.9e6,
+    "refresh_sweep_200MiB": None,
+    "refresh_2x256x256x640_step": None,
     "groupnorm_2x240x240x640_step": 531.1e6,
 }
 WORKLOAD = "sdxl1024_mid_b2_64x64_c640_p4_bf16"
