@@ -100,7 +100,7 @@ constexpr int REC_BYTES = REC_L + 2 * QT * 4;
 
 struct AttnArgs {
   int L, heads, P, Lp, g, n_pairs, nkt;
-  int* cnt;         // split: [tail unit][query tile] pieces finished (zero before the call)
+  int* cnt;         // split: [tail unit][query tile][warp] pieces finished (zero before the call)
   int U;            // units (batch, head, patch, pair of query tiles), pair fastest
   int G;            // CTAs
   int W;            // split: whole units per CTA (c, c+G, ...); 0 otherwise
@@ -119,11 +119,8 @@ struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[KV_STAGES], v_full[KV_STAGES], v_conv[KV_STAGES], kv_empty[KV_STAGES];
   uint64_t s_full[2], p_full[2], pv_done[2], drain;
-  uint64_t rec_done[2], merge_go[2];  // per tile: a cut unit's record written / merge decided
   uint32_t tmem_slot;
   int abort_flag;
-  int merge_from[2];  // per query tile: first CTA of the unit to merge, or -1
-  int merge_to[2];
 };
 static_assert(sizeof(Bars) <= 512, "barrier area");
 
@@ -138,13 +135,9 @@ __host__ __device__ __forceinline__ long long tail_bound(long long c, const Attn
   return c * a.tailT / a.G;
 }
 
-// The CTA whose tail run contains step s (ranges may be empty when tailT < G).
-__host__ __device__ __forceinline__ int tail_cta(long long s, const AttnArgs& a) {
-  return (int)(((s + 1) * a.G - 1) / a.tailT);
-}
-
-// The same from the CTA's table tb[c] = tail_bound(c) (no 64-bit divisions on the merge
-// path): the largest c < G with tb[c] <= s.
+// The CTA whose tail run contains step s (runs may be empty when tailT < G), from the
+// CTA's table tb[c] = tail_bound(c) (no 64-bit divisions on the merge path): the largest
+// c < G with tb[c] <= s.
 __device__ __forceinline__ int tail_cta_tb(const int* tb, long long s, int G) {
   int lo = 0, hi = G - 1;
   while (lo < hi) {
@@ -276,29 +269,41 @@ __device__ __forceinline__ void store_f16x16(uint4* d4, const uint32_t (&o)[16],
 // ca..cb (those with a non-empty run), in that order.  With pieces i = (m_i, l_i,
 // O_i/l_i), in one pass with a running maximum M: each piece rescales the sums so far by
 // 2^(M_old - M) and adds w_i = l_i 2^(m_i - M); o = sum_i w_i (O_i/l_i) / sum_i w_i,
-// times 2^-e (the records hold O in V's scaled units).  One round trip to L2 per piece.
-// The records were written by other SMs: read through L2 (ld.global.cg).
+// times 2^-e (the records hold O in V's scaled units).  The records were written by other
+// SMs and are complete when the merge starts; this SM has not read them before, so they
+// are prefetched into L1 (all pieces' round trips to L2 overlapped) and read from there.
 __device__ __forceinline__ void merge_rows(const AttnArgs& a, const int* tb, int ut, int t,
                                            int r, int ca, int cb, const UnitPos& up, int e) {
   const int row_in_patch = up.q0 + t * QT + r;
   if (row_in_patch >= a.Lp) return;
   const long long s_a = (long long)ut * a.nkt;
   const size_t row = (size_t)(t * QT + r);
+  // a CTA's first tail segment, or the last one of the CTA that started before the unit
+  auto record = [&](int c) -> const uint8_t* {
+    return a.part + (size_t)((c == ca && tb[c] != s_a) ? a.G + ut : c) * REC_BYTES;
+  };
+  // every piece's lines of this row into L1 first, so that their round trips to L2 overlap
+  // (the records are complete: the pieces' counter has been read)
+  for (int c = ca; c <= cb; ++c) {
+    if (tb[c] == tb[c + 1]) continue;
+    const uint8_t* base = record(c);
+    ptx::prefetch_l1(base + row * D * 2);
+    ptx::prefetch_l1(reinterpret_cast<const float*>(base + REC_M) + row);
+    ptx::prefetch_l1(reinterpret_cast<const float*>(base + REC_L) + row);
+  }
   float M = -INFINITY, wsum = 0.f;
   float acc[D];
 #pragma unroll
   for (int d = 0; d < D; ++d) acc[d] = 0.f;
   for (int c = ca; c <= cb; ++c) {
-    const int b0 = tb[c];
-    if (b0 == tb[c + 1]) continue;  // empty run
-    // a CTA's first tail segment, or the last one of the CTA that started before the unit
-    const uint8_t* base = a.part + (size_t)((c == ca && b0 != s_a) ? a.G + ut : c) * REC_BYTES;
-    const float m = __ldcg(reinterpret_cast<const float*>(base + REC_M) + row);
-    const float l = __ldcg(reinterpret_cast<const float*>(base + REC_L) + row);
+    if (tb[c] == tb[c + 1]) continue;  // empty run
+    const uint8_t* base = record(c);
+    const float m = __ldca(reinterpret_cast<const float*>(base + REC_M) + row);
+    const float l = __ldca(reinterpret_cast<const float*>(base + REC_L) + row);
     const uint4* src = reinterpret_cast<const uint4*>(base + row * D * 2);
     uint4 u[D / 8];
 #pragma unroll
-    for (int q = 0; q < D / 8; ++q) u[q] = __ldcg(src + q);
+    for (int q = 0; q < D / 8; ++q) u[q] = __ldca(src + q);
     const float mn = fmaxf(M, m);
     const float sc = exp2f(M - mn), w = l * exp2f(m - mn);
     M = mn;
@@ -467,8 +472,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       ptx::mbar_init(&bars->s_full[t], 1);
       ptx::mbar_init(&bars->p_full[t], 4);  // one arrival per softmax warp
       ptx::mbar_init(&bars->pv_done[t], 1);  // committed after each P V
-      ptx::mbar_init(&bars->rec_done[t], 4);  // one arrival per softmax warp
-      ptx::mbar_init(&bars->merge_go[t], 1);  // the warpgroup's deciding thread
     }
     ptx::mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -694,7 +697,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     const uint32_t tP = tmem + 384u + 64u * (uint32_t)t;  // P_t: 64 columns
     bool ok = true;
     bool tail_seen = false;  // a tail segment of this CTA has ended
-    uint32_t pieces = 0;     // pieces of cut units this warpgroup has recorded
     for (int v = 0, n = 0; v < sc.nsteps && ok; ++n) {
       const Seg sg = seg_at(sc, v, a);
       const int vbeg = v, vend = v + sg.len;
@@ -799,33 +801,22 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         }
         reinterpret_cast<float*>(base + REC_M)[t * QT + r] = m_ref;
         reinterpret_cast<float*>(base + REC_L)[t * QT + r] = l;
-        // The last piece of the unit to finish (for this query tile) merges them all.
-        // The hand-offs are mbarriers with bounded waits, so that a warp that gave up
-        // cannot leave the others waiting.
+        // The last piece of the unit to finish merges them all, warp by warp: each warp's
+        // 32 rows have their own counter, so that no warp waits for another.
         __threadfence();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bars->rec_done[t]);
-        if (quarter == 0 && lane == 0) {
-          int from = -1, to = 0;
-          if (wait_or_abort(&bars->rec_done[t], pieces & 1, a, bars)) {
-            __threadfence();
-            const long long s_a = (long long)ut * a.nkt;
-            const int ca = tail_cta_tb(tb, s_a, a.G), cb = tail_cta_tb(tb, s_a + a.nkt - 1, a.G);
-            int np = 0;
-            for (int c = ca; c <= cb; ++c) np += tb[c] != tb[c + 1];
-            const bool last = atomicAdd(&a.cnt[2 * ut + t], 1) == np - 1;
-            if (last) atomicExch(&a.cnt[2 * ut + t], 0);  // all arrived: ready for the next call
-            from = last ? ca : -1;
-            to = cb;
-          }
-          bars->merge_from[t] = from;
-          bars->merge_to[t] = to;
-          ptx::mbar_arrive(&bars->merge_go[t]);
+        const long long s_a = (long long)ut * a.nkt;
+        const int ca = tail_cta_tb(tb, s_a, a.G), cb = tail_cta_tb(tb, s_a + a.nkt - 1, a.G);
+        int last = 0;
+        if (lane == 0) {
+          int np = 0;
+          for (int c = ca; c <= cb; ++c) np += tb[c] != tb[c + 1];
+          int* cnt = a.cnt + (2 * ut + t) * 4 + quarter;
+          last = atomicAdd(cnt, 1) == np - 1;
+          if (last) atomicExch(cnt, 0);  // all arrived: ready for the next call
         }
-        if (!wait_or_abort(&bars->merge_go[t], pieces & 1, a, bars)) { ok = false; break; }
-        ++pieces;
-        const int ca = bars->merge_from[t], cb = bars->merge_to[t];
-        if (ca >= 0) {
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+          __syncwarp();
           __threadfence();
           merge_rows(a, tb, ut, t, r, ca, cb, up, e_cur);
         }
@@ -906,11 +897,11 @@ bool plan(int B, int L, int heads, int P, bool split, AttnArgs* a) {
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 // The scratch buffer: the per-(batch, head) maxima of |V|, then (split schedule) the
-// per-(tail unit, query tile) counters and the partial records.  The maxima and the
+// per-(tail unit, query tile, warp) counters and the partial records.  The maxima and the
 // counters must be zero when a launch starts.
 size_t vmax_bytes(int B, int heads) { return align256((size_t)B * heads * sizeof(unsigned)); }
-size_t counter_bytes(const AttnArgs& a) {
-  return a.split ? align256((size_t)2 * (a.U - a.W * a.G) * sizeof(int)) : 0;
+size_t counter_bytes(const AttnArgs& a) {  // per (tail unit, query tile, 32-row warp)
+  return a.split ? align256((size_t)8 * (a.U - a.W * a.G) * sizeof(int)) : 0;
 }
 size_t record_bytes(const AttnArgs& a) {
   return a.split ? (size_t)(a.G + (a.U - a.W * a.G)) * REC_BYTES : 0;
