@@ -38,17 +38,17 @@ METRIC = "patch-layer steps/s; attention TFLOP/s & refresh GB/s as % of GB300 ro
 # (its summary is under profiles/); None where no capture of the current version
 # exists.  Writes that are still in L2 when a kernel ends are not counted by the capture.
 TRAFFIC = {
-    "attention_sdxl1024_step": None,
+    "attention_sdxl1024_step": 52.53e6,
     "conv_sdxl1024_step": 18.89e6,
     "qkv_proj_sdxl1024_step": 12.97e6,
     "out_proj_sdxl1024_step": 11.33e6,
     "groupnorm_sdxl1024_step": 31.59e6,
-    "refresh_sdxl1024_step": None,
-    "attention_sdxl3840": None,
+    "refresh_sdxl1024_step": 43.96e6,
+    "attention_sdxl3840": 996.5e6,
     "conv_vae_1x256x256x512": 94.26e6,
     "conv_sdxl3840_latent_step": 266.3e6,
-    "refresh_sweep_200MiB": None,
-    "refresh_2x256x256x640_step": None,
+    "refresh_sweep_200MiB": 684.9e6,
+    "refresh_2x256x256x640_step": 1156.3e6,
     "groupnorm_2x240x240x640_step": 531.1e6,
 }
 WORKLOAD = "sdxl1024_mid_b2_64x64_c640_p4_bf16"
@@ -478,9 +478,10 @@ def run_gpu(args):
             _roof("conv_vae_1x256x256x512", "tc_gemm_kernel<conv>", "tensor",
                   vae["flop_per_launch"], vae["ms_mean"], peaks,
                   "2*H*W*C*9*C, 1x256x256, 512->512, P=8 (standalone, L2 flushed)"),
-            _roof("conv_sdxl3840_latent_step", "tc_gemm_kernel<conv, wrapping segments>",
+            _roof("conv_sdxl3840_latent_step", "tc_gemm_kernel<conv, padded row tiles>",
                   "tensor", lat["conv_flop"], lat["stage_ms"]["halo_conv"], peaks,
-                  "2*B*H*W*C*9*C, 2x240x240, 640->640, P=8 (W=240: 16-pixel row segments)"),
+                  "2*B*H*W*C*9*C, 2x240x240, 640->640, P=8 (W=240: tiles of 120 pixels of "
+                  "one row)"),
             _roof("refresh_sweep_200MiB", "refresh_kernel", "hbm", sweep["bytes_per_launch"],
                   sweep["ms_mean"], peaks,
                   "7.03125 B per element x 104988672 (standalone, L2 flushed)"),
@@ -961,6 +962,27 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+ONLY = {
+    "attention_sdxl3840": lambda dev, peaks: measure_attention_3840(dev, peaks),
+    "refresh_sweep": lambda dev, peaks: measure_refresh_sweep(dev, peaks),
+    "layer_2x256x256x640": lambda dev, peaks: measure_large_layer(dev, peaks),
+    "layer_sdxl3840_2x240x240x640": lambda dev, peaks: measure_large_layer(dev, peaks, H=240,
+                                                                           W=240),
+    "halo_conv_vae": lambda dev, peaks: measure_vae_conv(dev, peaks),
+}
+
+
+def run_only(name):
+    import torch
+
+    import stale_activations_gb300 as dpp
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dpp.load()
+    res = ONLY[name](dev, _peaks())
+    print(json.dumps({"only": name, **res}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -974,7 +996,13 @@ def main():
     ap.add_argument("--no-oracle-plan", action="store_true",
                     help="skip the oracle timings of the five workloads on the host cores")
     ap.add_argument("--oracle-plan-child", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--only", default=None, choices=sorted(ONLY),
+                    help="run one secondary measurement alone and print its line (for "
+                         "profiling one workload's kernels; no headline line)")
     args = ap.parse_args()
+    if args.only:
+        run_only(args.only)
+        return
     if args.oracle_plan_child:
         _oracle_plan_child(args.oracle_plan_child)
         return
