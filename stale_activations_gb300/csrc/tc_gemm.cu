@@ -267,8 +267,43 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
         // working on the same B tile at the same time fetch different slices (no
         // hot spot on one L2 slice) while a given tile always sums in one order.
         const int rot = (int)(mt % args.nkb);
+        // Per tile, once: for each row shift di and A box bx, whether the source row is
+        // the neighbouring band's halo (stale map) and, for the GroupNorm warps, whether it
+        // is an in-band row of the image (fresh x).  Bit (di + 1) * 16 + bx; the per-slice
+        // path then holds no division (the single producer thread's issue time bounds the
+        // slice rate: measured, each further box with its divisions cost ~0.2 us a slice).
+        uint64_t stale_bits = 0, fresh_bits = 0;
+        if (CONV) {
+          int rk = r, ck = c0;  // image row and column of box bx's first pixel
+          for (int bx = 0; bx < args.boxes; ++bx) {
+            for (int d = -1; d <= 1; ++d) {
+              const int rr = rk + d;
+              const bool in = rr >= 0 && rr < args.H;
+              const bool same = in && (rr / args.Hp) == (rk / args.Hp);
+              if (in && !same) stale_bits |= 1ull << ((d + 1) * 16 + bx);
+              if (same) fresh_bits |= 1ull << ((d + 1) * 16 + bx);
+            }
+            if (AMODE == 1) {
+              ck += args.box_px;
+              if (ck == args.W) {
+                ck = 0;
+                ++rk;
+              }
+            } else {
+              ++rk;
+            }
+          }
+        }
+        // the current slice kb and its tap (di, dj) and input-channel block cb, advanced
+        // by one slice at a time
+        int kb = rot, cb = 0, di = -1, dj = -1;
+        if (CONV) {
+          const int tap = rot / args.cin_blocks;
+          cb = rot - tap * args.cin_blocks;
+          di = tap / 3 - 1;
+          dj = tap - 3 * (tap / 3) - 1;
+        }
         for (int kq = 0; kq < args.nkb; ++kq, ++g) {
-          const int kb = kq + rot < args.nkb ? kq + rot : kq + rot - args.nkb;
           const int s = (int)(g % STAGES);
           const uint32_t ph = (uint32_t)((g / STAGES) & 1);
           if (!ptx::mbar_wait(&empty[s], ph ^ 1, args.wait_limit, abort_flag)) {
@@ -277,60 +312,57 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
             ok = false;
             break;
           }
-          if (g == args.skip_load) continue;  // test hook: this slice never lands
-          uint8_t* a_dst = smem + s * C::STAGE_BYTES;
-          uint8_t* b_dst = a_dst + C::A_BYTES;
-          if (GNF) {  // the note first: the arrive below releases it to the waiters
-            const int tap = kb / args.cin_blocks;
-            const int di = tap / 3 - 1;
-            uint32_t fresh = 0;
-            for (int bx = 0; bx < args.boxes; ++bx) {
-              const int rk = r + bx, rr = rk + di;
-              if (rr >= 0 && rr < args.H && (rr / args.Hp) == (rk / args.Hp)) fresh |= 1u << bx;
-            }
-            note[s] = StageNote{c0 + tap % 3 - 1, (int)fresh};
-          }
-          // padded row tiles: only box_px of the 128 A rows are loaded (the MMA rows past
-          // them compute values that the epilogue never stores)
-          ptx::mbar_arrive_expect_tx(
-              &full[s], AMODE == 2 ? (uint32_t)(args.box_px * 128 + C::B_BYTES) : C::STAGE_BYTES);
-          if (CONV) {
-            const int tap = kb / args.cin_blocks;
-            const int cb = kb - tap * args.cin_blocks;
-            const int di = tap / 3 - 1, dj = tap % 3 - 1;
-            // box bx holds pixels [m0 + bx * box_px, +box_px) of the image: one row
-            // segment (box_px divides W).  Whole rows (box_px == W) or one box per tile
-            // (W a multiple of 128): box bx is row r + bx from column c0; with WRAP the
-            // segments wrap across rows.
-            if (AMODE != 1) {
-              for (int bx = 0; bx < args.boxes; ++bx) {
-                const int rk = r + bx;   // image row of this box's pixels
-                const int rr = rk + di;  // source row
-                const bool stale = rr >= 0 && rr < args.H && (rr / args.Hp) != (rk / args.Hp);
-                ptx::tma_load_4d(a_dst + bx * args.box_px * 128, stale ? &tmA2 : &tmA,
-                                 &full[s], cb * BK, c0 + dj, rr, b);
-              }
-            } else {
+          if (g != args.skip_load) {  // test hook: that slice never lands
+            uint8_t* a_dst = smem + s * C::STAGE_BYTES;
+            uint8_t* b_dst = a_dst + C::A_BYTES;
+            const int sh = (di + 1) * 16;
+            if (GNF)  // the note first: the arrive below releases it to the waiters
+              note[s] = StageNote{c0 + dj, (int)((fresh_bits >> sh) & 0xFFFFu)};
+            // padded row tiles: only box_px of the 128 A rows are loaded (the MMA rows past
+            // them compute values that the epilogue never stores)
+            ptx::mbar_arrive_expect_tx(
+                &full[s], AMODE == 2 ? (uint32_t)(args.box_px * 128 + C::B_BYTES) : C::STAGE_BYTES);
+            if (CONV) {
+              // box bx holds pixels [m0 + bx * box_px, +box_px) of the image: one row
+              // segment (box_px divides W).  Whole rows (box_px == W) or one box per tile
+              // (W a multiple of 128): box bx is row r + bx from column c0; with WRAP the
+              // segments wrap across rows.
               int rk = r, ck = c0;
               for (int bx = 0; bx < args.boxes; ++bx) {
-                const int rr = rk + di;
-                const bool stale = rr >= 0 && rr < args.H && (rr / args.Hp) != (rk / args.Hp);
+                const bool stale = (stale_bits >> (sh + bx)) & 1u;
                 ptx::tma_load_4d(a_dst + bx * args.box_px * 128, stale ? &tmA2 : &tmA,
-                                 &full[s], cb * BK, ck + dj, rr, b);
-                ck += args.box_px;
-                if (ck == args.W) {
-                  ck = 0;
+                                 &full[s], cb * BK, ck + dj, rk + di, b);
+                if (AMODE == 1) {
+                  ck += args.box_px;
+                  if (ck == args.W) {
+                    ck = 0;
+                    ++rk;
+                  }
+                } else {
                   ++rk;
                 }
               }
+            } else {
+              ptx::tma_load_2d(a_dst, &tmA, &full[s], kb * BK, (int)m0);
             }
-          } else {
-            ptx::tma_load_2d(a_dst, &tmA, &full[s], kb * BK, (int)m0);
-          }
 #pragma unroll
-          for (int h = 0; h < C::NMMA; ++h)
-            ptx::tma_load_2d(b_dst + h * C::MMA_N * 128, &tmB, &full[s], kb * BK,
-                             n0 + h * C::MMA_N);
+            for (int h = 0; h < C::NMMA; ++h)
+              ptx::tma_load_2d(b_dst + h * C::MMA_N * 128, &tmB, &full[s], kb * BK,
+                               n0 + h * C::MMA_N);
+          }
+          // the next slice in the rotated order
+          if (++kb == args.nkb) {
+            kb = 0;
+            cb = 0;
+            di = -1;
+            dj = -1;
+          } else if (CONV && ++cb == args.cin_blocks) {
+            cb = 0;
+            if (++dj == 2) {
+              dj = -1;
+              ++di;
+            }
+          }
         }
       }
       if (*abort_flag) {  // wait for own copies still in flight before the CTA may exit

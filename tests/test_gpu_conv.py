@@ -28,6 +28,7 @@ def _conv_gpu(yf, ys, w, P):
     ("bf16", 1, 8, 256, 64, 128, 2),      # half a row per tile
     ("bf16", 1, 16, 32, 64, 256, 4),      # 4 rows per tile
     ("bf16", 1, 16, 128, 192, 128, 8),    # one row per tile, 1-row bands (both halos stale)
+    ("bf16", 1, 8, 64, 64, 128, 8),       # 2 rows per tile, 1-row bands: both rows' halos stale
     ("bf16", 1, 16, 64, 256, 320, 2),     # 36 K slices: 128 x 320 tiles (two MMAs per step)
     ("bf16", 1, 160, 128, 256, 320, 4),   # 160 such tiles: some CTAs reuse one accumulator
     # W neither a divisor nor a multiple of 128: tiles of 128 / gcd(W, 128) row segments
@@ -45,11 +46,14 @@ def test_conv_matches_oracle(dtype, B, H, W, Cin, Cout, P):
     assert rel_err(np64(out), ref) < (TOL_BF16 if dtype == "bf16" else TOL_F32)
 
 
-@pytest.mark.parametrize("W", [32, 64, 256, 240, 40])
-def test_conv_sentinel_halo_rows_bitexact(W):
+@pytest.mark.parametrize("W,P", [(32, 4), (64, 4), (256, 4), (240, 4), (40, 4), (64, 16),
+                                 (32, 16), (16, 2)])
+def test_conv_sentinel_halo_rows_bitexact(W, P):
     """fresh = +1, stale = -1 and one-hot weights (output channel o reads tap o % 9
-    of input channel o % Cin): every output is -1, 0 or +1 by the band rule alone."""
-    B, H, Cin, Cout, P = 1, 16, 64, 128, 4
+    of input channel o % Cin): every output is -1, 0 or +1 by the band rule alone.  Whole-row
+    tiles (W = 16, 32, 64) with 4-row bands, tiles that are whole bands (W = 16, 8-row bands)
+    and 1-row bands (every shifted row from the stale map)."""
+    B, H, Cin, Cout = 1, 16, 64, 128
     yf = torch.ones(B, H, W, Cin, dtype=torch.bfloat16)
     ys = -torch.ones(B, H, W, Cin, dtype=torch.bfloat16)
     w = torch.zeros(Cout, 3, 3, Cin, dtype=torch.bfloat16)
