@@ -8,9 +8,9 @@
 //   tap's source row taken from the fresh map inside r's band, from the stale
 //   map for the band's two halo rows, zero outside the image ("Benchmarking
 //   DistVAE", Glossary: halo rows of a sharded convolution).
-// simt_attention: one thread per query row of one patch and head; 64-key tiles
-//   of the spliced K/V (own patch fresh, other rows stale) in shared memory;
-//   online softmax in fp32.
+// simt_attention: one warp per query row of one patch and head (lanes split the keys);
+//   64-key tiles of the spliced K/V (own patch fresh, other rows stale) in shared
+//   memory; online softmax in fp32.
 #include "simt.cuh"
 
 namespace dpp {
@@ -90,35 +90,43 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(ALoad A, const T* __rest
   }
 }
 
+// One warp per query row (8 rows per block), each lane taking keys kk = lane and
+// lane + 32 of every 64-key tile with its own online-softmax state (m, l, acc[64]); the
+// lanes' states are merged once at the end (warp maximum of m, then warp sums of the
+// rescaled l and acc).  Padded shared rows keep the lanes' reads of 32 different keys on
+// 32 different banks.
 template <typename T>
-__global__ void __launch_bounds__(128) simt_attention_kernel(const T* __restrict__ q,
+__global__ void __launch_bounds__(256) simt_attention_kernel(const T* __restrict__ q,
                                                              const T* __restrict__ kf,
                                                              const T* __restrict__ vf,
                                                              const T* __restrict__ ks,
                                                              const T* __restrict__ vs,
                                                              T* __restrict__ o, int L, int heads,
                                                              int P) {
-  constexpr int D = 64, KT = 64;
+  constexpr int D = 64, KT = 64, ROWS = 8;
   __shared__ float Ks[KT][D + 1];
-  __shared__ float Vs[KT][D];
+  __shared__ float Vs[KT][D + 1];
   const int Lp = L / P;
-  const int tiles_per_patch = (Lp + 127) / 128;
-  const int p = blockIdx.x / tiles_per_patch;
-  const int qt = blockIdx.x - p * tiles_per_patch;
+  const int blocks_per_patch = (Lp + ROWS - 1) / ROWS;
+  const int p = blockIdx.x / blocks_per_patch;
+  const int qb = blockIdx.x - p * blocks_per_patch;
   const int h = blockIdx.y, b = blockIdx.z;
   const int C = heads * D;
-  const int t = p * Lp + qt * 128 + threadIdx.x;
-  const bool valid = qt * 128 + threadIdx.x < Lp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row_in_patch = qb * ROWS + warp;
+  const bool valid = row_in_patch < Lp;
   const long long rowbase = (long long)b * L;
+  const long long t = rowbase + p * Lp + (valid ? row_in_patch : 0);
   float qr[D], acc[D];
+#pragma unroll
   for (int e = 0; e < D; ++e) {
-    qr[e] = valid ? to_f32(q[(rowbase + t) * C + h * D + e]) * 0.125f : 0.f;  // 1/sqrt(64)
+    qr[e] = to_f32(q[t * C + h * D + e]) * 0.125f;  // 1/sqrt(64), exact
     acc[e] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
   for (int s0 = 0; s0 < L; s0 += KT) {
     __syncthreads();
-    for (int i = threadIdx.x; i < KT * D; i += 128) {
+    for (int i = threadIdx.x; i < KT * D; i += blockDim.x) {
       const int kk = i / D, e = i % D;
       const int s = s0 + kk;
       float kv = 0.f, vv = 0.f;
@@ -132,33 +140,46 @@ __global__ void __launch_bounds__(128) simt_attention_kernel(const T* __restrict
       Vs[kk][e] = vv;
     }
     __syncthreads();
-    const int nk = min(KT, L - s0);
-    float sc[KT];
-    float mt = m;
-#pragma unroll 4
-    for (int kk = 0; kk < KT; ++kk) {
+    float sc[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int kk = lane + 32 * j;
       float dot = 0.f;
 #pragma unroll
       for (int e = 0; e < D; ++e) dot = fmaf(qr[e], Ks[kk][e], dot);
-      sc[kk] = kk < nk ? dot : -INFINITY;
-      mt = fmaxf(mt, sc[kk]);
+      sc[j] = s0 + kk < L ? dot : -INFINITY;
     }
-    const float corr = expf(m - mt);  // m = -inf on the first tile gives 0
-    l *= corr;
+    const float mt = fmaxf(m, fmaxf(sc[0], sc[1]));
+    if (mt == -INFINITY) continue;  // no valid key for this lane yet
+    const float corr = expf(m - mt);  // m = -inf before the lane's first key gives 0
+    const float p0 = expf(sc[0] - mt), p1 = expf(sc[1] - mt);
+    l = fmaf(l, corr, p0 + p1);
 #pragma unroll
-    for (int e = 0; e < D; ++e) acc[e] *= corr;
+    for (int e = 0; e < D; ++e)
+      acc[e] = fmaf(p1, Vs[lane + 32][e], fmaf(p0, Vs[lane][e], acc[e] * corr));
     m = mt;
-#pragma unroll 4
-    for (int kk = 0; kk < KT; ++kk) {
-      const float pk = expf(sc[kk] - m);
-      l += pk;
+  }
+  // merge the 32 lanes' states
+  float M = m;
 #pragma unroll
-      for (int e = 0; e < D; ++e) acc[e] = fmaf(pk, Vs[kk][e], acc[e]);
-    }
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float f = m == -INFINITY ? 0.f : expf(m - M);
+  l *= f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+  float mine[2] = {0.f, 0.f};  // outputs e = lane and lane + 32
+#pragma unroll
+  for (int e = 0; e < D; ++e) {
+    float a = acc[e] * f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+    if (e == lane) mine[0] = a;
+    if (e == lane + 32) mine[1] = a;
   }
   if (valid) {
     const float inv = 1.f / l;
-    for (int e = 0; e < D; ++e) o[(rowbase + t) * C + h * D + e] = from_f32<T>(acc[e] * inv);
+    o[t * C + h * D + lane] = from_f32<T>(mine[0] * inv);
+    o[t * C + h * D + lane + 32] = from_f32<T>(mine[1] * inv);
   }
 }
 
@@ -197,14 +218,14 @@ int launch_simt_attention(const void* q, const void* kf, const void* vf, const v
                           const void* vs, void* o, int B, int L, int heads, int P, int dtype,
                           cudaStream_t stream) {
   const int Lp = L / P;
-  dim3 grid(P * ((Lp + 127) / 128), heads, B);
+  dim3 grid(P * ((Lp + 7) / 8), heads, B);  // 8 query rows (one warp each) per block
   if (dtype == DPP_BF16) {
     using T = __nv_bfloat16;
-    simt_attention_kernel<T><<<grid, 128, 0, stream>>>(
+    simt_attention_kernel<T><<<grid, 256, 0, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(kf), static_cast<const T*>(vf),
         static_cast<const T*>(ks), static_cast<const T*>(vs), static_cast<T*>(o), L, heads, P);
   } else {
-    simt_attention_kernel<float><<<grid, 128, 0, stream>>>(
+    simt_attention_kernel<float><<<grid, 256, 0, stream>>>(
         static_cast<const float*>(q), static_cast<const float*>(kf),
         static_cast<const float*>(vf), static_cast<const float*>(ks),
         static_cast<const float*>(vs), static_cast<float*>(o), L, heads, P);
