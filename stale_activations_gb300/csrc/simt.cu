@@ -15,12 +15,24 @@
 
 namespace dpp {
 
+// The A operand seen by one thread: a fixed set of rows (prepared once per row, no
+// divisions afterwards) and a column k that advances by 16 per K slice.
 struct ALinear {
   const void* a;
   int K;
+  struct Row {
+    long long m;
+    bool ok;
+  };
+  __device__ __forceinline__ Row row(long long m, long long M) const { return Row{m, m < M}; }
+  struct Col {
+    int k;
+  };
+  __device__ __forceinline__ Col col(int k) const { return Col{k}; }
+  __device__ __forceinline__ void advance(Col& c, int step) const { c.k += step; }
   template <typename T>
-  __device__ __forceinline__ float load(long long m, int k) const {
-    return to_f32(static_cast<const T*>(a)[m * K + k]);
+  __device__ __forceinline__ float load(const Row& r, const Col& c) const {
+    return r.ok && c.k < K ? to_f32(static_cast<const T*>(a)[r.m * K + c.k]) : 0.f;
   }
 };
 
@@ -28,22 +40,56 @@ struct AConv {
   const void* yf;
   const void* ys;
   int H, W, Cin, Hp;
-  template <typename T>
-  __device__ __forceinline__ float load(long long m, int k) const {
-    const int tap = k / Cin, ci = k - tap * Cin;
-    const int di = tap / 3 - 1, dj = tap % 3 - 1;
+  struct Row {  // pixel (b, r, c) and its band [lo, lo + Hp)
+    long long img;  // offset of image b
+    int r, c, lo;
+    bool ok;
+  };
+  __device__ __forceinline__ Row row(long long m, long long M) const {
+    Row x{};
+    x.ok = m < M;
     const long long hw = (long long)H * W;
-    const long long b = m / hw;
+    const long long b = x.ok ? m / hw : 0;
     const int rem = (int)(m - b * hw);
-    const int r = rem / W, c = rem - (rem / W) * W;
-    const int rr = r + di, cc = c + dj;
+    x.r = rem / W;
+    x.c = rem - x.r * W;
+    x.lo = (x.r / Hp) * Hp;
+    x.img = b * hw;
+    return x;
+  }
+  struct Col {  // k = tap * Cin + ci, tap = (di + 1) * 3 + (dj + 1)
+    int k, ci, di, dj;
+  };
+  __device__ __forceinline__ Col col(int k) const {
+    const int tap = k / Cin;
+    return Col{k, k - tap * Cin, tap / 3 - 1, tap % 3 - 1};
+  }
+  __device__ __forceinline__ void advance(Col& c, int step) const {
+    c.k += step;
+    c.ci += step;
+    while (c.ci >= Cin) {  // next tap
+      c.ci -= Cin;
+      if (++c.dj == 2) {
+        c.dj = -1;
+        ++c.di;
+      }
+    }
+  }
+  template <typename T>
+  __device__ __forceinline__ float load(const Row& x, const Col& k) const {
+    if (!x.ok || k.di > 1) return 0.f;  // past the last tap: K's ragged end
+    const int rr = x.r + k.di, cc = x.c + k.dj;
     if (rr < 0 || rr >= H || cc < 0 || cc >= W) return 0.f;
-    const bool own = (rr / Hp) == (r / Hp);
+    const bool own = rr >= x.lo && rr < x.lo + Hp;
     const T* src = static_cast<const T*>(own ? yf : ys);
-    return to_f32(src[((b * H + rr) * W + cc) * (long long)Cin + ci]);
+    return to_f32(src[(x.img + (long long)rr * W + cc) * Cin + k.ci]);
   }
 };
 
+// 64 x 64 output tile per block, 16-wide K slices in shared memory, 4 x 4 outputs per
+// thread; each thread fetches the same 4 rows of A (and of W) in every slice, so their
+// coordinates are prepared once, and the next slice's values are loaded into registers
+// while the current one is multiplied.
 template <typename T, typename ALoad>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(ALoad A, const T* __restrict__ Wt,
                                                         SimtOut out, long long M, int N, int K) {
@@ -52,22 +98,43 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(ALoad A, const T* __rest
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const long long m0 = (long long)blockIdx.y * 64;
   const int n0 = blockIdx.x * 64;
+  const int kk = threadIdx.x & 15;  // this thread's column within a slice
+  typename ALoad::Row rows[4];
+  bool nok[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int mm = (threadIdx.x >> 4) + 16 * i;
+    rows[i] = A.row(m0 + mm, M);
+    nok[i] = n0 + mm < N;
+  }
+  typename ALoad::Col ac = A.col(kk);
+  float ra[4], rb[4];
+  auto fetch = [&](int k) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ra[i] = A.template load<T>(rows[i], ac);
+      const int n = n0 + (threadIdx.x >> 4) + 16 * i;
+      rb[i] = nok[i] && k < K ? to_f32(Wt[(long long)n * K + k]) : 0.f;
+    }
+  };
+  fetch(kk);
   float acc[4][4] = {};
   for (int k0 = 0; k0 < K; k0 += 16) {
-    for (int i = threadIdx.x; i < 64 * 16; i += 256) {
-      const int mm = i / 16, kk = i % 16;
-      const long long m = m0 + mm;
-      const int k = k0 + kk;
-      As[kk][mm] = (m < M && k < K) ? A.template load<T>(m, k) : 0.f;
-      const int n = n0 + mm;
-      Bs[kk][mm] = (n < N && k < K) ? to_f32(Wt[(long long)n * K + k]) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      As[kk][(threadIdx.x >> 4) + 16 * i] = ra[i];
+      Bs[kk][(threadIdx.x >> 4) + 16 * i] = rb[i];
     }
     __syncthreads();
+    if (k0 + 16 < K) {  // the next slice's values, in flight during this slice's products
+      A.advance(ac, 16);
+      fetch(k0 + 16 + kk);
+    }
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
+    for (int q = 0; q < 16; ++q) {
       float a[4], bv[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) { a[i] = As[kk][ty * 4 + i]; bv[i] = Bs[kk][tx * 4 + i]; }
+      for (int i = 0; i < 4; ++i) { a[i] = As[q][ty * 4 + i]; bv[i] = Bs[q][tx * 4 + i]; }
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -124,22 +191,36 @@ __global__ void __launch_bounds__(256) simt_attention_kernel(const T* __restrict
     acc[e] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
-  for (int s0 = 0; s0 < L; s0 += KT) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < KT * D; i += blockDim.x) {
-      const int kk = i / D, e = i % D;
-      const int s = s0 + kk;
-      float kv = 0.f, vv = 0.f;
-      if (s < L) {
-        const bool own = s / Lp == p;
-        const long long off = (rowbase + s) * C + h * D + e;
-        kv = to_f32(own ? kf[off] : ks[off]);
-        vv = to_f32(own ? vf[off] : vs[off]);
+  // tile loads: thread -> key row tid / 4 of the tile, 16 of its 64 dimensions, all 32
+  // loads in flight before the stores; own patch's rows fresh, the others stale
+  const int lk = threadIdx.x >> 2, le = (threadIdx.x & 3) * 16;
+  const int own_lo = p * Lp, own_hi = own_lo + Lp;
+  float kv[16], vv[16];
+  auto fetch = [&](int s) {
+    if (s < L) {
+      const bool own = s >= own_lo && s < own_hi;
+      const T* kp = (own ? kf : ks) + (rowbase + s) * C + h * D + le;
+      const T* vp = (own ? vf : vs) + (rowbase + s) * C + h * D + le;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        kv[e] = to_f32(kp[e]);
+        vv[e] = to_f32(vp[e]);
       }
-      Ks[kk][e] = kv;
-      Vs[kk][e] = vv;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) kv[e] = vv[e] = 0.f;
+    }
+  };
+  fetch(lk);
+  for (int s0 = 0; s0 < L; s0 += KT) {
+    __syncthreads();  // the previous tile's products are done
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      Ks[lk][le + e] = kv[e];
+      Vs[lk][le + e] = vv[e];
     }
     __syncthreads();
+    if (s0 + KT < L) fetch(s0 + KT + lk);  // the next tile, in flight during this one
     float sc[2];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
