@@ -140,10 +140,11 @@ int layout(const dpp_layer_params* p, dpp_workspace_layout* o) {
 }
 
 int run_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,
-             int Cin, int Cout, int P, int dtype, const float* gn_par, int* st, cudaStream_t s) {
+             int Cin, int Cout, int P, int dtype, const float* gn_par, int* st, cudaStream_t s,
+             const void* vstale = nullptr, unsigned* vmax = nullptr, int heads = 0) {
   if (dtype == DPP_BF16)
     return dpp::launch_tc_conv(yf, ys, w, out, B, H, W, Cin, Cout, P, gn_par, st,
-                               dpp_host::wait_limit_from_env(), s);
+                               dpp_host::wait_limit_from_env(), s, vstale, Cout, vmax, heads);
   return dpp::launch_simt_conv(yf, ys, w, out, B, H, W, Cin, Cout, P, dtype, s);
 }
 
@@ -462,19 +463,24 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
   const bool fused = p.fuse_gn != 0;
   float* gn_params = fused ? reinterpret_cast<float*>(ws + lo.gn_params) : nullptr;
   // The attention's V scaling needs max |V| per (batch, head) of the V it reads: on the
-  // plain bf16 path the GroupNorm apply takes it over the stale V (a stale step with P > 1)
-  // and the Q/K/V projection's epilogue over the fresh V, instead of a separate pass.
+  // plain bf16 path the Q/K/V projection's epilogue takes it over the fresh V, and over
+  // the stale V (a stale step with P > 1) either the conv's epilogue warps, idle while
+  // its first accumulator fills, when each CTA's share is at most 256 rows (a few us of
+  // loads), or else the GroupNorm apply -- instead of a separate pass.
   const bool vmax_fold = p.dtype == DPP_BF16 && !fused && !fuse_rfx;
+  const bool vs_need = vmax_fold && !sync && p.P > 1;
+  const bool vs_in_conv = vs_need && M <= 256ll * dpp_host::sm_count();
   unsigned* vmax = reinterpret_cast<unsigned*>(ws + lo.attn_partial);
   rc = dpp::launch_gn(x, y, gn_partial, sync ? nullptr : st->gn_stats, gn_fresh, wts->gamma,
                       wts->beta, g, p.eps, sync ? DPP_GN_SYNC : p.gn_mode, p.dtype, status,
                       reinterpret_cast<int*>(ws + lo.attn_partial), ncnt, gn_params,
-                      fused ? 1 : 0, vmax_fold && !sync && p.P > 1 ? st->v_stale : nullptr,
-                      vmax, p.heads, s);
+                      fused ? 1 : 0, vs_need && !vs_in_conv ? st->v_stale : nullptr, vmax,
+                      p.heads, s);
   if (rc || (rc = mark(1))) return rc;
   // a3: halo conv, halo rows from the stale conv input (fresh at the synchronous step)
   rc = run_conv(fused ? x : y, sync ? y : st->y_stale, wts->w_conv, h, p.B, p.H, p.W, p.C, p.C,
-                p.P, p.dtype, gn_params, status, s);
+                p.P, p.dtype, gn_params, status, s,
+                vs_in_conv ? st->v_stale : nullptr, vmax, p.heads);
   if (rc || (rc = mark(2))) return rc;
   // a7 for the halo rows of y and a8, when the projection refreshes K and V: it runs
   // alongside the conv's end (it writes only the second state set and the message's

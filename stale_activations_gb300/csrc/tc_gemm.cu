@@ -86,6 +86,12 @@ struct GemmArgs {
   // vmax_L rows, 64-column head) into vmax as fp32 bits by atomicMax, or NULL
   unsigned* vmax;
   int vmax_L, vmax_heads;
+  // conv: max |V| per (batch of vmax_L rows, 64-column head) of this [vs_rows, vs_C] bf16
+  // tensor (the stale V) into vmax, by the epilogue warps while the first accumulator
+  // fills (NULL: none)
+  const __nv_bfloat16* vs_src;
+  long long vs_rows;
+  int vs_C;
 };
 
 // What the producer fetched into a stage, for the GroupNorm warps: the boxes' first
@@ -503,6 +509,39 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
     // accumulator g), so a refreshing epilogue may take two main loops' time.
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
     const int group = RFX ? (warp - 2) >> 2 : 0;
+    if (CONV && !GNF && args.vs_src) {
+      // This CTA's share of the rows, eight rows' loads in flight per thread; thread t
+      // takes the 16-byte columns t, t + 128, ... of each row (eight channels of one head)
+      // and keeps its maximum until the rows' batch changes.
+      const int et = threadIdx.x - 64, ncol = args.vs_C / 8;
+      const long long r0 = args.vs_rows * blockIdx.x / gridDim.x;
+      const long long r1 = args.vs_rows * (blockIdx.x + 1) / gridDim.x;
+      for (int cc = et; cc < ncol; cc += 128) {
+        uint32_t m = 0;
+        long long b = r0 / args.vmax_L, bend = (b + 1) * args.vmax_L;
+        for (long long row = r0; row < r1; row += 8) {
+          uint4 u[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (row + k < r1)
+              u[k] = __ldcs(reinterpret_cast<const uint4*>(args.vs_src + (row + k) * args.vs_C) + cc);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (row + k >= r1) break;
+            if (row + k == bend) {  // next batch: flush this one's maximum
+              if (m) atomicMax(args.vmax + b * args.vmax_heads + (cc * 8) / 64, m << 16);
+              m = 0;
+              ++b;
+              bend += args.vmax_L;
+            }
+            const uint32_t w4[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) m = max(m, max(w4[e] & 0x7FFFu, (w4[e] >> 16) & 0x7FFFu));
+          }
+        }
+        if (m) atomicMax(args.vmax + b * args.vmax_heads + (cc * 8) / 64, m << 16);
+      }
+    }
     int it = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
       if (RFX && (it & 1) != group) continue;
@@ -747,7 +786,8 @@ int launch_tc_linear_refresh(const void* a, const void* w, void* o0, void* o1, v
 
 int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,
                    int Cin, int Cout, int P, const float* gn_par, int* status,
-                   long long wait_limit, cudaStream_t s) {
+                   long long wait_limit, cudaStream_t s, const void* vstale, int vs_C,
+                   unsigned* vmax, int heads) {
   if (!tc_conv_supported(B, H, W, Cin, Cout, P)) return DPP_ERR_SHAPE;
   const int bn = pick_bn(Cout, Cout, 9 * Cin / BK);
   if (!bn) return DPP_ERR_SHAPE;
@@ -789,6 +829,15 @@ int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int
   g.box_px = box_px;
   g.gn_par = gn_par;
   g.P = P;
+  if (vstale && !gn_par) {  // [B, H*W, vs_C] stale V: its maxima by the epilogue warps
+    if (!vmax || vs_C % 64 || heads * 64 != vs_C) return DPP_ERR_SHAPE;
+    g.vs_src = static_cast<const __nv_bfloat16*>(vstale);
+    g.vs_rows = (long long)B * H * W;
+    g.vs_C = vs_C;
+    g.vmax = vmax;
+    g.vmax_L = H * W;
+    g.vmax_heads = heads;
+  }
   if (gn_par) return dispatch<true, true>(bn, tf, ts, tw, g, s);
   // each A staging mode is its own kernel instantiation, so that the common shapes keep
   // the simplest producer (a run-time branch alone cost the SDXL-1024 conv 7%)
