@@ -42,7 +42,7 @@ TRAFFIC = {
     "conv_sdxl1024_step": 18.89e6,
     "qkv_proj_sdxl1024_step": 12.97e6,
     "out_proj_sdxl1024_step": 11.33e6,
-    "groupnorm_sdxl1024_step": 31.59e6,
+    "groupnorm_sdxl1024_step": None,
     "refresh_sdxl1024_step": 43.96e6,
     "attention_sdxl3840": 996.5e6,
     "conv_vae_1x256x256x512": 94.26e6,
@@ -333,9 +333,9 @@ def run_gpu(args):
     qkv_flop = 2.0 * B * L * C * 3 * C
     o_flop = 2.0 * B * L * C * C
     act = B * L * C
-    # read x (stats), read x + write y (apply), and the stale V read on the way for the
-    # attention's per-(batch, head) V range
-    gn_bytes = 4 * act * 2
+    # x read by the stats and the apply kernel, y written (at this size the stale V's
+    # maximum for the attention's V range is taken by the conv, not by the GroupNorm)
+    gn_bytes = 3 * act * 2
     halo_elems = B * (P - 1) * 2 * cfg.W * C
     refresh_elems = 2 * act + halo_elems
     refresh_bytes = 7.03125 * refresh_elems
@@ -367,8 +367,8 @@ def run_gpu(args):
                   avg["out_proj"], peaks, f"2*M*C*C = {o_flop:.4g} FLOP"),
             _roof("groupnorm_sdxl1024_step", "gn_stats_kernel + gn_apply_kernel", "hbm",
                   gn_bytes, avg["groupnorm"], peaks,
-                  f"8 B per element x {act} = {gn_bytes:.4g} B: x read twice, y written, stale V "
-                  "read for the attention's V range (latency-bound at 42 MB)"),
+                  f"6 B per element x {act} = {gn_bytes:.4g} B: x read twice, y written "
+                  "(latency-bound at 31 MB)"),
             _roof("refresh_sdxl1024_step", "refresh_kernel", "hbm", refresh_bytes,
                   avg["state_update"], peaks,
                   f"7.03125 B per element x {refresh_elems} = {refresh_bytes:.4g} B")]
