@@ -39,14 +39,14 @@ METRIC = "patch-layer steps/s; attention TFLOP/s & refresh GB/s as % of GB300 ro
 # exists.  Writes that are still in L2 when a kernel ends are not counted by the capture.
 TRAFFIC = {
     "attention_sdxl1024_step": 52.53e6,
-    "conv_sdxl1024_step": 18.89e6,
-    "qkv_proj_sdxl1024_step": 12.97e6,
-    "out_proj_sdxl1024_step": 11.33e6,
+    "conv_sdxl1024_step": None,
+    "qkv_proj_sdxl1024_step": None,
+    "out_proj_sdxl1024_step": None,
     "groupnorm_sdxl1024_step": None,
     "refresh_sdxl1024_step": 43.96e6,
     "attention_sdxl3840": 996.5e6,
-    "conv_vae_1x256x256x512": 94.26e6,
-    "conv_sdxl3840_latent_step": 266.3e6,
+    "conv_vae_1x256x256x512": None,
+    "conv_sdxl3840_latent_step": None,
     "refresh_sweep_200MiB": 684.9e6,
     "refresh_2x256x256x640_step": 1156.3e6,
     "groupnorm_2x240x240x640_step": 531.1e6,
