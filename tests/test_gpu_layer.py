@@ -373,9 +373,10 @@ def test_layer_message_keeps_rank_copies_identical(name, dbuf, frx):
 def test_layer_v_outside_fp16_range(vshift):
     """The V projection weights scaled by 2^17 (V near 1e4..1e5, beyond fp16's 65504) or
     2^-20 (V in fp16's subnormal range): the layer step takes max |V| per (batch, head)
-    from the projection's epilogue (fresh V) and the GroupNorm pass (stale V) and scales
-    V by a power of two inside the attention.  A synchronous then a stale step; the
-    attention stage on the GPU's own Q, K, V and the state within the bf16 bound."""
+    from the projection's epilogue (fresh V) and, on this small map, the conv's epilogue
+    warps (stale V), and scales V by a power of two inside the attention.  A synchronous
+    then a stale step; the attention stage on the GPU's own Q, K, V and the state within
+    the bf16 bound."""
     cfg = CFGS["small_bf16"]
     wts = synth.layer_weights(cfg, seed=4, affine=True)
     C = cfg.C
@@ -404,3 +405,37 @@ def test_layer_v_outside_fp16_range(vshift):
                                   old["v_stale"].reshape(B, L, C), cfg.heads, cfg.P, "bf16")
     assert rel_err(v1["o"], o) < TOL_BF16
     assert rel_err(np64(out).reshape(B, L, C), oracle.linear(v1["o"], wn["w_o"], "bf16")) < TOL_BF16
+
+
+def test_layer_v_outside_fp16_range_large_map():
+    """The same with a map of 40960 rows (more than 256 per SM): there the GroupNorm apply
+    takes max |V_stale| instead of the conv (smaller maps).  V near 1e4..1e5 through the
+    projection weights times 2^17; a synchronous then a stale step; the attention stage on
+    the GPU's own Q, K, V and the old state, on 192 sampled query rows (the oracle would
+    need minutes for all of them), within the bf16 bound."""
+    cfg = synth.LayerConfig("large", B=1, H=320, W=128, C=128, P=4, G=8, heads=2,
+                            head_dim=64, dtype="bf16")
+    assert cfg.B * cfg.H * cfg.W > 256 * torch.cuda.get_device_properties(0).multi_processor_count
+    wts = synth.layer_weights(cfg, seed=5, affine=True)
+    C = cfg.C
+    w = wts["w_qkv"].clone()
+    w[2 * C:] = (w[2 * C:].float() * 2.0 ** 17).to(w.dtype)
+    wts["w_qkv"] = w
+    x, x_prev = synth.layer_inputs(cfg, seed=5)
+    prm = _params(cfg)
+    state, ws = dpp.alloc_layer(prm)
+    wd = {k: t.cuda() for k, t in wts.items()}
+    out = torch.empty(cfg.B, cfg.H, cfg.W, cfg.C, dtype=torch.bfloat16, device="cuda")
+    dpp.patch_layer_step(prm, wd, state, x_prev.cuda(), out, dpp.SYNC, ws)
+    assert dpp.read_device_status(ws) == 0
+    old = {k: np64(state[k]) for k in ("k_stale", "v_stale")}
+    assert np.abs(old["v_stale"]).max() > 65504
+    dpp.patch_layer_step(prm, wd, state, x.cuda(), out, dpp.STALE, ws)
+    assert dpp.read_device_status(ws) == 0
+    v1 = {k: np64(t) for k, t in dpp.workspace_views(prm, ws).items()}
+    B, L = cfg.B, cfg.L
+    rows = np.sort(np.random.default_rng(5).choice(L, 192, replace=False))
+    o = oracle.stale_kv_attention(v1["q"], v1["k"], v1["v"], old["k_stale"].reshape(B, L, C),
+                                  old["v_stale"].reshape(B, L, C), cfg.heads, cfg.P, "bf16",
+                                  rows=rows)
+    assert rel_err(v1["o"][:, rows], o) < TOL_BF16
