@@ -26,7 +26,9 @@
 //   warp 8           TMA producer: Q tiles per unit (two buffers), a 5-stage ring of K and V
 //                    tiles; each 128-key tile is fetched in sub-boxes of g rows
 //                    (g = largest power of two <= 128 dividing L/P), each sub-box
-//                    from the fresh or the stale tensor map -- the splice.
+//                    from the fresh or the stale tensor map -- the splice.  A stage is
+//                    refilled once the tile-1 softmax warps have seen P_1 V of its step
+//                    complete (every MMA that reads the stage is older than that one).
 //   warp 9           MMA issuer (one thread) and TMEM owner.  Per key tile j and
 //                    query tile t, once softmax t has written P_t(j):
 //                    S_t = Q_t K(j+1)^T (M=128, N=128, K=16 steps over d=64), then
@@ -41,8 +43,12 @@
 //                    one CTA at once faulted the GPU (an illegal memory access) in two
 //                    independent implementations.
 //   warps 10-11      widen each landed V tile from bf16 to fp16 in place (half a tile
-//                    each), times the (batch, head) power of two; the MMA thread waits
-//                    for this before P V.
+//                    each), times the (batch, head) power of two, and report V(v) ready
+//                    only once K(v+1) has landed too; the MMA thread waits for this
+//                    before the step's MMAs.  The single MMA thread is the pipeline's
+//                    bottleneck (its P arrives ~1000 cycles before it is free), and each
+//                    barrier test or commit it executes delays the next MMA batch; so
+//                    the K wait and the stage release are done by warps with slack.
 // P is rounded to fp16, not bf16: its 11-bit significand keeps the rounding of the
 // probabilities well inside the 2e-3 output tolerance (bf16's 8 bits would not), and
 // V is widened to fp16 so that P V runs as kind::f16 with both operands fp16.  fp16
@@ -466,7 +472,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       ptx::mbar_init(&bars->k_full[s], 1);
       ptx::mbar_init(&bars->v_full[s], 1);
       ptx::mbar_init(&bars->v_conv[s], NUM_CONVERTERS);
-      ptx::mbar_init(&bars->kv_empty[s], 1);
+      ptx::mbar_init(&bars->kv_empty[s], 4);  // the tile-1 softmax warps, after P_1 V
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(&bars->s_full[t], 1);
@@ -605,11 +611,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
             const uint32_t acc0 = v > vbeg ? 1u : 0u;
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
+              // P_t(v); once per step V(v) widened and K(v+1) landed (v_conv)
               if (!wait_or_abort(&bars->p_full[t], v & 1, a, bars) ||
                   (t == 0 && !wait_or_abort(&bars->v_conv[st], (v / KV_STAGES) & 1, a, bars)) ||
-                  (t == 0 && more &&
-                   !wait_or_abort(&bars->k_full[(v + 1) % KV_STAGES], ((v + 1) / KV_STAGES) & 1,
-                                  a, bars)) ||
                   (t == 0 && new_seg &&
                    !wait_or_abort(&bars->q_full[qn & 1], (qn >> 1) & 1, a, bars))) {
                 ok = false;
@@ -634,7 +638,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
               ptx::mma_commit(&bars->pv_done[t]);
             }
             if (!ok) break;
-            ptx::mma_commit(&bars->kv_empty[st]);
             // after a unit's last step every Q K^T of it has been issued: free its Q buffer
             if (last) ptx::mma_commit(&bars->q_empty[n & 1]);
           }
@@ -648,8 +651,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       // ------------------------------------------------ V widening (warps 10, 11)
       // Each landed V tile: this warp's half, 16 KB / 2 / 32 lanes = 16 vectors per lane,
       // in two passes of 8, bf16 -> fp16 times 2^e (exact: a power of two, and fp16 holds
-      // every bf16 value of the scaled range).  The MMA thread issues P V only after both
-      // halves are done (v_conv).
+      // every bf16 value of the scaled range).  The MMA thread issues step v's MMAs only
+      // after both halves are done and K(v+1) has landed (v_conv).
       const int half = warp - 10;
       bool ok = true;
       for (int v = 0; v < sc.nsteps && ok;) {
@@ -681,6 +684,13 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           }
           ptx::fence_proxy_async_smem();
           __syncwarp();
+          // S(v+1) = Q K(v+1)^T is issued in the same batch as P(v) V(v)
+          if (v + 1 < sc.nsteps &&
+              !wait_or_abort(&bars->k_full[(v + 1) % KV_STAGES], ((v + 1) / KV_STAGES) & 1, a,
+                             bars)) {
+            ok = false;
+            break;
+          }
           if (lane == 0) ptx::mbar_arrive(&bars->v_conv[st]);
         }
       }
@@ -746,6 +756,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           ok = false;
           break;
         }
+        if (t == 1 && v > vbeg) {  // K(v-1), V(v-1) no longer read: free their stage
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&bars->kv_empty[(v - 1) % KV_STAGES]);
+        }
         ptx::tc_fence_after();
         if (redo) {  // rescale the running O_t, then P from the scores in TMEM
 #pragma unroll 1
@@ -772,6 +786,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       if (!ok) break;
       // ---- end of the segment: O_t complete once its last P V has finished
       if (!wait_or_abort(&bars->pv_done[t], (vend - 1) & 1, a, bars)) { ok = false; break; }
+      if (t == 1) {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->kv_empty[(vend - 1) % KV_STAGES]);
+      }
       ptx::tc_fence_after();
       if (sg.j0 == 0 && sg.len == a.nkt) {  // whole unit: normalised bf16 output
         const float inv = pow2(-e_cur) / l;
