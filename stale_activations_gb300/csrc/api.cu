@@ -464,9 +464,9 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
   float* gn_params = fused ? reinterpret_cast<float*>(ws + lo.gn_params) : nullptr;
   // The attention's V scaling needs max |V| per (batch, head) of the V it reads: on the
   // plain bf16 path the Q/K/V projection's epilogue takes it over the fresh V, and over
-  // the stale V (a stale step with P > 1) either the conv's epilogue warps, idle while
-  // its first accumulator fills, when each CTA's share is at most 256 rows (a few us of
-  // loads), or else the GroupNorm apply -- instead of a separate pass.
+  // the stale V (a stale step with P > 1) the conv when each CTA's share is at most 256
+  // rows (CTAs of their own on the SMs its tiles leave idle, else its epilogue warps while
+  // the first accumulator fills), or else the GroupNorm apply -- not a separate pass.
   const bool vmax_fold = p.dtype == DPP_BF16 && !fused && !fuse_rfx;
   const bool vs_need = vmax_fold && !sync && p.P > 1;
   const bool vs_in_conv = vs_need && M <= 256ll * dpp_host::sm_count();

@@ -35,9 +35,10 @@ int launch_tc_linear_refresh(const void* a, const void* w, void* o0, void* o1, v
 // Implicit-GEMM halo conv3x3 (see halo_conv3x3 in dpp.h).  With gn_par non-NULL, yf is
 // the raw GroupNorm input x and the kernel applies GroupNorm to its in-band rows on the
 // fly (gn_par: [B][P][3][Cin] fp32 mean, rstd * gamma, beta); ys is the stale y.
-// vstale (bf16 [B, H*W, vs_C], may be NULL, not with gn_par): the conv's epilogue warps
-// also take its max |.| per (batch, head of 64 channels) into vmax [B][heads] as fp32 bits
-// by atomicMax (vmax zeroed before the launch), while the first accumulator fills.
+// vstale (bf16 [B, H*W, vs_C], may be NULL, not with gn_par): the launch also takes its
+// max |.| per (batch, head of 64 channels) into vmax [B][heads] as fp32 bits by atomicMax
+// (vmax zeroed before the launch): with extra CTAs on the SMs the tiles leave idle, or by
+// the epilogue warps while the first accumulator fills.
 int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int B, int H, int W,
                    int Cin, int Cout, int P, const float* gn_par, int* status,
                    long long wait_limit, cudaStream_t s, const void* vstale = nullptr,

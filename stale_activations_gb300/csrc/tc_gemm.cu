@@ -87,11 +87,12 @@ struct GemmArgs {
   unsigned* vmax;
   int vmax_L, vmax_heads;
   // conv: max |V| per (batch of vmax_L rows, 64-column head) of this [vs_rows, vs_C] bf16
-  // tensor (the stale V) into vmax, by the epilogue warps while the first accumulator
-  // fills (NULL: none)
+  // tensor (the stale V) into vmax (NULL: none); vs_scan = 1: by the CTAs past the last
+  // tile, which do nothing else; 0: by the epilogue warps while the first accumulator fills
   const __nv_bfloat16* vs_src;
   long long vs_rows;
   int vs_C;
+  int vs_scan;
 };
 
 // What the producer fetched into a stage, for the GroupNorm warps: the boxes' first
@@ -189,6 +190,47 @@ __device__ __forceinline__ void refresh_row(uint32_t t_row, __nv_bfloat16* dst, 
   }
 }
 
+// max |V| per (batch, head) over rows [vs_rows e / E, vs_rows (e + 1) / E) of the stale V,
+// by every thread of the CTA: virtual thread c takes the 16-byte column c mod ncol (eight
+// channels of one head) of rows r0 + c / ncol, then every rpp-th row, eight rows' loads in
+// flight, and flushes its maximum by atomicMax (fp32 bits of a non-negative value) when
+// its rows enter the next batch.
+__device__ __noinline__ void scan_vmax(const GemmArgs& a, int e, int E) {
+  const int ncol = a.vs_C / 8;
+  const int rpp = max(1, (int)blockDim.x / ncol);
+  const long long r0 = a.vs_rows * e / E, r1 = a.vs_rows * (e + 1) / E;
+  for (int c = threadIdx.x; c < ncol * rpp; c += blockDim.x) {
+    const int cc = c % ncol;
+    unsigned* const col_max = a.vmax + (cc * 8) / 64;
+    uint32_t m = 0;
+    long long row = r0 + c / ncol;
+    long long b = row / a.vmax_L, bend = (b + 1) * a.vmax_L;
+    for (; row < r1; row += 8ll * rpp) {
+      uint4 u[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (row + (long long)k * rpp < r1)
+          u[k] = __ldcs(reinterpret_cast<const uint4*>(a.vs_src + (row + (long long)k * rpp) *
+                                                                     a.vs_C) + cc);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const long long rk = row + (long long)k * rpp;
+        if (rk >= r1) break;
+        while (rk >= bend) {  // next batch: flush this one's maximum
+          if (m) atomicMax(col_max + b * a.vmax_heads, m << 16);
+          m = 0;
+          ++b;
+          bend += a.vmax_L;
+        }
+        const uint32_t w4[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m = max(m, max(w4[i] & 0x7FFFu, (w4[i] >> 16) & 0x7FFFu));
+      }
+    }
+    if (m) atomicMax(col_max + b * a.vmax_heads, m << 16);
+  }
+}
+
 // RFX (linear, 128-wide tiles): a K or V tile row is exactly one 128-element refresh
 // block, so the epilogue thread that stores a row of fresh K or V also quantises its
 // residual against the stale row and writes the refreshed row, the codes and the scale.
@@ -215,6 +257,13 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = args.m_tiles * args.n_tiles;
+  if constexpr (CONV && !GNF) {
+    if (args.vs_scan && (int)blockIdx.x >= ntiles) {  // no tile: the stale V's maxima only
+      ptx::grid_dep_wait();  // vmax was zeroed by an earlier kernel of the chain
+      scan_vmax(args, blockIdx.x - ntiles, gridDim.x - ntiles);
+      return;
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -509,7 +558,7 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
     // accumulator g), so a refreshing epilogue may take two main loops' time.
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
     const int group = RFX ? (warp - 2) >> 2 : 0;
-    if (CONV && !GNF && args.vs_src) {
+    if (CONV && !GNF && args.vs_src && !args.vs_scan) {
       // This CTA's share of the rows, eight rows' loads in flight per thread; thread t
       // takes the 16-byte columns t, t + 128, ... of each row (eight channels of one head)
       // and keeps its maximum until the rows' batch changes.
@@ -686,7 +735,15 @@ int launch(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
   if (rc) return rc;
   g.n_tiles = g.N / BN;
   const long long ntiles = (long long)g.m_tiles * g.n_tiles;
-  const int grid = (int)(ntiles < dpp_host::sm_count() ? ntiles : dpp_host::sm_count());
+  const int sms = dpp_host::sm_count();
+  int grid = (int)(ntiles < sms ? ntiles : sms);
+  // The stale V's maxima: by CTAs of their own on the SMs the tiles leave idle (at most
+  // 1 MB each, a few us beside the tiles' main loops), else by the epilogue warps.
+  if (CONV && !GNF && g.vs_src && ntiles < sms &&
+      (long long)(sms - ntiles) << 20 >= g.vs_rows * g.vs_C * 2) {
+    g.vs_scan = 1;
+    grid = sms;
+  }
   const cudaError_t e =
       dpp_host::launch_pdl(tc_gemm_kernel<CONV, BN, GNF, RFX, AMODE>, dim3(grid),
                            dim3(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS), Cfg<BN>::SMEM, s, ta, ta2,
@@ -829,7 +886,7 @@ int launch_tc_conv(const void* yf, const void* ys, const void* w, void* out, int
   g.box_px = box_px;
   g.gn_par = gn_par;
   g.P = P;
-  if (vstale && !gn_par) {  // [B, H*W, vs_C] stale V: its maxima by the epilogue warps
+  if (vstale && !gn_par) {  // [B, H*W, vs_C] stale V: its maxima (scan CTAs or epilogue)
     if (!vmax || vs_C % 64 || heads * 64 != vs_C) return DPP_ERR_SHAPE;
     g.vs_src = static_cast<const __nv_bfloat16*>(vstale);
     g.vs_rows = (long long)B * H * W;

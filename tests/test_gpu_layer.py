@@ -373,10 +373,10 @@ def test_layer_message_keeps_rank_copies_identical(name, dbuf, frx):
 def test_layer_v_outside_fp16_range(vshift):
     """The V projection weights scaled by 2^17 (V near 1e4..1e5, beyond fp16's 65504) or
     2^-20 (V in fp16's subnormal range): the layer step takes max |V| per (batch, head)
-    from the projection's epilogue (fresh V) and, on this small map, the conv's epilogue
-    warps (stale V), and scales V by a power of two inside the attention.  A synchronous
-    then a stale step; the attention stage on the GPU's own Q, K, V and the state within
-    the bf16 bound."""
+    from the projection's epilogue (fresh V) and, on this small map, CTAs of the conv
+    that have no tile (stale V), and scales V by a power of two inside the attention.  A
+    synchronous then a stale step; the attention stage on the GPU's own Q, K, V and the
+    state within the bf16 bound."""
     cfg = CFGS["small_bf16"]
     wts = synth.layer_weights(cfg, seed=4, affine=True)
     C = cfg.C
@@ -407,15 +407,19 @@ def test_layer_v_outside_fp16_range(vshift):
     assert rel_err(np64(out).reshape(B, L, C), oracle.linear(v1["o"], wn["w_o"], "bf16")) < TOL_BF16
 
 
-def test_layer_v_outside_fp16_range_large_map():
-    """The same with a map of 40960 rows (more than 256 per SM): there the GroupNorm apply
-    takes max |V_stale| instead of the conv (smaller maps).  V near 1e4..1e5 through the
-    projection weights times 2^17; a synchronous then a stale step; the attention stage on
-    the GPU's own Q, K, V and the old state, on 192 sampled query rows (the oracle would
-    need minutes for all of them), within the bf16 bound."""
-    cfg = synth.LayerConfig("large", B=1, H=320, W=128, C=128, P=4, G=8, heads=2,
+@pytest.mark.parametrize("H", [256, 320], ids=["conv-epilogue", "groupnorm"])
+def test_layer_v_outside_fp16_range_large_map(H):
+    """The same on larger maps, where other kernels take max |V_stale|: 256 x 128 rows
+    (256 conv tiles, no SM left over: the conv's epilogue warps) and 320 x 128 rows (more
+    than 256 rows per SM: the GroupNorm apply).  V near 1e4..1e5 through the projection
+    weights times 2^17; a synchronous then a stale step; the attention stage on the GPU's
+    own Q, K, V and the old state, on 192 sampled query rows (the oracle would need
+    minutes for all of them), within the bf16 bound."""
+    cfg = synth.LayerConfig("large", B=1, H=H, W=128, C=128, P=4, G=8, heads=2,
                             head_dim=64, dtype="bf16")
-    assert cfg.B * cfg.H * cfg.W > 256 * torch.cuda.get_device_properties(0).multi_processor_count
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = cfg.B * cfg.H * cfg.W
+    assert (rows > 256 * sms) == (H == 320) and rows // 128 >= sms
     wts = synth.layer_weights(cfg, seed=5, affine=True)
     C = cfg.C
     w = wts["w_qkv"].clone()
