@@ -39,14 +39,14 @@ METRIC = "patch-layer steps/s; attention TFLOP/s & refresh GB/s as % of GB300 ro
 # exists.  Writes that are still in L2 when a kernel ends are not counted by the capture.
 TRAFFIC = {
     "attention_sdxl1024_step": 52.56e6,
-    "conv_sdxl1024_step": None,
-    "qkv_proj_sdxl1024_step": 12.97e6,
+    "conv_sdxl1024_step": 29.40e6,
+    "qkv_proj_sdxl1024_step": 13.01e6,
     "out_proj_sdxl1024_step": 11.33e6,
     "groupnorm_sdxl1024_step": 21.11e6,
     "refresh_sdxl1024_step": 43.96e6,
     "attention_sdxl3840": 1012.5e6,
-    "conv_vae_1x256x256x512": None,
-    "conv_sdxl3840_latent_step": None,
+    "conv_vae_1x256x256x512": 93.7e6,
+    "conv_sdxl3840_latent_step": 265.7e6,
     "refresh_sweep_200MiB": 684.3e6,
     "refresh_2x256x256x640_step": 1157.5e6,
     "groupnorm_2x240x240x640_step": 530.8e6,
