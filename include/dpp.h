@@ -58,9 +58,8 @@ extern "C" {
 #define DPP_ERR_DTYPE 4       /* dtype is neither DPP_F32 nor DPP_BF16 */
 #define DPP_ERR_CUDA 5        /* a CUDA runtime/driver call failed */
 #define DPP_ERR_TIMEOUT 6     /* device status: a bounded wait gave up */
-#define DPP_ERR_BOUNDS 7      /* reserved for a device index check; no kernel of this
-                                 build sets it (the host checks the shapes that each
-                                 launch's index arithmetic relies on) */
+#define DPP_ERR_BOUNDS 7      /* dpp_debug_bounds: a kernel of the index-checking build
+                                 computed a global index outside its tensor's extent */
 #define DPP_ERR_UNSUPPORTED 8 /* the combination is not implemented */
 #define DPP_ERR_ARG 9         /* an enum/flag argument is invalid */
 #define DPP_ERR_SCRATCH_LIMIT 10 /* the layer needs more workspace than the fixed
@@ -313,6 +312,21 @@ int patch_layer_step_timed(const dpp_layer_params* prm, const dpp_layer_weights*
 /* Synchronizes `stream` and returns the workspace's device status word
  * (DPP_OK, DPP_ERR_TIMEOUT, ...), or DPP_ERR_CUDA if the copy fails. */
 int dpp_read_device_status(const void* workspace, void* stream);
+
+/*
+ * dpp_debug_bounds -- the index check of a library built with -DDPP_DEBUG_BOUNDS (a
+ * self-checking build that stands in for a memory checker).  In that build every kernel
+ * checks each global-memory index it computes (TMA copies excepted: the copy engine
+ * clips them to their tensor maps) against the extent that the call's shapes give the
+ * tensor it addresses; an index outside skips that access, traps nothing, and the first
+ * one is recorded.  rec (host, 4 values): {source file (1 groupnorm.cu, 2 refresh.cu,
+ * 3 tc_gemm.cu, 4 tc_attn.cu, 5 simt.cu, 6 otil.cu), source line, index, extent} of the
+ * first recorded index since the last reset, all 0 if none; reset != 0 clears the
+ * records.  Synchronizes the device.  Returns DPP_OK (checked build, nothing recorded),
+ * DPP_ERR_BOUNDS (checked build, rec holds the first violation), DPP_ERR_UNSUPPORTED
+ * (a normal build: no checks compiled, rec zeroed), DPP_ERR_NULL or DPP_ERR_CUDA.
+ */
+int dpp_debug_bounds(long long* rec, int reset);
 
 /*
  * dpp_apply_layer_message -- brings another rank's copy of the layer state up to date

@@ -8,6 +8,7 @@ been built, every call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -70,7 +71,7 @@ EXPORTS = ("dpp_status_string", "dpp_version", "refresh_residual", "halo_conv3x3
            "dpp_message_blocks", "patch_layer_step", "patch_layer_step_timed",
            "dpp_read_device_status", "dpp_layer_kernel_count", "patch_layer_step_noalloc",
            "dpp_noalloc_read_status",
-           "dpp_otil_blocks", "dpp_otil_step", "dpp_otil_finalize")
+           "dpp_otil_blocks", "dpp_otil_step", "dpp_otil_finalize", "dpp_debug_bounds")
 
 
 def load(build_if_missing: bool = False):
@@ -83,6 +84,13 @@ def load(build_if_missing: bool = False):
         if not build_if_missing:
             raise DppError(-1, f"CUDA library not built ({path}); run __graft_entry__.build()")
         _build.build_library()
+    _lib = open_library(path)
+    return _lib
+
+
+def open_library(path: str):
+    """A ctypes handle on the library at `path` (e.g. the index-checking build), with
+    the argument types set; `using(handle)` makes the calls of this module go to it."""
     lib = ctypes.CDLL(path)
     P, I64 = ctypes.POINTER, ctypes.c_int64
     lib.dpp_status_string.restype = ctypes.c_char_p
@@ -134,8 +142,21 @@ def load(build_if_missing: bool = False):
     lib.dpp_otil_finalize.argtypes = [P(OtilParams), _c_void, _c_void, _c_void, _c_int, _c_void]
     lib.dpp_layer_kernel_count.restype = _c_int
     lib.dpp_layer_kernel_count.argtypes = [P(LayerParams), _c_int]
-    _lib = lib
+    lib.dpp_debug_bounds.restype = _c_int
+    lib.dpp_debug_bounds.argtypes = [P(I64), _c_int]
     return lib
+
+
+@contextlib.contextmanager
+def using(lib):
+    """Within the block, this module's calls go to the library handle `lib`."""
+    global _lib
+    prev = load()
+    _lib = lib
+    try:
+        yield lib
+    finally:
+        _lib = prev
 
 
 def status_string(code: int) -> str:
@@ -336,6 +357,15 @@ def patch_layer_step_noalloc(prm: LayerParams, weights: dict, state: dict, x, ou
 
 def read_device_status(workspace, stream=None) -> int:
     return load().dpp_read_device_status(_ptr(workspace), _stream(stream))
+
+
+def debug_bounds(reset: bool = False):
+    """(code, record) of the index-checking build's first out-of-extent index (see
+    dpp_debug_bounds): code DPP_OK / DPP_ERR_BOUNDS (7) / DPP_ERR_UNSUPPORTED (8, a normal
+    build); record = (file, line, index, extent)."""
+    rec = (ctypes.c_int64 * 4)()
+    rc = load().dpp_debug_bounds(rec, 1 if reset else 0)
+    return rc, tuple(rec)
 
 
 def noalloc_read_status(stream=None) -> int:

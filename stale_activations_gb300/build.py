@@ -1,7 +1,10 @@
 """Builds the CUDA library in-tree: stale_activations_gb300/_build/libdpp.so (sm_103a).
 
 Plain nvcc, one -gencode, translation units compiled in parallel; no torch
-extension machinery (the C ABI has no torch types).
+extension machinery (the C ABI has no torch types).  build_library(bounds=True) builds
+the index-checking variant (-DDPP_DEBUG_BOUNDS: every kernel checks the global indices
+it computes and records the first one outside its tensor, see dpp_debug_bounds) as
+_build/bounds/libdpp_bounds.so, for the tests.
 """
 from __future__ import annotations
 
@@ -16,6 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libdpp.so")
+BOUNDS_DIR = os.path.join(OUT_DIR, "bounds")
+LIB_BOUNDS = os.path.join(BOUNDS_DIR, "libdpp_bounds.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -34,14 +39,19 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build_library(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every csrc/*.cu and link libdpp.so; returns its path."""
+def build_library(force: bool = False, verbose: bool = False, extra_flags=(),
+                  bounds: bool = False) -> str:
+    """Compile every csrc/*.cu and link libdpp.so (or, with bounds, the index-checking
+    libdpp_bounds.so); returns its path."""
     deps = _deps()
-    if not force and not _stale(LIB, deps):
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+    lib, out_dir = (LIB_BOUNDS, BOUNDS_DIR) if bounds else (LIB, OUT_DIR)
+    if bounds:
+        extra_flags = (*extra_flags, "-DDPP_DEBUG_BOUNDS")
+    if not force and not _stale(lib, deps):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    objs = [os.path.join(OUT_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(out_dir, os.path.basename(s)[:-3] + ".o") for s in srcs]
 
     def compile_one(src_obj):
         src, obj = src_obj
@@ -55,13 +65,13 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=()) ->
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         list(ex.map(compile_one, zip(srcs, objs)))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

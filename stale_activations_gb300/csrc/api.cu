@@ -189,6 +189,17 @@ int refresh_segments(dpp::RefreshSeg* segs, int nseg, int dtype, cudaStream_t s)
 
 }  // namespace
 
+#ifdef DPP_DEBUG_BOUNDS
+namespace dpp {  // each kernel file's index-check record (DPP_BOUNDS_READER)
+int bounds_groupnorm(long long* rec, int reset);
+int bounds_refresh(long long* rec, int reset);
+int bounds_tc_gemm(long long* rec, int reset);
+int bounds_tc_attn(long long* rec, int reset);
+int bounds_simt(long long* rec, int reset);
+int bounds_otil(long long* rec, int reset);
+}  // namespace dpp
+#endif
+
 extern "C" {
 
 const char* dpp_status_string(int status) {
@@ -607,6 +618,35 @@ int dpp_read_device_status(const void* workspace, void* stream) {
     return DPP_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return DPP_ERR_CUDA;
   return v;
+}
+
+int dpp_debug_bounds(long long* rec, int reset) {
+  if (!rec) return DPP_ERR_NULL;
+  for (int i = 0; i < 4; ++i) rec[i] = 0;
+#ifdef DPP_DEBUG_BOUNDS
+  if (cudaDeviceSynchronize() != cudaSuccess) return DPP_ERR_CUDA;
+  // the record of each translation unit that holds kernels, in the order the header lists
+  int (*const readers[])(long long*, int) = {dpp::bounds_groupnorm, dpp::bounds_refresh,
+                                             dpp::bounds_tc_gemm,   dpp::bounds_tc_attn,
+                                             dpp::bounds_simt,      dpp::bounds_otil};
+  int rc = DPP_OK;
+  for (int f = 0; f < 6; ++f) {
+    long long r[3];
+    const int e = readers[f](r, reset);
+    if (e) return e;
+    if (r[0] && rc == DPP_OK) {
+      rec[0] = f + 1;
+      rec[1] = r[0];
+      rec[2] = r[1];
+      rec[3] = r[2];
+      rc = DPP_ERR_BOUNDS;
+    }
+  }
+  return rc;
+#else
+  (void)reset;
+  return DPP_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // extern "C"

@@ -61,6 +61,52 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// ------------------------------------------------------------ index checks
+// In a library built with -DDPP_DEBUG_BOUNDS every kernel checks each global-memory index
+// it computes against the extent of the tensor it addresses, as the call's shapes give it
+// (TMA copies are clipped to their tensor maps by the copy engine itself and are not
+// checked): DPP_IN(i, n, extent) is true when elements [i, i + n) lie in [0, extent);
+// otherwise the access is skipped and the first such index of this translation unit is
+// recorded (source line, index, extent) for dpp_debug_bounds().  Without the flag DPP_IN
+// is the constant true and the checks compile away.
+#ifdef DPP_DEBUG_BOUNDS
+namespace {  // one record per translation unit
+__device__ long long g_bounds[3];  // source line (0: none), index, extent
+__device__ int g_bounds_claim;
+__device__ __noinline__ bool bounds_violation(long long i, long long ext, int line) {
+  if (atomicCAS(&g_bounds_claim, 0, 1) == 0) {
+    g_bounds[1] = i;
+    g_bounds[2] = ext;
+    __threadfence();
+    atomicExch(reinterpret_cast<unsigned long long*>(&g_bounds[0]), (unsigned long long)line);
+  }
+  return false;
+}
+__device__ __forceinline__ bool in_extent(long long i, long long n, long long ext, int line) {
+  return (i >= 0 && n >= 0 && i + n <= ext) ? true : bounds_violation(i, ext, line);
+}
+}  // namespace
+#define DPP_IN(i, n, ext) \
+  ::dpp::in_extent((long long)(i), (long long)(n), (long long)(ext), __LINE__)
+// The host reader of this translation unit's record: rec = {line, index, extent}.
+#define DPP_BOUNDS_READER(fn)                                                           \
+  int fn(long long* rec, int reset) {                                                   \
+    if (cudaMemcpyFromSymbol(rec, g_bounds, sizeof(g_bounds)) != cudaSuccess)          \
+      return DPP_ERR_CUDA;                                                              \
+    if (reset) {                                                                        \
+      const long long z[3] = {0, 0, 0};                                                 \
+      const int zi = 0;                                                                 \
+      if (cudaMemcpyToSymbol(g_bounds, z, sizeof(z)) != cudaSuccess ||                  \
+          cudaMemcpyToSymbol(g_bounds_claim, &zi, sizeof(zi)) != cudaSuccess)          \
+        return DPP_ERR_CUDA;                                                            \
+    }                                                                                   \
+    return DPP_OK;                                                                      \
+  }
+#else
+#define DPP_IN(i, n, ext) true
+#define DPP_BOUNDS_READER(fn)
+#endif
+
 }  // namespace dpp
 
 // ------------------------------------------------------------ host helpers

@@ -53,13 +53,15 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const T* __restrict__ x,
   float s1[VEC], s2[VEC];
 #pragma unroll
   for (int i = 0; i < VEC; ++i) { s1[i] = 0.f; s2[i] = 0.f; }
+  const long long act = (long long)g.B * g.H * g.W * g.C;  // elements of x
   if (pl < PIX) {
-    const T* base = x + (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C + v * VEC;
+    const long long xo = (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C + v * VEC;
+    const T* base = x + xo;
     for (long long px = p0 + pl; px < p1; px += kGnBatch * PIX) {
       uint4 u[kGnBatch];
 #pragma unroll
       for (int k = 0; k < kGnBatch; ++k)
-        if (px + k * PIX < p1)
+        if (px + k * PIX < p1 && DPP_IN(xo + (px + k * PIX) * g.C, VEC, act))
           u[k] = __ldg(reinterpret_cast<const uint4*>(base + (px + k * PIX) * g.C));
 #pragma unroll
       for (int k = 0; k < kGnBatch; ++k) {
@@ -95,10 +97,10 @@ __global__ void __launch_bounds__(256) gn_stats_kernel(const T* __restrict__ x,
       a += __shfl_xor_sync(0xffffffffu, a, m);
       q += __shfl_xor_sync(0xffffffffu, q, m);
     }
-    if (gi < g.G && part == 0) {
-      float* out = partial + ((((long long)b * g.P + p) * g.nchunk + chunk) * g.G + gi) * 2;
-      out[0] = a;
-      out[1] = q;
+    const long long po = ((((long long)b * g.P + p) * g.nchunk + chunk) * g.G + gi) * 2;
+    if (gi < g.G && part == 0 && DPP_IN(po, 2, (long long)g.B * g.P * g.nchunk * g.G * 2)) {
+      partial[po] = a;
+      partial[po + 1] = q;
     }
   }
 }
@@ -139,6 +141,8 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
     p1 = p0 + g.W;
   }
   const long long base = (((long long)b * g.H + (long long)p * g.Hp) * g.W) * g.C + v * VEC;
+  const long long act = (long long)g.B * g.H * g.W * g.C;  // elements of x, y and the stale V
+  const long long nstat = (long long)g.B * g.P * G2;       // [B, P, G, 2] sums
 
   // What does not depend on the stats kernel is fetched before waiting for it: the first
   // batch of x, this thread's gamma and beta, the stale sums.  (Every block of the
@@ -149,11 +153,11 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
   if (active && rows) {
 #pragma unroll
     for (int k = 0; k < kGnBatch; ++k)
-      if (px + k * PIX < p1)
+      if (px + k * PIX < p1 && DPP_IN(base + (px + k * PIX) * g.C, VEC, act))
         u[k] = __ldcs(reinterpret_cast<const uint4*>(x + base + (px + k * PIX) * g.C));
   }
   float ga[VEC], be[VEC];
-  if (active) {
+  if (active && DPP_IN(v * VEC, VEC, g.C)) {
 #pragma unroll
     for (int k = 0; k < VEC; ++k) {
       ga[k] = __ldg(gamma + v * VEC + k);
@@ -162,7 +166,8 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
   }
   if (!all_fresh)
     for (int idx = tid; idx < g.P * G2; idx += blockDim.x)
-      if (idx / G2 != p) s_tot[idx] = stale_stats[(long long)b * g.P * G2 + idx];
+      if (idx / G2 != p && DPP_IN((long long)b * g.P * G2 + idx, 1, nstat))
+        s_tot[idx] = stale_stats[(long long)b * g.P * G2 + idx];
   // The stale V has x's layout ([B, H*W, C]): its max |V| per (batch, head) over this
   // block's pixels, for the attention's fp16 scaling of V.  It is state written before the
   // stats kernel started, so it is read before the wait; the per-(batch, head) maxima are
@@ -176,7 +181,7 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
         uint4 w[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          if (q + k * PIX < p1)
+          if (q + k * PIX < p1 && DPP_IN(base + (q + k * PIX) * g.C, VEC, act))
             w[k] = __ldcs(reinterpret_cast<const uint4*>(vstale + base + (q + k * PIX) * g.C));
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -193,7 +198,8 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
   }
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  if (vstale && tid < heads && s_hmax[tid])
+  if (vstale && tid < heads && s_hmax[tid] &&
+      DPP_IN((long long)b * heads + tid, 1, (long long)g.B * heads))
     atomicMax(vmax + (long long)b * heads + tid, s_hmax[tid] << 16);  // bf16 -> fp32 bits
   // fresh sums over chunks, for own patch (and every patch when all are fresh): tps
   // threads per sum, each a fixed stride of chunks with eight loads in flight, then a
@@ -205,16 +211,21 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
     const int q = all_fresh ? si / G2 : p, r = si % G2;
     float val = 0.f;
     if (si < nq * G2) {
-      const float* src = partial + (((long long)b * g.P + q) * g.nchunk) * G2 + r;
+      const long long so = (((long long)b * g.P + q) * g.nchunk) * G2 + r;
+      const long long npart = (long long)g.B * g.P * g.nchunk * G2;
+      const float* src = partial + so;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       int c = part;
       for (; c + 7 * tps < g.nchunk; c += 8 * tps) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] += src[(long long)(c + k * tps) * G2];
+        for (int k = 0; k < 8; ++k)
+          if (DPP_IN(so + (long long)(c + k * tps) * G2, 1, npart))
+            acc[k] += src[(long long)(c + k * tps) * G2];
       }
 #pragma unroll
       for (int k = 0; k < 7; ++k)
-        if (c + k * tps < g.nchunk) acc[k] += src[(long long)(c + k * tps) * G2];
+        if (c + k * tps < g.nchunk && DPP_IN(so + (long long)(c + k * tps) * G2, 1, npart))
+          acc[k] += src[(long long)(c + k * tps) * G2];
       val = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     }
     for (int m = tps >> 1; m > 0; m >>= 1) val += __shfl_xor_sync(0xffffffffu, val, m);
@@ -223,7 +234,8 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
   __syncthreads();
   if (chunk == 0 && fresh_out)
     for (int r = tid; r < G2; r += blockDim.x)
-      fresh_out[((long long)b * g.P + p) * G2 + r] = s_tot[p * G2 + r];
+      if (DPP_IN(((long long)b * g.P + p) * G2 + r, 1, nstat))
+        fresh_out[((long long)b * g.P + p) * G2 + r] = s_tot[p * G2 + r];
   // group statistics: own patch first (its previous-step sums under DPP_GN_PREVIOUS),
   // then the others in order; mu = S1/N, var = max(S2/N - mu^2, 0)
   const int cg = g.C / g.G;
@@ -231,7 +243,11 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
   const float* own = mode == DPP_GN_PREVIOUS ? stale_stats + ((long long)b * g.P + p) * G2
                                              : s_tot + p * G2;
   for (int gi = tid; gi < g.G; gi += blockDim.x) {
-    float S1 = own[gi * 2], S2 = own[gi * 2 + 1];
+    float S1 = 0.f, S2 = 0.f;
+    if (mode != DPP_GN_PREVIOUS || DPP_IN(((long long)b * g.P + p) * G2 + gi * 2, 2, nstat)) {
+      S1 = own[gi * 2];
+      S2 = own[gi * 2 + 1];
+    }
     for (int q = 0; q < g.P; ++q)
       if (q != p) { S1 += s_tot[q * G2 + gi * 2]; S2 += s_tot[q * G2 + gi * 2 + 1]; }
     const float mu = (float)(S1 * invN);
@@ -248,7 +264,9 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
     mu[k] = s_grp[gi * 2];
     sc[k] = s_grp[gi * 2 + 1] * ga[k];
   }
-  if (params_out && chunk == 0 && pl == 0) {  // the per-channel parameters, for a fused consumer
+  if (params_out && chunk == 0 && pl == 0 &&  // the per-channel parameters, for a fused consumer
+      DPP_IN(((long long)b * g.P + p) * 3 * g.C + v * VEC, 2 * g.C + VEC,
+             (long long)g.B * g.P * 3 * g.C)) {
     float* dst = params_out + ((long long)b * g.P + p) * 3 * g.C + v * VEC;
 #pragma unroll
     for (int k = 0; k < VEC; ++k) {
@@ -266,16 +284,19 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const T* __restrict__ x, 
       unpack16(u[k], f);
 #pragma unroll
       for (int i = 0; i < VEC; ++i) f[i] = fmaf(f[i] - mu[i], sc[i], be[i]);
-      *reinterpret_cast<uint4*>(y + base + (px + k * PIX) * g.C) = pack16(f);
+      if (DPP_IN(base + (px + k * PIX) * g.C, VEC, act))
+        *reinterpret_cast<uint4*>(y + base + (px + k * PIX) * g.C) = pack16(f);
     }
     px += kGnBatch * PIX;
     if (px >= p1) break;
 #pragma unroll
     for (int k = 0; k < kGnBatch; ++k)
-      if (px + k * PIX < p1)
+      if (px + k * PIX < p1 && DPP_IN(base + (px + k * PIX) * g.C, VEC, act))
         u[k] = __ldcs(reinterpret_cast<const uint4*>(x + base + (px + k * PIX) * g.C));
   }
 }
+
+DPP_BOUNDS_READER(bounds_groupnorm)
 
 GnDims make_gn_dims(int B, int H, int W, int C, int P, int G) {
   GnDims g;

@@ -56,7 +56,8 @@ __global__ void __launch_bounds__(kOtilThreads) otil_step_kernel(const T* __rest
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const long long img = (long long)d.B * d.C * d.H * d.W;
-  const T* peer = views + (long long)((p + 1) % d.P) * img;
+  const long long peer0 = (long long)((p + 1) % d.P) * img;  // offset of the peer's view
+  const T* peer = views + peer0;
   // 1. scores
   const long long plane = (long long)d.H * d.W;
   const int planes = d.B * d.C;
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(kOtilThreads) otil_step_kernel(const T* __rest
       for (int rr = 0; rr < d.bh; ++rr) {
         const long long row = pl * plane + o0 + (long long)rr * d.W;
         for (int cc = lane; cc < d.bw; cc += 32) {
+          if (!DPP_IN(row + cc, 1, img) || !DPP_IN(peer0 + row + cc, 1, d.P * img)) continue;
           const float x = to_f32(fresh[row + cc]), s = to_f32(peer[row + cc]);
           xs = fmaf(x, s, xs);
           xx = fmaf(x, x, xx);
@@ -83,7 +85,9 @@ __global__ void __launch_bounds__(kOtilThreads) otil_step_kernel(const T* __rest
     if (lane == 0) {
       const float den = sqrtf(xx) * sqrtf(ss);
       const float dis = den > 0.f ? 1.f - xs / den : 1.f;
-      s_score[i] = dis + (visited[(long long)p * d.K + i] ? 0.f : 10.f);
+      const bool seen = DPP_IN((long long)p * d.K + i, 1, (long long)d.P * d.K) &&
+                        visited[(long long)p * d.K + i];
+      s_score[i] = dis + (seen ? 0.f : 10.f);
       s_taken[i] = 0;
     }
   }
@@ -104,8 +108,9 @@ __global__ void __launch_bounds__(kOtilThreads) otil_step_kernel(const T* __rest
         s_sel[m] = t;
       }
     for (int j = 0; j < d.k; ++j) {
-      sel[(long long)p * d.k + j] = s_sel[j];
-      visited[(long long)p * d.K + s_sel[j]] = 1;
+      if (DPP_IN((long long)p * d.k + j, 1, (long long)d.P * d.k)) sel[(long long)p * d.k + j] = s_sel[j];
+      if (DPP_IN((long long)p * d.K + s_sel[j], 1, (long long)d.P * d.K))
+        visited[(long long)p * d.K + s_sel[j]] = 1;
     }
   }
   __syncthreads();
@@ -118,12 +123,16 @@ __global__ void __launch_bounds__(kOtilThreads) otil_step_kernel(const T* __rest
     const int j = q / (planes * d.bh), rem = q - j * planes * d.bh;
     const int pl = rem / d.bh, rr = rem - pl * d.bh;
     const long long row = pl * plane + block_origin(d, p, s_sel[j]) + (long long)rr * d.W;
-    T* mrow = msg + (long long)p * per + (long long)j * d.belem + ((long long)pl * d.bh + rr) * d.bw;
+    const long long m0 =
+        (long long)p * per + (long long)j * d.belem + ((long long)pl * d.bh + rr) * d.bw;
+    T* mrow = msg + m0;
     for (int cc = lane; cc < d.bw; cc += 32) {
+      if (!DPP_IN(row + cc, 1, img) || !DPP_IN(m0 + cc, 1, d.P * per)) continue;
       const T v = fresh[row + cc];
       mrow[cc] = v;
       for (int r = 0; r < d.P; ++r)
-        if (r != p) views[(long long)r * img + row + cc] = v;
+        if (r != p && DPP_IN((long long)r * img + row + cc, 1, d.P * img))
+          views[(long long)r * img + row + cc] = v;
     }
   }
   // own band in full (rows [p*Hp, (p+1)*Hp) of every (b, ch) plane): a warp per
@@ -133,7 +142,9 @@ __global__ void __launch_bounds__(kOtilThreads) otil_step_kernel(const T* __rest
   for (int q = warp; q < planes * d.Hp; q += nwarps) {
     const int pl = q / d.Hp, rr = q - pl * d.Hp;
     const long long row = pl * plane + ((long long)p * d.Hp + rr) * d.W;
-    for (int cc = lane; cc < d.W; cc += 32) own[row + cc] = fresh[row + cc];
+    for (int cc = lane; cc < d.W; cc += 32)
+      if (DPP_IN(row + cc, 1, img) && DPP_IN((long long)p * img + row + cc, 1, d.P * img))
+        own[row + cc] = fresh[row + cc];
   }
 }
 
@@ -165,6 +176,8 @@ OtilDims dims(const dpp_otil_params& p) {
 }
 
 }  // namespace
+
+DPP_BOUNDS_READER(bounds_otil)
 
 int otil_check(const dpp_otil_params* p) {
   if (!p) return DPP_ERR_NULL;

@@ -96,6 +96,8 @@ __device__ __forceinline__ void start_block(const RefreshTable& tab, long long g
   const long long j = gb - tab.blk_start[seg];
   const long long e0 = j * 128;
   if (!sg.vec_ok || sg.n - e0 < 128) return;
+  // the whole block and its scale (the same for the 16 lanes, which shuffle together)
+  if (!DPP_IN(e0, 128, sg.n) || !DPP_IN(j, 1, (sg.n + 127) / 128)) return;
   const T* fr = reinterpret_cast<const T*>(sg.fresh) + e0;
   T* st = reinterpret_cast<T*>(sg.stale) + e0;
   constexpr int NV = 8 / Vec<T>::N;  // 16-byte vectors per lane: 1 (bf16) or 2 (fp32)
@@ -159,6 +161,8 @@ __global__ void __launch_bounds__(256, 4) refresh_kernel(const __grid_constant__
     const long long nblk = tab.blk_start[k + 1] - tab.blk_start[k];
     for (long long j = (sg.vec_ok ? sg.n / 128 : 0) + group; j < nblk; j += stride) {
       const long long e0 = j * 128;
+      if (!DPP_IN(e0, min(128ll, sg.n - e0), sg.n) || !DPP_IN(j, 1, (sg.n + 127) / 128))
+        continue;  // the same for the 16 lanes
       refresh_block_scalar<T>(reinterpret_cast<const T*>(sg.fresh) + e0,
                               reinterpret_cast<const T*>(sg.stale) + e0,
                               reinterpret_cast<T*>(sg.out) + e0, sg.codes + e0, sg.scales + j,
@@ -229,6 +233,7 @@ __global__ void __launch_bounds__(256) apply_kernel(const __grid_constant__ Appl
     const long long j = gb - tab.blk_start[seg];
     const long long e0 = j * 128;
     const int nb = (int)min(128ll, sg.n - e0);
+    if (!DPP_IN(j, 1, (sg.n + 127) / 128) || !DPP_IN(e0, nb, sg.n)) continue;
     const float s = sg.scales[j];
     T* st = static_cast<T*>(sg.stale) + e0;
     const int8_t* cd = sg.codes + e0;
@@ -240,6 +245,8 @@ __global__ void __launch_bounds__(256) apply_kernel(const __grid_constant__ Appl
     }
   }
 }
+
+DPP_BOUNDS_READER(bounds_refresh)
 
 int launch_apply(const ApplyTable& tab, int dtype, cudaStream_t stream) {
   const long long total = tab.blk_start[tab.nseg];

@@ -20,6 +20,9 @@ namespace dpp {
 struct ALinear {
   const void* a;
   int K;
+#ifdef DPP_DEBUG_BOUNDS
+  long long n_a;  // elements of A (M * K), for the index checks
+#endif
   struct Row {
     long long m;
     bool ok;
@@ -32,6 +35,9 @@ struct ALinear {
   __device__ __forceinline__ void advance(Col& c, int step) const { c.k += step; }
   template <typename T>
   __device__ __forceinline__ float load(const Row& r, const Col& c) const {
+#ifdef DPP_DEBUG_BOUNDS
+    if (r.ok && c.k < K && !DPP_IN(r.m * K + c.k, 1, n_a)) return 0.f;
+#endif
     return r.ok && c.k < K ? to_f32(static_cast<const T*>(a)[r.m * K + c.k]) : 0.f;
   }
 };
@@ -40,6 +46,9 @@ struct AConv {
   const void* yf;
   const void* ys;
   int H, W, Cin, Hp;
+#ifdef DPP_DEBUG_BOUNDS
+  long long n_y;  // elements of each input map (B * H * W * Cin), for the index checks
+#endif
   struct Row {  // pixel (b, r, c) and its band [lo, lo + Hp)
     long long img;  // offset of image b
     int r, c, lo;
@@ -82,7 +91,8 @@ struct AConv {
     if (rr < 0 || rr >= H || cc < 0 || cc >= W) return 0.f;
     const bool own = rr >= x.lo && rr < x.lo + Hp;
     const T* src = static_cast<const T*>(own ? yf : ys);
-    return to_f32(src[(x.img + (long long)rr * W + cc) * Cin + k.ci]);
+    const long long i = (x.img + (long long)rr * W + cc) * Cin + k.ci;
+    return DPP_IN(i, 1, n_y) ? to_f32(src[i]) : 0.f;
   }
 };
 
@@ -114,7 +124,9 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(ALoad A, const T* __rest
     for (int i = 0; i < 4; ++i) {
       ra[i] = A.template load<T>(rows[i], ac);
       const int n = n0 + (threadIdx.x >> 4) + 16 * i;
-      rb[i] = nok[i] && k < K ? to_f32(Wt[(long long)n * K + k]) : 0.f;
+      rb[i] = nok[i] && k < K && DPP_IN((long long)n * K + k, 1, (long long)N * K)
+                  ? to_f32(Wt[(long long)n * K + k])
+                  : 0.f;
     }
   };
   fetch(kk);
@@ -152,7 +164,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(ALoad A, const T* __rest
       if (n >= N) continue;
       const int which = n / out.ncols;
       const int col = n - which * out.ncols;
-      static_cast<T*>(out.ptr[which])[m * out.ncols + col] = from_f32<T>(acc[i][j]);
+      if (DPP_IN(m * out.ncols + col, 1, M * out.ncols))
+        static_cast<T*>(out.ptr[which])[m * out.ncols + col] = from_f32<T>(acc[i][j]);
     }
   }
 }
@@ -184,10 +197,12 @@ __global__ void __launch_bounds__(256) simt_attention_kernel(const T* __restrict
   const bool valid = row_in_patch < Lp;
   const long long rowbase = (long long)b * L;
   const long long t = rowbase + p * Lp + (valid ? row_in_patch : 0);
+  const long long nel = (long long)gridDim.z * L * C;  // elements of Q, K, V and O
+  const bool q_in = DPP_IN(t * C + h * D, D, nel);
   float qr[D], acc[D];
 #pragma unroll
   for (int e = 0; e < D; ++e) {
-    qr[e] = to_f32(q[t * C + h * D + e]) * 0.125f;  // 1/sqrt(64), exact
+    qr[e] = q_in ? to_f32(q[t * C + h * D + e]) * 0.125f : 0.f;  // 1/sqrt(64), exact
     acc[e] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -197,7 +212,7 @@ __global__ void __launch_bounds__(256) simt_attention_kernel(const T* __restrict
   const int own_lo = p * Lp, own_hi = own_lo + Lp;
   float kv[16], vv[16];
   auto fetch = [&](int s) {
-    if (s < L) {
+    if (s < L && DPP_IN((rowbase + s) * C + h * D + le, 16, nel)) {
       const bool own = s >= own_lo && s < own_hi;
       const T* kp = (own ? kf : ks) + (rowbase + s) * C + h * D + le;
       const T* vp = (own ? vf : vs) + (rowbase + s) * C + h * D + le;
@@ -257,17 +272,22 @@ __global__ void __launch_bounds__(256) simt_attention_kernel(const T* __restrict
     if (e == lane) mine[0] = a;
     if (e == lane + 32) mine[1] = a;
   }
-  if (valid) {
+  if (valid && DPP_IN(t * C + h * D, D, nel)) {
     const float inv = 1.f / l;
     o[t * C + h * D + lane] = from_f32<T>(mine[0] * inv);
     o[t * C + h * D + lane + 32] = from_f32<T>(mine[1] * inv);
   }
 }
 
+DPP_BOUNDS_READER(bounds_simt)
+
 int launch_simt_linear(const void* a, const void* w, const SimtOut& out, long long M, int N, int K,
                        int dtype, cudaStream_t stream) {
   dim3 grid((N + 63) / 64, (unsigned)((M + 63) / 64));
   ALinear A{a, K};
+#ifdef DPP_DEBUG_BOUNDS
+  A.n_a = M * K;
+#endif
   if (dtype == DPP_BF16)
     simt_gemm_kernel<__nv_bfloat16, ALinear><<<grid, 256, 0, stream>>>(
         A, static_cast<const __nv_bfloat16*>(w), out, M, N, K);
@@ -283,6 +303,9 @@ int launch_simt_conv(const void* yf, const void* ys, const void* w, void* out, i
   const int K = 9 * Cin;
   dim3 grid((Cout + 63) / 64, (unsigned)((M + 63) / 64));
   AConv A{yf, ys, H, W, Cin, H / P};
+#ifdef DPP_DEBUG_BOUNDS
+  A.n_y = M * Cin;
+#endif
   SimtOut o{};
   o.ptr[0] = out;
   o.ncols = Cout;

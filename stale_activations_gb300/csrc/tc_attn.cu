@@ -216,8 +216,20 @@ __host__ __device__ __forceinline__ UnitPos unit_pos(int u, const AttnArgs& a) {
 // range: e = 0 when max|V| lies in [2^-6, 2^15); otherwise 14 - floor(log2 max|V|), so
 // that the scaled maximum lies in [2^14, 2^15), clamped to [-125, 125] (only |V| below
 // 2^-111 then keeps some fp16 subnormals).  An all-zero V gets 0.
+// Extents for the index checks: batches, elements of O (and of each of Q/K/V), partial
+// records, piece counters.
+__device__ __forceinline__ long long n_batch(const AttnArgs& a) {
+  return a.U / ((long long)a.heads * a.P * a.n_pairs);
+}
+__device__ __forceinline__ long long n_elems(const AttnArgs& a) {
+  return n_batch(a) * a.L * a.heads * D;
+}
+__device__ __forceinline__ long long n_records(const AttnArgs& a) {
+  return a.split ? (long long)a.G + a.U - (long long)a.W * a.G : 0;
+}
+
 __device__ __forceinline__ unsigned vmax_bits(const AttnArgs& a, int b, int h) {
-  return __ldg(a.vmax + b * a.heads + h);
+  return DPP_IN(b * a.heads + h, 1, n_batch(a) * a.heads) ? __ldg(a.vmax + b * a.heads + h) : 0u;
 }
 __device__ __forceinline__ int v_exponent(unsigned bits) {
   const float amax = __uint_as_float(bits);
@@ -285,13 +297,14 @@ __device__ __forceinline__ void merge_rows(const AttnArgs& a, const int* tb, int
   const long long s_a = (long long)ut * a.nkt;
   const size_t row = (size_t)(t * QT + r);
   // a CTA's first tail segment, or the last one of the CTA that started before the unit
+  auto rec_index = [&](int c) -> int { return (c == ca && tb[c] != s_a) ? a.G + ut : c; };
   auto record = [&](int c) -> const uint8_t* {
-    return a.part + (size_t)((c == ca && tb[c] != s_a) ? a.G + ut : c) * REC_BYTES;
+    return a.part + (size_t)rec_index(c) * REC_BYTES;
   };
   // every piece's lines of this row into L1 first, so that their round trips to L2 overlap
   // (the records are complete: the pieces' counter has been read)
   for (int c = ca; c <= cb; ++c) {
-    if (tb[c] == tb[c + 1]) continue;
+    if (tb[c] == tb[c + 1] || !DPP_IN(rec_index(c), 1, n_records(a))) continue;
     const uint8_t* base = record(c);
     ptx::prefetch_l1(base + row * D * 2);
     ptx::prefetch_l1(reinterpret_cast<const float*>(base + REC_M) + row);
@@ -303,6 +316,7 @@ __device__ __forceinline__ void merge_rows(const AttnArgs& a, const int* tb, int
   for (int d = 0; d < D; ++d) acc[d] = 0.f;
   for (int c = ca; c <= cb; ++c) {
     if (tb[c] == tb[c + 1]) continue;  // empty run
+    if (!DPP_IN(rec_index(c), 1, n_records(a))) continue;
     const uint8_t* base = record(c);
     const float m = __ldca(reinterpret_cast<const float*>(base + REC_M) + row);
     const float l = __ldca(reinterpret_cast<const float*>(base + REC_L) + row);
@@ -325,8 +339,10 @@ __device__ __forceinline__ void merge_rows(const AttnArgs& a, const int* tb, int
       }
     }
   }
-  __nv_bfloat16* dst =
-      a.o + ((long long)up.b * a.L + up.patch0 + row_in_patch) * (long long)(a.heads * D) + up.h * D;
+  const long long o_off =
+      ((long long)up.b * a.L + up.patch0 + row_in_patch) * (long long)(a.heads * D) + up.h * D;
+  if (!DPP_IN(o_off, D, n_elems(a))) return;
+  __nv_bfloat16* dst = a.o + o_off;
   const float inv = pow2(-e) / wsum;
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -430,6 +446,7 @@ __global__ void __launch_bounds__(256) vrange_kernel(const __nv_bfloat16* vf,
   unsigned m = 0;
   for (int r = r0 + warp * 4 + (lane >> 3); r < r1; r += 32) {
     const long long off = ((long long)b * L + r) * C + h * D + (lane & 7) * 8;
+    if (!DPP_IN(off, 8, (long long)gridDim.z * L * C)) continue;
     uint4 u = __ldg(reinterpret_cast<const uint4*>(vf + off));
     unsigned w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -447,7 +464,8 @@ __global__ void __launch_bounds__(256) vrange_kernel(const __nv_bfloat16* vf,
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int i = 1; i < 8; ++i) m = max(m, red[i]);
-    if (m) atomicMax(vmax + b * heads + h, m << 16);  // bf16 bits -> fp32 bits
+    if (m && DPP_IN(b * heads + h, 1, (long long)gridDim.z * heads))
+      atomicMax(vmax + b * heads + h, m << 16);  // bf16 bits -> fp32 bits
   }
 }
 
@@ -794,9 +812,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       if (sg.j0 == 0 && sg.len == a.nkt) {  // whole unit: normalised bf16 output
         const float inv = pow2(-e_cur) / l;
         const int row_in_patch = up.q0 + t * QT + r;
-        const bool valid = row_in_patch < a.Lp;
-        __nv_bfloat16* dst = a.o + ((long long)up.b * a.L + up.patch0 + row_in_patch) *
-                                       (long long)(a.heads * D) + up.h * D;
+        const long long o_off = ((long long)up.b * a.L + up.patch0 + row_in_patch) *
+                                    (long long)(a.heads * D) + up.h * D;
+        const bool valid = row_in_patch < a.Lp && DPP_IN(o_off, D, n_elems(a));
+        __nv_bfloat16* dst = a.o + o_off;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[16];
@@ -808,6 +827,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         const float inv = 1.f / l;
         const int ut = sg.u - a.W * a.G;
         const int rec = tail_seen ? a.G + ut : (int)blockIdx.x;
+        const bool rec_in = DPP_IN(rec, 1, n_records(a));  // the same for the whole warp
         uint8_t* base = a.part + (size_t)rec * REC_BYTES;
         uint4* dst = reinterpret_cast<uint4*>(base + ((size_t)(t * QT + r) * D) * 2);
 #pragma unroll
@@ -815,10 +835,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           uint32_t o[16];
           ptx::tmem_ld16(tO + lane_off + c * 16, o);
           ptx::tmem_ld_wait();
-          store_f16x16(dst + 2 * c, o, inv);
+          if (rec_in) store_f16x16(dst + 2 * c, o, inv);
         }
-        reinterpret_cast<float*>(base + REC_M)[t * QT + r] = m_ref;
-        reinterpret_cast<float*>(base + REC_L)[t * QT + r] = l;
+        if (rec_in) {
+          reinterpret_cast<float*>(base + REC_M)[t * QT + r] = m_ref;
+          reinterpret_cast<float*>(base + REC_L)[t * QT + r] = l;
+        }
         // The last piece of the unit to finish merges them all, warp by warp: each warp's
         // 32 rows have their own counter, so that no warp waits for another.
         __threadfence();
@@ -830,7 +852,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           int np = 0;
           for (int c = ca; c <= cb; ++c) np += tb[c] != tb[c + 1];
           int* cnt = a.cnt + (2 * ut + t) * 4 + quarter;
-          last = atomicAdd(cnt, 1) == np - 1;
+          last = DPP_IN((2 * ut + t) * 4 + quarter, 1, (n_records(a) - a.G) * 8) &&
+                 atomicAdd(cnt, 1) == np - 1;
           if (last) atomicExch(cnt, 0);  // all arrived: ready for the next call
         }
         if (__shfl_sync(0xffffffffu, last, 0)) {
@@ -926,6 +949,8 @@ size_t record_bytes(const AttnArgs& a) {
 }
 
 }  // namespace
+
+DPP_BOUNDS_READER(bounds_tc_attn)
 
 size_t tc_attention_scratch_bytes(int B, int L, int heads, int P, bool split) {
   AttnArgs a;

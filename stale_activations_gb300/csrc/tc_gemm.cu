@@ -199,6 +199,7 @@ __device__ __noinline__ void scan_vmax(const GemmArgs& a, int e, int E) {
   const int ncol = a.vs_C / 8;
   const int rpp = max(1, (int)blockDim.x / ncol);
   const long long r0 = a.vs_rows * e / E, r1 = a.vs_rows * (e + 1) / E;
+  const long long nv = a.vs_rows * a.vs_C, nmax = a.vs_rows / a.vmax_L * a.vmax_heads;
   for (int c = threadIdx.x; c < ncol * rpp; c += blockDim.x) {
     const int cc = c % ncol;
     unsigned* const col_max = a.vmax + (cc * 8) / 64;
@@ -209,7 +210,8 @@ __device__ __noinline__ void scan_vmax(const GemmArgs& a, int e, int E) {
       uint4 u[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (row + (long long)k * rpp < r1)
+        if (row + (long long)k * rpp < r1 &&
+            DPP_IN((row + (long long)k * rpp) * a.vs_C + cc * 8, 8, nv))
           u[k] = __ldcs(reinterpret_cast<const uint4*>(a.vs_src + (row + (long long)k * rpp) *
                                                                      a.vs_C) + cc);
 #pragma unroll
@@ -217,7 +219,8 @@ __device__ __noinline__ void scan_vmax(const GemmArgs& a, int e, int E) {
         const long long rk = row + (long long)k * rpp;
         if (rk >= r1) break;
         while (rk >= bend) {  // next batch: flush this one's maximum
-          if (m) atomicMax(col_max + b * a.vmax_heads, m << 16);
+          if (m && DPP_IN(b * a.vmax_heads + (cc * 8) / 64, 1, nmax))
+            atomicMax(col_max + b * a.vmax_heads, m << 16);
           m = 0;
           ++b;
           bend += a.vmax_L;
@@ -227,7 +230,8 @@ __device__ __noinline__ void scan_vmax(const GemmArgs& a, int e, int E) {
         for (int i = 0; i < 4; ++i) m = max(m, max(w4[i] & 0x7FFFu, (w4[i] >> 16) & 0x7FFFu));
       }
     }
-    if (m) atomicMax(col_max + b * a.vmax_heads, m << 16);
+    if (m && DPP_IN(b * a.vmax_heads + (cc * 8) / 64, 1, nmax))
+      atomicMax(col_max + b * a.vmax_heads, m << 16);
   }
 }
 
@@ -506,8 +510,11 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
         const int kb = kq + rot < args.nkb ? kq + rot : kq + rot - args.nkb;
         const float* par = par_tile + (kb % args.cin_blocks) * BK;
         float mu[8], sc[8], be[8];
+        const bool par_in = DPP_IN(((long long)tb * args.P + band) * 3 * args.Cin + c +
+                                       (kb % args.cin_blocks) * BK,
+                                   2 * args.Cin + 8, args.M / hw * args.P * 3 * args.Cin);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 2 && par_in; ++h) {
           const float4 m = __ldg(reinterpret_cast<const float4*>(par) + h);
           const float4 k = __ldg(reinterpret_cast<const float4*>(par + args.Cin) + h);
           const float4 e = __ldg(reinterpret_cast<const float4*>(par + 2 * args.Cin) + h);
@@ -565,6 +572,8 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
       const int et = threadIdx.x - 64, ncol = args.vs_C / 8;
       const long long r0 = args.vs_rows * blockIdx.x / gridDim.x;
       const long long r1 = args.vs_rows * (blockIdx.x + 1) / gridDim.x;
+      const long long nv = args.vs_rows * args.vs_C;
+      const long long nmax = args.vs_rows / args.vmax_L * args.vmax_heads;
       for (int cc = et; cc < ncol; cc += 128) {
         uint32_t m = 0;
         long long b = r0 / args.vmax_L, bend = (b + 1) * args.vmax_L;
@@ -572,13 +581,14 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
           uint4 u[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            if (row + k < r1)
+            if (row + k < r1 && DPP_IN((row + k) * args.vs_C + cc * 8, 8, nv))
               u[k] = __ldcs(reinterpret_cast<const uint4*>(args.vs_src + (row + k) * args.vs_C) + cc);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             if (row + k >= r1) break;
             if (row + k == bend) {  // next batch: flush this one's maximum
-              if (m) atomicMax(args.vmax + b * args.vmax_heads + (cc * 8) / 64, m << 16);
+              if (m && DPP_IN(b * args.vmax_heads + (cc * 8) / 64, 1, nmax))
+                atomicMax(args.vmax + b * args.vmax_heads + (cc * 8) / 64, m << 16);
               m = 0;
               ++b;
               bend += args.vmax_L;
@@ -588,7 +598,8 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
             for (int e = 0; e < 4; ++e) m = max(m, max(w4[e] & 0x7FFFu, (w4[e] >> 16) & 0x7FFFu));
           }
         }
-        if (m) atomicMax(args.vmax + b * args.vmax_heads + (cc * 8) / 64, m << 16);
+        if (m && DPP_IN(b * args.vmax_heads + (cc * 8) / 64, 1, nmax))
+          atomicMax(args.vmax + b * args.vmax_heads + (cc * 8) / 64, m << 16);
       }
     }
     int it = 0;
@@ -618,7 +629,10 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(obase) + row * args.ncols + col0;
       const uint32_t t_base = tmem + ab * BN + ((uint32_t)(quarter * 32) << 16);
       const bool rfx_row = RFX && which > 0;
-      if (rfx_row) refresh_row(t_base, dst, row_ok, which == 1, args, row * args.ncols + col0);
+      const long long nout = args.M * args.ncols;  // elements of each output
+      if (rfx_row)
+        refresh_row(t_base, dst, row_ok && DPP_IN(row * args.ncols + col0, 128, nout), which == 1,
+                    args, row * args.ncols + col0);
 #pragma unroll 1
       for (int ch = 0; ch < (rfx_row ? 0 : BN / 32); ++ch) {
         uint32_t v[32];
@@ -632,7 +646,7 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
           pk[i].z = pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
           pk[i].w = pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
         }
-        if (row_ok) {
+        if (row_ok && DPP_IN(row * args.ncols + col0 + ch * 32, 32, nout)) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) d4[i] = pk[i];
@@ -646,8 +660,10 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
             for (int e = 0; e < 4; ++e) m = max(m, max(w4[e] & 0x7FFFu, (w4[e] >> 16) & 0x7FFFu));
           }
           m = __reduce_max_sync(0xffffffffu, row_ok ? m : 0u);
-          if (lane == 0 && m) {  // the warp's 32 rows lie in one batch (L % 128 == 0)
-            const long long r0 = (long long)mt * BM + quarter * 32;
+          const long long r0 = (long long)mt * BM + quarter * 32;
+          if (lane == 0 && m &&  // the warp's 32 rows lie in one batch (L % 128 == 0)
+              DPP_IN((r0 / args.vmax_L) * args.vmax_heads + (col0 + ch * 32) / 64, 1,
+                     args.M / args.vmax_L * args.vmax_heads)) {
             atomicMax(args.vmax + (r0 / args.vmax_L) * args.vmax_heads + (col0 + ch * 32) / 64,
                       m << 16);
           }
@@ -668,6 +684,8 @@ __global__ void __launch_bounds__(GNF || RFX ? GEMM_GN_THREADS : GEMM_THREADS, 1
 }
 
 }  // namespace
+
+DPP_BOUNDS_READER(bounds_tc_gemm)
 
 PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() {
   static std::once_flag once;
