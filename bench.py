@@ -38,18 +38,18 @@ METRIC = "patch-layer steps/s; attention TFLOP/s & refresh GB/s as % of GB300 ro
 # (its summary is under profiles/); None where no capture of the current version
 # exists.  Writes that are still in L2 when a kernel ends are not counted by the capture.
 TRAFFIC = {
-    "attention_sdxl1024_step": 52.56e6,
+    "attention_sdxl1024_step": 52.55e6,
     "conv_sdxl1024_step": 29.40e6,
-    "qkv_proj_sdxl1024_step": 13.01e6,
+    "qkv_proj_sdxl1024_step": 13.02e6,
     "out_proj_sdxl1024_step": 11.33e6,
     "groupnorm_sdxl1024_step": 21.11e6,
-    "refresh_sdxl1024_step": 43.96e6,
-    "attention_sdxl3840": 1012.5e6,
-    "conv_vae_1x256x256x512": 93.7e6,
-    "conv_sdxl3840_latent_step": 265.7e6,
-    "refresh_sweep_200MiB": 684.3e6,
-    "refresh_2x256x256x640_step": 1157.5e6,
-    "groupnorm_2x240x240x640_step": 530.8e6,
+    "refresh_sdxl1024_step": 44.16e6,
+    "attention_sdxl3840": 983.3e6,
+    "conv_vae_1x256x256x512": 93.44e6,
+    "conv_sdxl3840_latent_step": 264.9e6,
+    "refresh_sweep_200MiB": 684.6e6,
+    "refresh_2x256x256x640_step": 1157.3e6,
+    "groupnorm_2x240x240x640_step": 531.1e6,
 }
 WORKLOAD = "sdxl1024_mid_b2_64x64_c640_p4_bf16"
 
