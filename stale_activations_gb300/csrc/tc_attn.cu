@@ -13,9 +13,10 @@
 // U mod G units are shared by all CTAs key tile by key tile ("split" schedule):
 // each CTA takes an equal contiguous run of their (unit, key tile) steps, a unit
 // cut between CTAs leaves one partial result per piece (O/l in fp16, the running
-// maximum m and sum l in fp32); the warpgroup that finishes a unit's last piece
-// (an atomic count per unit and query tile) merges all of them in CTA order, so the
-// result does not depend on which piece finished last.
+// maximum m and sum l in fp32); for each 32-row warp of a query tile, the warp that
+// finishes the unit's last piece (an atomic count per unit, query tile and warp) merges
+// its rows of all of them in CTA order, so the result does not depend on which piece
+// finished last.
 //
 // A CTA's steps run through one pipeline: the next unit's Q is loaded into the second
 // Q buffer while the current unit finishes, and its first S = Q K^T is issued right
@@ -46,16 +47,17 @@
 //                    each), times the (batch, head) power of two, and report V(v) ready
 //                    only once K(v+1) has landed too; the MMA thread waits for this
 //                    before the step's MMAs.  The single MMA thread is the pipeline's
-//                    bottleneck (its P arrives ~1000 cycles before it is free), and each
+//                    bottleneck (each P is ready 700-1000 cycles before it is free), and each
 //                    barrier test or commit it executes delays the next MMA batch; so
 //                    the K wait and the stage release are done by warps with slack.
 // P is rounded to fp16, not bf16: its 11-bit significand keeps the rounding of the
 // probabilities well inside the 2e-3 output tolerance (bf16's 8 bits would not), and
 // V is widened to fp16 so that P V runs as kind::f16 with both operands fp16.  fp16
 // covers [2^-14, 65504] at full precision; V is brought into that range by a power of
-// two 2^e per (batch, head), found by a small pass over the fresh and stale V before
-// the kernel (e = 0 when max|V| lies in [2^-6, 2^15), the usual case), applied in the
-// widening and removed again from O in the epilogue.
+// two 2^e per (batch, head), from max |V| over the fresh and stale V (taken by the
+// kernels that write or read them before this one inside the layer step, by a small pass
+// before the kernel for the standalone calls; e = 0 when max|V| lies in [2^-6, 2^15), the
+// usual case), applied in the widening and removed again from O in the epilogue.
 // Online softmax in the log2 domain with a lazily moved reference maximum: the row
 // maximum of a unit's first key tile is the reference, later tiles are exponentiated
 // against it without a maximum pass, and the reference moves (O and l rescaled, P
